@@ -1,0 +1,426 @@
+#!/usr/bin/env python
+"""Benchmark of the OSCAR hot path on GB300: INT2 paged decode, bs1, 100k context, Qwen3-8B shape.
+
+One step = one decode token through every layer of the model shape: per layer
+one demote (the oldest BF16 recent token is rotated, clipped, quantized and
+packed into an INT2 slot) and one paged decode (query rotation, split-K
+attention over the INT2 history and the BF16 sink/recent segment,
+online-softmax merge, un-rotation). The history length stays fixed from step
+to step: the demoted token lands in a spare slot past the history.
+
+`python bench.py [--gpus N] [--steps K] [--warmup W] [--impl oscar|reference]`
+prints one JSON line. Under torchrun (N > 1) every rank runs its own replica
+of the workload: there is no data-path collective, only the timing barrier.
+"""
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "INT2 paged decode: KV tokens/s and achieved HBM GB/s (bs1, 100k ctx, Qwen3-8B shape)"
+UNIT = "KV tokens/s"
+P = 16
+
+
+# --------------------------------------------------------------------------- distributed helpers
+
+def dist_env():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
+
+
+def max_over_ranks(x, device=None):
+    """Max of a float across ranks (identity without an initialised process group)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device or "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(units_per_rank, world, max_seconds):
+    """Aggregate throughput: the units every rank processed over the slowest rank's time."""
+    return units_per_rank * world / max_seconds
+
+
+def barrier():
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
+
+# --------------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """Samples nvidia-smi SM clocks and throttle reasons every 200 ms while active."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
+                 "-lms", "200", "-f", self.path], stdout=subprocess.DEVNULL, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.3)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        rows = []
+        if self.path and os.path.exists(self.path):
+            for line in open(self.path):
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    rows.append((float(parts[1]), float(parts[2]), parts[5:9]))
+                except ValueError:
+                    continue
+            os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"], "samples": 0}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for _, _, r in rows for i, v in enumerate(r) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": reasons, "samples": len(rows)}
+
+
+# --------------------------------------------------------------------------- workload
+
+def workload_cfg(name):
+    from bit_kv_cache_write_gb300 import synth
+    return dict(synth.WORKLOADS[name])
+
+
+def algorithmic_bytes(cfg, hist, n_bf16, batch=1):
+    """Decode bytes per layer: packed INT2 codes + fp16 scale/zero + BF16 sink/recent (q, out, tables excluded)."""
+    d, g, h = cfg["d"], cfg["group"], cfg["h_kv"]
+    return batch * (hist * h * 2 * (d // 4 + 4 * (d // g)) + n_bf16 * h * 2 * d * 2)
+
+
+def demote_bytes(cfg, n):
+    d, g, h = cfg["d"], cfg["group"], cfg["h_kv"]
+    return n * h * 2 * (d * 2 + d // 4 + 4 * (d // g))
+
+
+class GpuWorkload:
+    """Device-resident caches for every layer, written through the library's own write path."""
+
+    def __init__(self, cfg, layers, dev, seed_offset=0):
+        import numpy as np
+        import torch
+        from bit_kv_cache_write_gb300 import calibration, synth
+        from bit_kv_cache_write_gb300 import oscar as O
+
+        self.cfg, self.layers, self.dev = cfg, layers, dev
+        d, h_kv, h_q, group = cfg["d"], cfg["h_kv"], cfg["h_q"], cfg["group"]
+        self.hist = cfg["hist"]
+        self.n_bf16 = synth.SINK + synth.RECENT
+        self.ctx = O.Oscar(n_layers=layers, n_q_heads=h_q, n_kv_heads=h_kv, head_dim=d, group=group)
+        self.hist_pages = synth.pages_for(self.hist)
+        self.pool_pages = self.hist_pages + 1                 # + one spare page for the demoted token
+        self.bf16_pages = self.n_bf16 // P
+        pb = self.ctx.int2_page_bytes()
+        gen = torch.Generator(device=dev)
+        self.int2_pools, self.bf16_pools, self.tables, self.bf16_tables, self.qs = [], [], [], [], []
+        chunk = 16384
+        for layer in range(layers):
+            li = synth.LayerInputs(cfg, layer + seed_offset)
+            q_cal, k_cal, v_cal = li.calibration()
+            rk, rv, tk, tv = calibration.calibrate_layer(q_cal, k_cal, v_cal, d ** -0.5, cfg["clip_ratio"])
+            self.ctx.calibrate_upload(layer, rk, rv, tk, tv)
+            perm = synth.page_permutation(li.seed, "int2", self.hist_pages)
+            table = torch.from_numpy(np.append(perm, self.hist_pages).astype(np.int32)).to(dev).view(1, -1)
+            pool = torch.zeros(self.pool_pages * pb, dtype=torch.uint8, device=dev)
+            gen.manual_seed(li.seed)
+            km = torch.from_numpy(li.k_prof.mult).to(dev)
+            vm = torch.from_numpy(li.v_prof.mult).to(dev)
+            for t0 in range(0, self.hist, chunk):
+                n = min(chunk, self.hist - t0)
+                k = (torch.randn(n, h_kv, d, generator=gen, device=dev) * km).to(torch.bfloat16)
+                v = (torch.randn(n, h_kv, d, generator=gen, device=dev) * vm).to(torch.bfloat16)
+                t = torch.arange(t0, t0 + n, device=dev)
+                slots = table[0, t // P].to(torch.int64) * P + t % P
+                self.ctx.write_tokens(layer, k, v, slots, pool)
+            bf = torch.randn(self.bf16_pages, h_kv, 2, P, d, generator=gen, device=dev)
+            bf = bf * torch.stack([km, vm], dim=1)[None, :, :, None, :]
+            self.bf16_pools.append(bf.to(torch.bfloat16).contiguous())
+            self.bf16_tables.append(torch.arange(self.bf16_pages, dtype=torch.int32, device=dev).view(1, -1))
+            self.int2_pools.append(pool)
+            self.tables.append(table)
+            self.qs.append(torch.randn(1, h_q, d, generator=gen, device=dev).to(torch.bfloat16))
+        self.hist_len = torch.tensor([self.hist], dtype=torch.int32, device=dev)
+        self.bf16_len = torch.tensor([self.n_bf16], dtype=torch.int32, device=dev)
+        self.src = torch.tensor([synth.SINK * 1], dtype=torch.int64, device=dev)          # oldest recent token
+        self.dst = torch.tensor([self.hist_pages * P], dtype=torch.int64, device=dev)     # spare INT2 slot
+        self.ws = torch.empty(self.ctx.decode_workspace_size(1, self.hist), dtype=torch.uint8, device=dev)
+        self.out = torch.empty(layers, 1, h_q, d, dtype=torch.float32, device=dev)
+        self.q_all = torch.cat(self.qs, 0).view(layers, 1, h_q, d).contiguous()
+        torch.cuda.synchronize()
+
+    def step(self):
+        for layer in range(self.layers):
+            self.ctx.demote_recent(layer, self.bf16_pools[layer], self.src, self.int2_pools[layer], self.dst)
+            self.ctx.decode(layer, self.q_all[layer], self.int2_pools[layer], self.tables[layer], self.hist_len,
+                            self.hist, self.bf16_pools[layer], self.bf16_tables[layer], self.bf16_len,
+                            self.out[layer], self.ws)
+
+    launches_per_step_per_layer = 4     # write (demote), q rotation, split, merge
+
+
+def kernel_traffic(kernel, workload):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on the current kernel source."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    rec = json.load(open(path)).get("%s/%s" % (kernel, workload))
+    if not rec:
+        return None
+    src = os.path.join(ROOT, "bit_kv_cache_write_gb300", "csrc", rec["source"])
+    if not os.path.exists(src) or hashlib.sha256(open(src, "rb").read()).hexdigest()[:16] != rec["source_sha"]:
+        return None
+    return rec["bytes_per_launch"]
+
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        return float(json.load(open(path))["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+# --------------------------------------------------------------------------- CPU oracle baseline
+
+def oracle_sample(cfg, sample_hist, layer=0):
+    """Build the oracle-side cache for a bounded sample (one layer, ``sample_hist`` history tokens)."""
+    import numpy as np
+    sys.path.insert(0, os.path.join(ROOT, "tests"))
+    import cases
+    from bit_kv_cache_write_gb300 import synth
+    c = dict(cfg)
+    c["hist"] = sample_hist
+    case = cases.DecodeCase(c, [sample_hist], [synth.SINK + synth.RECENT], layer=layer, extra_pages=1)
+    return case
+
+
+def time_oracle_step(case):
+    """One oracle pass of the hot path on the sample: demote one BF16 token, then decode every head."""
+    import numpy as np
+    from oracle import cache
+    geo = case.geo
+    spare = np.zeros(geo.page_bytes, np.uint8)
+    t0 = time.perf_counter()
+    cache.demote(case.bf16_pool, spare, geo, [synth_sink()], [0], case.rk, case.rv, case.tk, case.tv)
+    case.oracle_out()
+    return time.perf_counter() - t0
+
+
+def synth_sink():
+    from bit_kv_cache_write_gb300 import synth
+    return synth.SINK
+
+
+def cpu_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count()
+
+
+def run_reference(args, cfg, world, rank):
+    """--impl reference: the fp64 CPU oracle timed on the host cores, on a bounded sample of the workload."""
+    if rank != 0:
+        return 0
+    sample_hist = args.oracle_hist
+    case = oracle_sample(cfg, sample_hist)
+    tokens = sample_hist + case.bf16_lens[0]
+    for _ in range(args.warmup):
+        time_oracle_step(case)
+    times = [time_oracle_step(case) for _ in range(args.steps)]
+    total = sum(times)
+    value = tokens * args.steps / total
+    sample = "1 layer, %d INT2 + %d BF16 tokens, %d Q / %d KV heads, d=%d, G=%d; demote 1 token + decode" % (
+        sample_hist, case.bf16_lens[0], cfg["h_q"], cfg["h_kv"], cfg["d"], cfg["group"])
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": args.workload, "batch": 1, "context": cfg["hist"] + 320,
+                       "note": "each step is a bounded sample of the workload"},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+    return 0
+
+
+# --------------------------------------------------------------------------- main
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["oscar", "reference"], default="oscar")
+    ap.add_argument("--workload", default="qwen3_8b_bs1_100k")
+    ap.add_argument("--layers", type=int, default=0, help="override the layer count (0: the workload's)")
+    ap.add_argument("--oracle-hist", type=int, default=24_992, help="INT2 tokens in the oracle's bounded sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)
+
+    rank, world, local = dist_env()
+    cfg = workload_cfg(args.workload)
+    if args.impl == "reference":
+        return run_reference(args, cfg, world, rank)
+
+    import torch
+    import torch.distributed as dist
+    if world > 1:
+        dist.init_process_group("nccl", init_method="env://")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    import __graft_entry__
+    __graft_entry__.build()
+    from bit_kv_cache_write_gb300 import oscar as O
+
+    layers = args.layers or cfg["layers"]
+    wl = GpuWorkload(cfg, layers, dev, seed_offset=1000 * rank)
+    stream = torch.cuda.current_stream()
+
+    # ---- capture one step in a CUDA graph (the library launches on the capturing stream)
+    wl.step()
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        wl.step()
+    for _ in range(args.warmup):
+        graph.replay()
+    torch.cuda.synchronize()
+
+    # ---- timed region: K graph replays; inputs (2.1 GB of pages over the layers) exceed L2
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clocks:
+        barrier()
+        torch.cuda.synchronize()
+        start.record(stream)
+        for _ in range(args.steps):
+            graph.replay()
+        stop.record(stream)
+        torch.cuda.synchronize()
+        barrier()
+    sec = start.elapsed_time(stop) / 1e3
+    max_sec = max_over_ranks(sec, dev)
+    tokens_per_step = layers * (wl.hist + wl.n_bf16)
+    value = whole_job_rate(tokens_per_step * args.steps, world, max_sec)
+    ms_per_step = 1e3 * max_sec / args.steps
+    step_bytes = layers * (algorithmic_bytes(cfg, wl.hist, wl.n_bf16) + demote_bytes(cfg, 1))
+
+    # ---- per-kernel durations (same launches, eager, events around each kernel on its stream)
+    wl.ctx.profile_enable(True)
+    for _ in range(args.steps):
+        wl.step()
+    torch.cuda.synchronize()
+    wl.ctx.profile_enable(False)
+    kt = {}
+    for name, kid in (("write", O.OSCAR_KERNEL_WRITE), ("q_rotate", O.OSCAR_KERNEL_QROT),
+                      ("split", O.OSCAR_KERNEL_SPLIT), ("merge", O.OSCAR_KERNEL_MERGE)):
+        ms, n = wl.ctx.profile_read(kid)
+        kt[name] = {"launches": n, "avg_us": 1e3 * ms / max(n, 1)}
+    split_bytes = algorithmic_bytes(cfg, wl.hist, wl.n_bf16)
+    achieved = split_bytes / (kt["split"]["avg_us"] * 1e-6) / 1e9
+    peak, peak_kind = measured_peak()
+
+    # ---- end to end through the public API with host buffers: q in (pinned H2D), outputs out (D2H)
+    q_host = wl.q_all.cpu().pin_memory()
+    out_host = torch.empty(wl.out.shape, dtype=torch.float32).pin_memory()
+    for _ in range(2):
+        wl.q_all.copy_(q_host, non_blocking=True)
+        graph.replay()
+        out_host.copy_(wl.out, non_blocking=True)
+    torch.cuda.synchronize()
+    barrier()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        wl.q_all.copy_(q_host, non_blocking=True)
+        graph.replay()
+        out_host.copy_(wl.out, non_blocking=True)
+        stream.synchronize()
+    e2e_sec = max_over_ranks(time.perf_counter() - t0, dev)
+    e2e_value = whole_job_rate(tokens_per_step * args.steps, world, e2e_sec)
+
+    # ---- CPU oracle baseline (rank 0, N = 1 only), bounded sample
+    cpu_baseline = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        case = oracle_sample(cfg, args.oracle_hist)
+        time_oracle_step(case)
+        reps, spent = 0, 0.0
+        while spent < 10.0 and reps < 50:
+            spent += time_oracle_step(case)
+            reps += 1
+        tok = args.oracle_hist + case.bf16_lens[0]
+        cpu_baseline = {"value": tok * reps / spent, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
+                        "sample": "%d oracle steps on 1 layer with %d INT2 + %d BF16 tokens (demote 1 token + "
+                                  "decode all %d query heads), fp64 NumPy" % (reps, args.oracle_hist,
+                                                                              case.bf16_lens[0], cfg["h_q"])}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": args.workload, "batch": 1, "context": wl.hist + wl.n_bf16, "int2_history": wl.hist,
+                       "bf16_tokens": wl.n_bf16, "layers": layers, "h_q": cfg["h_q"], "h_kv": cfg["h_kv"],
+                       "head_dim": cfg["d"], "group": cfg["group"], "page_size": P,
+                       "step": "per layer: demote 1 token + decode; one CUDA graph per step",
+                       "l2": "inputs larger than L2: %.2f GB of distinct pages per step" % (step_bytes / 1e9),
+                       "parallelism": "replicas" if world > 1 else "single GPU"},
+            "hbm_gbs_step": step_bytes * args.steps * world / max_sec / 1e9,
+            "us_per_layer": 1e6 * max_sec / args.steps / layers,
+            "roofline": {"bound": "hbm", "kernel": "split (INT2 history + BF16 segment)", "achieved": achieved,
+                         "peak": peak, "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / peak,
+                         "traffic": kernel_traffic("split", args.workload),
+                         "algorithmic_bytes_per_launch": split_bytes},
+            "kernels": kt,
+            "clocks": clocks.summary(),
+            "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": q_host.numel() * 2,
+                    "d2h_bytes_per_step": out_host.numel() * 4},
+            "gpu_launches": args.steps * layers * GpuWorkload.launches_per_step_per_layer,
+            "cpu_baseline": cpu_baseline,
+        }
+        print(json.dumps(line))
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,123 @@
+// Internal declarations shared by the host API and the kernel translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cstdint>
+#include <vector>
+
+#include "../../include/oscar.h"
+
+namespace oscar {
+
+constexpr int kPage = 16;
+constexpr int kMaxBf16 = 512;     // sink + recent upper bound
+constexpr float kLog2e = 1.4426950408889634f;
+
+// Per-layer device parameters. All pointers index into one allocation.
+struct LayerParams {
+    const float* r_k;      // [H_kv][d][d]
+    const float* r_v;      // [H_kv][d][d]
+    const float* r_vt;     // [H_kv][d][d], r_vt[h][i][c] = r_v[h][c][i]
+    const float* t_k;      // [H_kv][d]
+    const float* t_v;      // [H_kv][d]
+};
+
+struct Shape {
+    int h_q, h_kv, d, group, page, sink, recent;
+    float sm_scale;
+    int debug;
+};
+
+// Opt-in launch timing: event pairs on the launching stream, per kernel class.
+struct Profiler {
+    bool on = false;
+    std::vector<std::pair<cudaEvent_t, cudaEvent_t>> pending[OSCAR_KERNEL_COUNT];
+};
+
+// Records a start event at construction and a stop event at stop() on `st`.
+class ProfScope {
+  public:
+    ProfScope(Profiler* p, int kernel, cudaStream_t st) : p_(p && p->on ? p : nullptr), k_(kernel), st_(st) {
+        if (p_ && cudaEventCreate(&a_) == cudaSuccess && cudaEventCreate(&b_) == cudaSuccess)
+            cudaEventRecord(a_, st_);
+        else
+            p_ = nullptr;
+    }
+    void stop() {
+        if (!p_) return;
+        cudaEventRecord(b_, st_);
+        p_->pending[k_].push_back({a_, b_});
+        p_ = nullptr;
+    }
+    ~ProfScope() { stop(); }
+
+  private:
+    Profiler* p_;
+    int k_;
+    cudaStream_t st_;
+    cudaEvent_t a_ = nullptr, b_ = nullptr;
+};
+
+// Device error word: {kind, pad, index}.
+struct DebugWord {
+    int kind;
+    int pad;
+    long long index;
+};
+
+}  // namespace oscar
+
+struct oscar_ctx {
+    oscar_config_t cfg;
+    oscar::Shape shape;
+    int device;
+    int num_sms;
+    float* params;                 // all layers' parameters
+    size_t params_floats;
+    std::vector<char> calibrated;  // per layer
+    oscar::DebugWord* dbg;         // device error word
+    oscar::Profiler prof;
+};
+
+namespace oscar {
+
+LayerParams layer_params(const oscar_ctx* ctx, int layer);
+
+// ---- write path (write_kernels.cu)
+cudaError_t launch_write(const Shape& s, const LayerParams& p, int num_sms,
+                         const void* k, const void* v, const int64_t* slots, int n,
+                         const void* bf16_pool, int64_t bf16_pages, const int64_t* src_slots,
+                         void* int2_pool, int64_t int2_pages, DebugWord* dbg, Profiler* prof, cudaStream_t st);
+
+cudaError_t launch_transpose(const float* src, float* dst, int h, int d, cudaStream_t st);
+
+// ---- decode path (decode_kernels.cu)
+struct DecodePlan {
+    int int2_splits;        // splits over the INT2 history
+    int pages_per_split;    // INT2 pages per split
+    int bf16_splits;        // splits over the BF16 segment (0 if the segment is empty by config)
+    int total_splits;
+    size_t ws_partials;     // bytes of split partials
+    size_t ws_qrot;         // bytes of rotated queries
+    size_t ws_total;
+};
+
+DecodePlan plan_decode(const Shape& s, int num_sms, int batch, int max_hist);
+
+struct DecodeArgs {
+    const void* q;
+    const uint8_t* int2_pool; int64_t int2_pages;
+    const int32_t* int2_tables; int int2_stride;
+    const int32_t* hist_len; int max_hist;
+    const uint16_t* bf16_pool; int64_t bf16_pages;
+    const int32_t* bf16_tables; int bf16_stride;
+    const int32_t* bf16_len;
+    float* out;
+    void* ws;
+    int batch;
+};
+
+cudaError_t launch_decode(const Shape& s, const LayerParams& p, const DecodePlan& plan,
+                          const DecodeArgs& a, DebugWord* dbg, Profiler* prof, cudaStream_t st);
+
+}  // namespace oscar

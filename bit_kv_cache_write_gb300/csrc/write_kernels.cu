@@ -1,0 +1,252 @@
+// Write / demote kernel on CUDA cores: rotate -> clip -> group scale/zero ->
+// 2-bit quantize -> pack into the paged INT2 cache.
+//
+// Method: QbitAI article on OSCAR, serving-pipeline part. The demoted token is
+// rotated, clipped, quantized and packed, four codes per byte, with a scale and
+// zero point per group. R and the clip thresholds are the fixed per-layer
+// calibration (section "OSCAR aligns the rotation with attention"; arXiv
+// 2605.17757 abstracts).
+//
+// One CTA owns one (KV head, K|V) pair and a contiguous range of tokens, and
+// keeps that pair's R (d x d fp32) in shared memory. Each warp rotates kTok
+// tokens at a time: lane l produces rotated channels [CPL*l, CPL*l + CPL). That
+// keeps a quantization group on an aligned run of G/CPL lanes, so group min/max
+// is a butterfly shuffle. Codes are packed with one warp OR-reduction per 32-bit
+// word of the row.
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cfloat>
+
+#include "layout.cuh"
+#include "oscar_internal.h"
+
+namespace oscar {
+namespace {
+
+constexpr int kWarps = 4;
+constexpr int kTok = 8;      // tokens per warp iteration (register blocking over R)
+
+template <int D, int G>
+__global__ void __launch_bounds__(kWarps * 32)
+write_kernel(const float* __restrict__ r_all, const float* __restrict__ t_all,
+             const __nv_bfloat16* __restrict__ k_in, const __nv_bfloat16* __restrict__ v_in,
+             const int64_t* __restrict__ dst_slots, int n, int h_kv,
+             const __nv_bfloat16* __restrict__ bf16_pool, int64_t bf16_pages,
+             const int64_t* __restrict__ src_slots,
+             uint8_t* __restrict__ int2_pool, int64_t int2_pages,
+             int debug, DebugWord* dbg) {
+    constexpr int CPL = D / 32;             // rotated channels per lane
+    constexpr int LPG = G / CPL;            // lanes per group
+    constexpr int WORDS = D / 16;           // 32-bit words per code row
+    using GE = Geo<D, G>;
+
+    extern __shared__ __align__(16) float smem[];
+    float* r_s = smem;                                  // [D][D]
+    float* x_s = smem + D * D;                          // [kWarps][kTok][D]
+
+    const int head = blockIdx.y;
+    const int kind = blockIdx.z;                        // 0 = K, 1 = V
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+
+    const float* r_g = r_all + ((size_t)kind * h_kv + head) * D * D;
+    for (int i = threadIdx.x; i < D * D / 4; i += blockDim.x)
+        reinterpret_cast<float4*>(r_s)[i] = __ldg(reinterpret_cast<const float4*>(r_g) + i);
+
+    float thr[CPL];
+    const float* t_g = t_all + ((size_t)kind * h_kv + head) * D;
+#pragma unroll
+    for (int j = 0; j < CPL; ++j) thr[j] = __ldg(t_g + CPL * lane + j);
+
+    // bit offset of each of this lane's channels inside the packed row
+    int off[CPL];
+#pragma unroll
+    for (int j = 0; j < CPL; ++j) {
+        const int c = CPL * lane + j;
+        off[j] = kind == 0 ? k_bit_offset(c, D) : v_bit_offset(c, D);
+    }
+    __syncthreads();
+
+    const int per_cta = (n + gridDim.x - 1) / gridDim.x;
+    const int t_begin = blockIdx.x * per_cta;
+    const int t_end = min(n, t_begin + per_cta);
+    float* xw = x_s + warp * kTok * D;
+
+    for (int base = t_begin + warp * kTok; base < t_end; base += kWarps * kTok) {
+        const int cnt = min(kTok, t_end - base);
+        // stage the kTok input rows (bf16 -> fp32) in this warp's smem tile
+        for (int t = 0; t < kTok; ++t) {
+            const __nv_bfloat16* src = nullptr;
+            if (t < cnt) {
+                const int tok = base + t;
+                if (src_slots) {
+                    const int64_t s = src_slots[tok];
+                    const int64_t pg = s / kPage;
+                    if (debug && (s < 0 || pg >= bf16_pages)) {
+                        if (lane == 0) record_error(&dbg->kind, &dbg->index, 1, s);
+                    } else {
+                        src = bf16_pool + ((((size_t)pg * h_kv + head) * 2 + kind) * kPage + (s % kPage)) * D;
+                    }
+                } else {
+                    src = (kind == 0 ? k_in : v_in) + ((size_t)tok * h_kv + head) * D;
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < CPL; ++j)
+                xw[t * D + lane + 32 * j] = src ? __bfloat162float(src[lane + 32 * j]) : 0.0f;
+        }
+        __syncwarp();
+
+        float acc[kTok][CPL];
+#pragma unroll
+        for (int t = 0; t < kTok; ++t)
+#pragma unroll
+            for (int j = 0; j < CPL; ++j) acc[t][j] = 0.0f;
+
+#pragma unroll 4
+        for (int i = 0; i < D; ++i) {
+            float rv[CPL];
+            if constexpr (CPL == 4) {
+                const float4 r4 = *reinterpret_cast<const float4*>(r_s + i * D + 4 * lane);
+                rv[0] = r4.x; rv[1] = r4.y; rv[2] = r4.z; rv[3] = r4.w;
+            } else {
+                const float2 r2 = *reinterpret_cast<const float2*>(r_s + i * D + 2 * lane);
+                rv[0] = r2.x; rv[1] = r2.y;
+            }
+#pragma unroll
+            for (int t = 0; t < kTok; ++t) {
+                const float xv = xw[t * D + i];
+#pragma unroll
+                for (int j = 0; j < CPL; ++j) acc[t][j] = fmaf(xv, rv[j], acc[t][j]);
+            }
+        }
+
+#pragma unroll 1
+        for (int t = 0; t < cnt; ++t) {
+            const int tok = base + t;
+            const int64_t slot = dst_slots[tok];
+            const int64_t pg = slot / kPage;
+            bool ok = !(slot < 0 || pg >= int2_pages);
+            if (!ok && debug && lane == 0) record_error(&dbg->kind, &dbg->index, 1, slot);
+            if (src_slots && debug) {
+                const int64_t s = src_slots[tok];
+                if (s < 0 || s / kPage >= bf16_pages) ok = false;
+            }
+            if (!ok) continue;   // warp-uniform
+
+            float xh[CPL];
+            float mn = FLT_MAX, mx = -FLT_MAX;
+#pragma unroll
+            for (int j = 0; j < CPL; ++j) {
+                xh[j] = fminf(fmaxf(acc[t][j], -thr[j]), thr[j]);
+                mn = fminf(mn, xh[j]);
+                mx = fmaxf(mx, xh[j]);
+            }
+#pragma unroll
+            for (int o = 1; o < LPG; o <<= 1) {
+                mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+            }
+            const float rng = __fsub_rn(mx, mn);
+            const bool degenerate = !(rng >= FLT_MIN);
+            const float inv = __fdiv_rn(3.0f, degenerate ? 1.0f : rng);
+
+            uint32_t contrib[WORDS];
+#pragma unroll
+            for (int w = 0; w < WORDS; ++w) contrib[w] = 0u;
+#pragma unroll
+            for (int j = 0; j < CPL; ++j) {
+                const float u = __fmul_rn(__fsub_rn(xh[j], mn), inv);
+                int code = degenerate ? 0 : (int)rintf(u);
+                code = min(max(code, 0), 3);
+#pragma unroll
+                for (int w = 0; w < WORDS; ++w)
+                    if ((off[j] >> 5) == w) contrib[w] |= (uint32_t)code << (off[j] & 31);
+            }
+            uint32_t mine = 0u;
+#pragma unroll
+            for (int w = 0; w < WORDS; ++w) {
+                const uint32_t r = __reduce_or_sync(0xffffffffu, contrib[w]);
+                if (lane == w) mine = r;
+            }
+            uint8_t* seg = int2_pool + ((size_t)pg * h_kv + head) * GE::kBlock + (size_t)kind * GE::kSeg;
+            const int row = (int)(slot % kPage);
+            if (lane < WORDS)
+                reinterpret_cast<uint32_t*>(seg + row * GE::kCodeRow)[lane] = mine;
+            if (lane % LPG == 0) {
+                const int grp = lane / LPG;
+                __half2 sz;
+                sz.x = __float2half_rn(__fdiv_rn(rng, 3.0f));
+                sz.y = __float2half_rn(mn);
+                reinterpret_cast<__half2*>(seg + GE::kCodeBytes)[row * GE::kGroups + grp] = sz;
+            }
+        }
+        __syncwarp();
+    }
+}
+
+template <int D, int G>
+cudaError_t launch_write_t(const Shape& s, const LayerParams& p, int num_sms,
+                           const void* k, const void* v, const int64_t* slots, int n,
+                           const void* bf16_pool, int64_t bf16_pages, const int64_t* src_slots,
+                           void* int2_pool, int64_t int2_pages, DebugWord* dbg, Profiler* prof,
+                           cudaStream_t st) {
+    const size_t smem = (size_t)(D * D + kWarps * kTok * D) * sizeof(float);
+    auto kern = write_kernel<D, G>;
+    // Opt in to the large dynamic shared memory once per process (outside any stream capture:
+    // the first call of a shape happens before a caller can capture it).
+    static cudaError_t attr = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (attr != cudaSuccess) return attr;
+    // K and V rotations/thresholds sit back to back: r_k then r_v, t_k then t_v.
+    const int pairs = s.h_kv * 2;
+    const int want_ctas = 2 * num_sms;
+    int gx = (want_ctas + pairs - 1) / pairs;
+    const int max_gx = (n + kWarps * kTok - 1) / (kWarps * kTok);
+    gx = gx < 1 ? 1 : (gx > max_gx ? max_gx : gx);
+    dim3 grid(gx, s.h_kv, 2);
+    ProfScope ps(prof, OSCAR_KERNEL_WRITE, st);
+    kern<<<grid, kWarps * 32, smem, st>>>(
+        p.r_k, p.t_k, static_cast<const __nv_bfloat16*>(k), static_cast<const __nv_bfloat16*>(v),
+        slots, n, s.h_kv, static_cast<const __nv_bfloat16*>(bf16_pool), bf16_pages, src_slots,
+        static_cast<uint8_t*>(int2_pool), int2_pages, s.debug, dbg);
+    return cudaGetLastError();
+}
+
+__global__ void transpose_kernel(const float* __restrict__ src, float* __restrict__ dst, int d) {
+    __shared__ float tile[32][33];
+    const size_t mat = (size_t)blockIdx.z * d * d;
+    const int bx = blockIdx.x * 32, by = blockIdx.y * 32;
+    for (int j = threadIdx.y; j < 32; j += blockDim.y)
+        tile[j][threadIdx.x] = src[mat + (size_t)(by + j) * d + bx + threadIdx.x];
+    __syncthreads();
+    for (int j = threadIdx.y; j < 32; j += blockDim.y)
+        dst[mat + (size_t)(bx + j) * d + by + threadIdx.x] = tile[threadIdx.x][j];
+}
+
+}  // namespace
+
+cudaError_t launch_write(const Shape& s, const LayerParams& p, int num_sms,
+                         const void* k, const void* v, const int64_t* slots, int n,
+                         const void* bf16_pool, int64_t bf16_pages, const int64_t* src_slots,
+                         void* int2_pool, int64_t int2_pages, DebugWord* dbg, Profiler* prof,
+                         cudaStream_t st) {
+#define OSCAR_WRITE_CASE(D_, G_)                                                              \
+    if (s.d == D_ && s.group == G_)                                                           \
+        return launch_write_t<D_, G_>(s, p, num_sms, k, v, slots, n, bf16_pool, bf16_pages,   \
+                                      src_slots, int2_pool, int2_pages, dbg, prof, st);
+    OSCAR_WRITE_CASE(64, 32)
+    OSCAR_WRITE_CASE(64, 64)
+    OSCAR_WRITE_CASE(128, 32)
+    OSCAR_WRITE_CASE(128, 64)
+    OSCAR_WRITE_CASE(128, 128)
+#undef OSCAR_WRITE_CASE
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_transpose(const float* src, float* dst, int h, int d, cudaStream_t st) {
+    dim3 grid(d / 32, d / 32, h);
+    transpose_kernel<<<grid, dim3(32, 8), 0, st>>>(src, dst, d);
+    return cudaGetLastError();
+}
+
+}  // namespace oscar

@@ -72,6 +72,8 @@ def decode_one(q, r_k, r_v, k_deq, v_deq, k_bf, v_bf, sm_scale):
     lg_int2 = sm_scale * (np.asarray(k_deq, dtype=np.float64) @ q_rot)
     lg_bf = sm_scale * (np.asarray(k_bf, dtype=np.float64) @ q)
     logits = np.concatenate([lg_bf, lg_int2])
+    if logits.size == 0:                      # no cached token at all: defined as zeros
+        return np.zeros(q.shape[0])
     m = logits.max()
     e = np.exp(logits - m)
     p = e / e.sum()

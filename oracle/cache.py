@@ -11,18 +11,20 @@ import numpy as np
 from . import attention, layout, quantize
 
 
-def write_tokens(pool, geo, k, v, slots, r_k, r_v, t_k, t_v):
+def write_tokens(pool, geo, k, v, slots, r_k, r_v, t_k, t_v, keep=True):
     """Quantize k, v [n, H_kv, d] into the INT2 pool at ``slots`` [n].
 
-    Returns {"k": [per-head quantize dicts], "v": [...]} for tolerance checks.
+    Returns {"k": [per-head quantize dicts], "v": [...]} for tolerance checks
+    (or None with keep=False, which holds one head's intermediates at a time).
     """
     info = {"k": [], "v": []}
     for kind, x, r, t in (("k", k, r_k, t_k), ("v", v, r_v, t_v)):
         for h in range(geo.h_kv):
             q = quantize.quantize(np.asarray(x[:, h, :], dtype=np.float64), r[h], t[h], geo.group)
-            info[kind].append(q)
             layout.write_int2_rows(pool, geo, slots, h, kind, q["codes"], q["scale"], q["zero"])
-    return info
+            if keep:
+                info[kind].append(q)
+    return info if keep else None
 
 
 def demote(bf16_pool, int2_pool, geo, src_slots, dst_slots, r_k, r_v, t_k, t_v):
@@ -42,20 +44,29 @@ def demote(bf16_pool, int2_pool, geo, src_slots, dst_slots, r_k, r_v, t_k, t_v):
 
 
 def decode_batch(q, int2_pool, geo, int2_tables, hist_len, bf16_pool, bf16_tables, bf16_len,
-                 r_k, r_v, sm_scale, seqs=None):
-    """Decode outputs [B, H_q, d] (fp64) for the given batch (or only ``seqs``)."""
+                 r_k, r_v, sm_scale, seqs=None, heads=None):
+    """Decode outputs [B, H_q, d] (fp64) for the given batch (or only ``seqs`` / query ``heads``).
+
+    Works one (sequence, KV head) at a time so full-length histories fit in host memory.
+    """
     b_total, h_q, d = q.shape
+    g = h_q // geo.h_kv
     out = np.zeros((b_total, h_q, d))
     todo = range(b_total) if seqs is None else seqs
+    want = set(range(h_q)) if heads is None else set(heads)
     for b in todo:
-        kd, vd, kb, vb = [], [], [], []
-        for h in range(geo.h_kv):
-            ck, sk, zk = layout.read_int2_sequence(int2_pool, geo, int2_tables[b], int(hist_len[b]), h, "k")
-            cv, sv, zv = layout.read_int2_sequence(int2_pool, geo, int2_tables[b], int(hist_len[b]), h, "v")
-            kd.append(quantize.dequantize(ck, sk, zk, geo.group))
-            vd.append(quantize.dequantize(cv, sv, zv, geo.group))
-            kb.append(layout.read_bf16_sequence(bf16_pool, bf16_tables[b], int(bf16_len[b]), h, "k", d, geo.h_kv, geo.page))
-            vb.append(layout.read_bf16_sequence(bf16_pool, bf16_tables[b], int(bf16_len[b]), h, "v", d, geo.h_kv, geo.page))
-        out[b] = attention.decode_heads(np.asarray(q[b], dtype=np.float64), r_k, r_v,
-                                        kd, vd, kb, vb, sm_scale)
+        for kv in range(geo.h_kv):
+            hs = [h for h in range(kv * g, (kv + 1) * g) if h in want]
+            if not hs:
+                continue
+            n_hist, n_bf = int(hist_len[b]), int(bf16_len[b])
+            ck, sk, zk = layout.read_int2_sequence(int2_pool, geo, int2_tables[b], n_hist, kv, "k")
+            cv, sv, zv = layout.read_int2_sequence(int2_pool, geo, int2_tables[b], n_hist, kv, "v")
+            kd = quantize.dequantize(ck, sk, zk, geo.group)
+            vd = quantize.dequantize(cv, sv, zv, geo.group)
+            kb = layout.read_bf16_sequence(bf16_pool, bf16_tables[b], n_bf, kv, "k", d, geo.h_kv, geo.page)
+            vb = layout.read_bf16_sequence(bf16_pool, bf16_tables[b], n_bf, kv, "v", d, geo.h_kv, geo.page)
+            for h in hs:
+                out[b, h] = attention.decode_one(np.asarray(q[b, h], dtype=np.float64), r_k[kv], r_v[kv],
+                                                 kd, vd, kb, vb, sm_scale)
     return out

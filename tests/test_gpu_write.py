@@ -1,0 +1,163 @@
+"""GPU parity of the write and demote paths (through the C ABI) against the oracle.
+
+Bar: packed codes bit-exact except off-by-one codes whose oracle ratio lies
+within 1e-5 of a rounding boundary; scale and zero within 1 fp16 ulp; no byte
+outside the written rows changes.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import cases
+from bit_kv_cache_write_gb300 import oscar as O
+from bit_kv_cache_write_gb300 import synth
+from oracle import cache, layout, quantize
+
+pytestmark = pytest.mark.gpu
+P = 16
+
+
+def make_ctx(cfg, debug=0, layers=1):
+    return O.Oscar(n_layers=layers, n_q_heads=cfg["h_q"], n_kv_heads=cfg["h_kv"], head_dim=cfg["d"],
+                   group=cfg["group"], debug_bounds=debug)
+
+
+def bf16(a, dev):
+    return torch.from_numpy(np.ascontiguousarray(a, np.float32)).to(dev).to(torch.bfloat16)
+
+
+WRITE_CASES = [
+    ("tiny", {}, 1000),
+    ("tiny", dict(group=64), 257),
+    ("qwen3_8b_bs1_100k", {}, 777),
+    ("qwen3_4b_b64_32k", {}, 1024),
+    ("qwen3_8b_bs1_100k", dict(group=32), 333),
+    ("qwen3_8b_bs1_100k", dict(group=64, h_kv=2, h_q=4), 5),
+    ("tiny", {}, 1),
+]
+
+
+@pytest.mark.parametrize("name,over,n", WRITE_CASES, ids=lambda x: str(x))
+def test_write_tokens_parity(cuda, name, over, n):
+    cfg = cases.workload(name, **over)
+    li, (rk, rv, tk, tv) = cases.calibration(cfg)
+    geo = layout.Int2Geometry(cfg["d"], cfg["group"], cfg["h_kv"])
+    n_pages = synth.pages_for(n) + 5
+    slots = synth.rng_for(li.seed, "slots").permutation(n_pages * P)[:n].astype(np.int64)
+    k, v = li.kv("write", n)
+    ref = np.zeros(n_pages * geo.page_bytes, np.uint8)
+    info = cache.write_tokens(ref, geo, k, v, slots, rk, rv, tk, tv)
+
+    ctx = make_ctx(cfg)
+    ctx.calibrate_upload(0, rk, rv, tk, tv)
+    assert ctx.int2_page_bytes() == geo.page_bytes
+    pool = torch.zeros(n_pages * geo.page_bytes, dtype=torch.uint8, device=cuda)
+    ctx.write_tokens(0, bf16(k, cuda), bf16(v, cuda), torch.from_numpy(slots).to(cuda), pool)
+    torch.cuda.synchronize()
+    flips = cases.compare_int2(pool.cpu().numpy(), ref, geo, slots, info)
+    print("tolerated boundary flips:", flips)
+
+
+def test_write_twice_is_idempotent_and_n0_is_noop(cuda):
+    cfg = cases.workload("tiny")
+    li, (rk, rv, tk, tv) = cases.calibration(cfg)
+    geo = layout.Int2Geometry(cfg["d"], cfg["group"], cfg["h_kv"])
+    k, v = li.kv("twice", 40)
+    slots = torch.arange(7, 47, dtype=torch.int64, device=cuda)
+    ctx = make_ctx(cfg)
+    ctx.calibrate_upload(0, rk, rv, tk, tv)
+    pool = torch.zeros(4 * geo.page_bytes, dtype=torch.uint8, device=cuda)
+    ctx.write_tokens(0, bf16(k, cuda), bf16(v, cuda), slots, pool)
+    first = pool.clone()
+    ctx.write_tokens(0, bf16(k, cuda), bf16(v, cuda), slots, pool)
+    ctx.write_tokens(0, bf16(k[:0], cuda), bf16(v[:0], cuda), slots[:0], pool)
+    torch.cuda.synchronize()
+    assert torch.equal(first, pool)
+
+
+@pytest.mark.parametrize("name,n", [("tiny", 300), ("qwen3_8b_bs1_100k", 256)])
+def test_demote_parity(cuda, name, n):
+    cfg = cases.workload(name)
+    li, (rk, rv, tk, tv) = cases.calibration(cfg)
+    d, h_kv = cfg["d"], cfg["h_kv"]
+    geo = layout.Int2Geometry(d, cfg["group"], h_kv)
+    r = synth.rng_for(li.seed, "demote")
+    bf_pages = synth.pages_for(n) + 3
+    src = r.permutation(bf_pages * P)[:n].astype(np.int64)
+    i2_pages = synth.pages_for(n) + 2
+    dst = r.permutation(i2_pages * P)[:n].astype(np.int64)
+    k, v = li.kv("recent", bf_pages * P)
+    bf_pool = np.zeros(bf_pages * h_kv * 2 * P * d, np.float32)
+    for s in range(bf_pages * P):
+        for h in range(h_kv):
+            o = layout.bf16_offset(s // P, h, "k", s % P, d, h_kv)
+            bf_pool[o:o + d] = k[s, h]
+            o = layout.bf16_offset(s // P, h, "v", s % P, d, h_kv)
+            bf_pool[o:o + d] = v[s, h]
+    ref = np.zeros(i2_pages * geo.page_bytes, np.uint8)
+    info = cache.demote(bf_pool, ref, geo, src, dst, rk, rv, tk, tv)
+
+    ctx = make_ctx(cfg)
+    ctx.calibrate_upload(0, rk, rv, tk, tv)
+    pool = torch.zeros(i2_pages * geo.page_bytes, dtype=torch.uint8, device=cuda)
+    ctx.demote_recent(0, bf16(bf_pool, cuda), torch.from_numpy(src).to(cuda), pool, torch.from_numpy(dst).to(cuda))
+    torch.cuda.synchronize()
+    cases.compare_int2(pool.cpu().numpy(), ref, geo, dst, info)
+
+
+def test_bulk_write_full_size(cuda):
+    """The bulk-write workload at full size: 131,072 tokens x 8 KV heads x (K, V), seeded slot permutation."""
+    cfg = cases.workload("bulk_write_131k")
+    li, (rk, rv, tk, tv) = cases.calibration(cfg)
+    n = cfg["tokens"]
+    geo = layout.Int2Geometry(cfg["d"], cfg["group"], cfg["h_kv"])
+    n_pages = n // P
+    slots = synth.rng_for(li.seed, "slots").permutation(n).astype(np.int64)
+    k, v = li.kv("bulk", n)
+    ctx = make_ctx(cfg)
+    ctx.calibrate_upload(0, rk, rv, tk, tv)
+    pool = torch.zeros(n_pages * geo.page_bytes, dtype=torch.uint8, device=cuda)
+    ctx.write_tokens(0, bf16(k, cuda), bf16(v, cuda), torch.from_numpy(slots).to(cuda), pool)
+    torch.cuda.synchronize()
+    got = pool.cpu().numpy()
+    ref = np.zeros_like(got)
+    flips = 0
+    for kind, x, r, t in (("k", k, rk, tk), ("v", v, rv, tv)):
+        for h in range(geo.h_kv):
+            q = quantize.quantize(x[:, h, :].astype(np.float64), r[h], t[h], geo.group)
+            layout.write_int2_rows(ref, geo, slots, h, kind, q["codes"], q["scale"], q["zero"])
+            flips += cases.compare_int2_head(got, ref, geo, slots, kind, h, q)
+            del q
+    assert flips <= 1e-4 * 2 * geo.h_kv * n * geo.d
+    assert np.array_equal(got, ref) or flips > 0
+    print("tolerated boundary flips:", flips)
+
+
+def test_debug_bounds_records_bad_slot(cuda):
+    cfg = cases.workload("tiny")
+    li, (rk, rv, tk, tv) = cases.calibration(cfg)
+    geo = layout.Int2Geometry(cfg["d"], cfg["group"], cfg["h_kv"])
+    ctx = make_ctx(cfg, debug=1)
+    ctx.calibrate_upload(0, rk, rv, tk, tv)
+    k, v = li.kv("dbg", 3)
+    pool = torch.zeros(2 * geo.page_bytes, dtype=torch.uint8, device=cuda)
+    slots = torch.tensor([0, 5 * P + 1, 17], dtype=torch.int64, device=cuda)   # page 5 does not exist
+    ctx.write_tokens(0, bf16(k, cuda), bf16(v, cuda), slots, pool)
+    st, kind, index = ctx.debug_error()
+    assert st == -5 and kind == 1 and index == 5 * P + 1
+    assert ctx.debug_error()[0] == 0
+    # the valid tokens were still written
+    got = pool.cpu().numpy()
+    c, s, z = layout.read_int2_token(got, geo, 17, 0, "k")
+    assert float(np.abs(s.astype(np.float64)).max()) > 0
+
+
+def test_uncalibrated_layer_is_rejected(cuda):
+    cfg = cases.workload("tiny")
+    ctx = make_ctx(cfg, layers=2)
+    pool = torch.zeros(4096, dtype=torch.uint8, device=cuda)
+    k = torch.zeros(1, cfg["h_kv"], cfg["d"], dtype=torch.bfloat16, device=cuda)
+    with pytest.raises(O.OscarError) as e:
+        ctx.write_tokens(1, k, k, torch.zeros(1, dtype=torch.int64, device=cuda), pool)
+    assert e.value.status == -3
