@@ -110,7 +110,7 @@ oscar_status oscar_create(const oscar_config_t* cfg, oscar_ctx_t** out) {
     oscar::Shape& s = ctx->shape;
     s.h_q = c.n_q_heads; s.h_kv = c.n_kv_heads; s.d = c.head_dim; s.group = c.group;
     s.page = c.page_size; s.sink = c.sink; s.recent = c.recent;
-    s.sm_scale = c.sm_scale > 0.0f ? c.sm_scale : 1.0f / std::sqrt((float)c.head_dim);
+    s.sm_scale = c.sm_scale > 0.0f ? (double)c.sm_scale : 1.0 / std::sqrt((double)c.head_dim);
     s.debug = c.debug_bounds ? 1 : 0;
     ctx->calibrated.assign(c.n_layers, 0);
 

@@ -34,24 +34,81 @@ constexpr int kWarps = 4;
 
 __device__ __forceinline__ float fast_exp2(float x) { return exp2f(x); }
 
-template <int D>
-__global__ void q_rotate_kernel(const __nv_bfloat16* __restrict__ q, const float* __restrict__ r_k,
-                                float* __restrict__ q_rot, int h_q, int g) {
+// Error-free transformations on fp32 (no contraction: explicit _rn intrinsics).
+__device__ __forceinline__ void two_sum(float a, float b, float& s, float& e) {
+    s = __fadd_rn(a, b);
+    const float bp = __fsub_rn(s, a);
+    e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bp)), __fsub_rn(b, bp));
+}
+
+__device__ __forceinline__ void two_prod(float a, float b, float& p, float& e) {
+    p = __fmul_rn(a, b);
+    e = __fmaf_rn(a, b, -p);
+}
+
+// Rotated query prepared for exact INT2 logits. Per query head:
+//   q_rot = q @ R_k accumulated as an unevaluated sum hi + lo of two fp32 (about 48 bits);
+//   qg = hi rounded to a grid of 2^(E-12) where max|hi| < 2^E, so sum_c code_c * qg_c over
+//        d <= 128 channels (codes <= 3) is an integer multiple of the grid below 2^24: exact in fp32;
+//   qr = (hi - qg) + lo, the residual (|qr| <= 2^(E-13));
+//   qsum[g] = sum over group g of q_rot, as hi/lo fp32 from an fp64 reduction.
+template <int D, int G>
+__global__ void q_prep_kernel(const __nv_bfloat16* __restrict__ q, const float* __restrict__ r_k,
+                              float* __restrict__ qg, float* __restrict__ qr, float* __restrict__ qsum,
+                              int h_q, int g) {
+    constexpr int NG = D / G;
     __shared__ float qs[D];
+    __shared__ float wmax[D / 32];
+    __shared__ double part[D];
     const int bh = blockIdx.x;
     const int kv = (bh % h_q) / g;
     const int c = threadIdx.x;
     qs[c] = __bfloat162float(q[(size_t)bh * D + c]);
     __syncthreads();
     const float* r = r_k + (size_t)kv * D * D;
-    float acc = 0.0f;
-#pragma unroll 8
-    for (int i = 0; i < D; ++i) acc = fmaf(qs[i], __ldg(r + i * D + c), acc);
-    q_rot[(size_t)bh * D + c] = acc;
+    float hi = 0.0f, lo = 0.0f;
+#pragma unroll 4
+    for (int i = 0; i < D; ++i) {
+        float p, e, s2, e2;
+        two_prod(qs[i], __ldg(r + i * D + c), p, e);
+        two_sum(hi, p, s2, e2);
+        hi = s2;
+        lo = __fadd_rn(lo, __fadd_rn(e, e2));
+    }
+    {
+        float s2, e2;
+        two_sum(hi, lo, s2, e2);
+        hi = s2;
+        lo = e2;
+    }
+    float m = fabsf(hi);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    if (c % 32 == 0) wmax[c / 32] = m;
+    part[c] = (double)hi + (double)lo;
+    __syncthreads();
+    m = 0.0f;
+#pragma unroll
+    for (int w = 0; w < D / 32; ++w) m = fmaxf(m, wmax[w]);
+    int ex = 0;
+    frexpf(m, &ex);                                  // m < 2^ex
+    const float grid_hi = m > 0.0f ? rintf(ldexpf(hi, 12 - ex)) : 0.0f;
+    const float gq = ldexpf(grid_hi, ex - 12);
+    qg[(size_t)bh * D + c] = gq;
+    qr[(size_t)bh * D + c] = __fadd_rn(__fsub_rn(hi, gq), lo);
+    if (c < NG) {
+        double sum = 0.0;
+        for (int j = 0; j < G; ++j) sum += part[c * G + j];
+        const float sh = (float)sum;
+        qsum[((size_t)bh * NG + c) * 2 + 0] = sh;
+        qsum[((size_t)bh * NG + c) * 2 + 1] = (float)(sum - (double)sh);
+    }
 }
 
 struct SplitArgs {
-    const float* q_rot;           // [B][H_q][D]
+    const float* qg;              // [B][H_q][D] grid part of q_rot
+    const float* qr;              // [B][H_q][D] residual of q_rot
+    const float* qsum;            // [B][H_q][D/G][2] group sums of q_rot (hi, lo)
     const __nv_bfloat16* q;       // [B][H_q][D]
     const uint8_t* int2_pool; int64_t int2_pages;
     const int32_t* int2_tables; int int2_stride;
@@ -61,7 +118,7 @@ struct SplitArgs {
     const int32_t* bf16_len; int max_bf16;
     float* partials;              // [B][H_q][S][D+2]
     int h_kv, int2_splits, pages_per_split, bf16_splits, bf16_pages_per_split, total_splits;
-    float scale_log2;             // sm_scale * log2(e)
+    float scale_log2, scale_log2_lo;   // sm_scale * log2(e) as hi + lo
     int debug; DebugWord* dbg;
 };
 
@@ -72,8 +129,9 @@ struct WarpState {
 
 // Online-softmax update for one page of 16 tokens held one token per lane
 // (lanes t and t+16 carry the same logit). Returns p for this lane's token.
+// Logits arrive as hi + lo (lo = 0 for the BF16 segment); m tracks the max of hi.
 template <int GQ>
-__device__ __forceinline__ void softmax_page(float (&lg)[GQ], float (&m)[GQ], float (&l)[GQ],
+__device__ __forceinline__ void softmax_page(float (&lg)[GQ], float (&lgl)[GQ], float (&m)[GQ], float (&l)[GQ],
                                              float (&alpha)[GQ], float (&p)[GQ]) {
 #pragma unroll
     for (int h = 0; h < GQ; ++h) {
@@ -87,7 +145,7 @@ __device__ __forceinline__ void softmax_page(float (&lg)[GQ], float (&m)[GQ], fl
             continue;
         }
         alpha[h] = fast_exp2(m[h] - mn);
-        p[h] = fast_exp2(lg[h] - mn);
+        p[h] = fast_exp2(__fadd_rn(__fsub_rn(lg[h], mn), lgl[h]));
         float ps = p[h];
 #pragma unroll
         for (int o = 1; o < 16; o <<= 1) ps += __shfl_xor_sync(0xffffffffu, ps, o);
@@ -105,7 +163,9 @@ split_kernel(SplitArgs a) {
     constexpr int NG = D / G;
     using GE = Geo<D, G>;
 
-    __shared__ __align__(16) float qs[GQ * D];
+    __shared__ __align__(16) float qs[GQ * D];     // INT2: grid part of q_rot; BF16: q
+    __shared__ __align__(16) float qrs[GQ * D];    // INT2: residual of q_rot
+    __shared__ float qsum_s[GQ][NG][2];
     __shared__ float p_s[kWarps][16][GQ];
     __shared__ float acc_s[GQ * D];
     __shared__ float ml_s[kWarps][GQ][2];
@@ -117,9 +177,12 @@ split_kernel(SplitArgs a) {
 
     for (int i = threadIdx.x; i < GQ * D; i += blockDim.x) {
         const size_t qi = ((size_t)b * h_q + kv * GQ) * D + i;
-        qs[i] = is_int2 ? a.q_rot[qi] : __bfloat162float(a.q[qi]);
+        qs[i] = is_int2 ? a.qg[qi] : __bfloat162float(a.q[qi]);
+        qrs[i] = is_int2 ? a.qr[qi] : 0.0f;
         acc_s[i] = 0.0f;
     }
+    if (threadIdx.x < GQ * NG * 2)
+        (&qsum_s[0][0][0])[threadIdx.x] = a.qsum[((size_t)b * h_q + kv * GQ) * NG * 2 + threadIdx.x];
     __syncthreads();
 
     float m[GQ], l[GQ];
@@ -138,23 +201,6 @@ split_kernel(SplitArgs a) {
         const int n_pages = (len + kPage - 1) / kPage;
         const int pg0 = split * a.pages_per_split;
         const int pg1 = min(n_pages, pg0 + a.pages_per_split);
-
-        // per-lane constant: sum of q_rot over this lane's K channels, per head and group
-        float qsum[GQ][NG];
-#pragma unroll
-        for (int h = 0; h < GQ; ++h)
-#pragma unroll
-            for (int gg = 0; gg < NG; ++gg) qsum[h][gg] = 0.0f;
-#pragma unroll
-        for (int tl = 0; tl < 2; ++tl)
-#pragma unroll
-            for (int kk = 0; kk < n; ++kk)
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const int c = 16 * kk + 4 * (2 * hf + tl) + i;
-#pragma unroll
-                    for (int h = 0; h < GQ; ++h) qsum[h][(16 * kk) / G] += qs[h * D + c];
-                }
 
         float acc[GQ][MPL];
 #pragma unroll
@@ -185,11 +231,12 @@ split_kernel(SplitArgs a) {
                 const uint2 u = *reinterpret_cast<const uint2*>(kseg + t * GE::kCodeRow + 8 * hf);
                 w[0] = u.x; w[1] = u.y;
             }
-            float sdot[GQ][NG];
+            // S = sum_c code_c * q_rot_c per group: grid part exact, residual in fp32
+            float shi[GQ][NG], slo[GQ][NG];
 #pragma unroll
             for (int h = 0; h < GQ; ++h)
 #pragma unroll
-                for (int gg = 0; gg < NG; ++gg) sdot[h][gg] = 0.0f;
+                for (int gg = 0; gg < NG; ++gg) { shi[h][gg] = 0.0f; slo[h][gg] = 0.0f; }
 #pragma unroll
             for (int tl = 0; tl < 2; ++tl)
 #pragma unroll
@@ -201,24 +248,40 @@ split_kernel(SplitArgs a) {
                         const float cf = (float)((w[word] >> bit) & 3u);
                         const int c = 16 * kk + 4 * (2 * hf + tl) + i;
 #pragma unroll
-                        for (int h = 0; h < GQ; ++h)
-                            sdot[h][(16 * kk) / G] = fmaf(qs[h * D + c], cf, sdot[h][(16 * kk) / G]);
+                        for (int h = 0; h < GQ; ++h) {
+                            shi[h][(16 * kk) / G] = __fmaf_rn(qs[h * D + c], cf, shi[h][(16 * kk) / G]);
+                            slo[h][(16 * kk) / G] = __fmaf_rn(qrs[h * D + c], cf, slo[h][(16 * kk) / G]);
+                        }
                     }
             const __half2* ksz = reinterpret_cast<const __half2*>(kseg + GE::kCodeBytes) + t * NG;
-            float lg[GQ];
+            float lg[GQ], lgl[GQ];
 #pragma unroll
             for (int h = 0; h < GQ; ++h) {
-                float dot = 0.0f;
+                // logit = sm2 * sum_g (s_g * S_g + z_g * Q_g), carried as hi + lo
+                float dh = 0.0f, dl = 0.0f;
 #pragma unroll
                 for (int gg = 0; gg < NG; ++gg) {
+                    const float sh = __fadd_rn(shi[h][gg], __shfl_xor_sync(0xffffffffu, shi[h][gg], 16));
+                    const float sl = __fadd_rn(slo[h][gg], __shfl_xor_sync(0xffffffffu, slo[h][gg], 16));
                     const float2 sz = __half22float2(ksz[gg]);
-                    dot = fmaf(sz.x, sdot[h][gg], fmaf(sz.y, qsum[h][gg], dot));
+                    float p1, e1, p2, e2, t1, e3, t2, e4;
+                    two_prod(sz.x, sh, p1, e1);
+                    two_prod(sz.y, qsum_s[h][gg][0], p2, e2);
+                    two_sum(p1, p2, t1, e3);
+                    const float low = __fadd_rn(__fadd_rn(e1, e2), __fadd_rn(e3,
+                                      __fmaf_rn(sz.x, sl, __fmul_rn(sz.y, qsum_s[h][gg][1]))));
+                    two_sum(dh, t1, t2, e4);
+                    dh = t2;
+                    dl = __fadd_rn(dl, __fadd_rn(low, e4));
                 }
-                dot += __shfl_xor_sync(0xffffffffu, dot, 16);
-                lg[h] = valid ? dot * a.scale_log2 : -INFINITY;
+                float lh, ll;
+                two_prod(dh, a.scale_log2, lh, ll);
+                ll = __fadd_rn(ll, __fmaf_rn(dl, a.scale_log2, __fmul_rn(dh, a.scale_log2_lo)));
+                lg[h] = valid ? lh : -INFINITY;
+                lgl[h] = valid ? ll : 0.0f;
             }
             float alpha[GQ], p[GQ];
-            softmax_page<GQ>(lg, m, l, alpha, p);
+            softmax_page<GQ>(lg, lgl, m, l, alpha, p);
             if (hf == 0) {
 #pragma unroll
                 for (int h = 0; h < GQ; ++h) p_s[warp][t][h] = p[h];
@@ -305,13 +368,18 @@ split_kernel(SplitArgs a) {
                         lg[h] = fmaf(qs[h * D + c], kf.x, fmaf(qs[h * D + c + 1], kf.y, lg[h]));
                 }
             }
+            float lgl[GQ];
 #pragma unroll
             for (int h = 0; h < GQ; ++h) {
                 lg[h] += __shfl_xor_sync(0xffffffffu, lg[h], 16);
-                lg[h] = valid ? lg[h] * a.scale_log2 : -INFINITY;
+                float lh, ll;
+                two_prod(lg[h], a.scale_log2, lh, ll);
+                ll = __fmaf_rn(lg[h], a.scale_log2_lo, ll);
+                lg[h] = valid ? lh : -INFINITY;
+                lgl[h] = valid ? ll : 0.0f;
             }
             float alpha[GQ], p[GQ];
-            softmax_page<GQ>(lg, m, l, alpha, p);
+            softmax_page<GQ>(lg, lgl, m, l, alpha, p);
             if (hf == 0) {
 #pragma unroll
                 for (int h = 0; h < GQ; ++h) p_s[warp][t][h] = p[h];
@@ -435,7 +503,7 @@ DecodePlan plan_decode(const Shape& s, int num_sms, int batch, int max_hist) {
     p.bf16_splits = 1;
     p.total_splits = p.int2_splits + p.bf16_splits;
     p.ws_partials = align256((size_t)batch * s.h_q * p.total_splits * (s.d + 2) * sizeof(float));
-    p.ws_qrot = align256((size_t)batch * s.h_q * s.d * sizeof(float));
+    p.ws_qrot = align256((size_t)batch * s.h_q * (2 * s.d + 2 * (s.d / s.group)) * sizeof(float));
     p.ws_total = p.ws_partials + p.ws_qrot;
     return p;
 }
@@ -444,19 +512,28 @@ cudaError_t launch_decode(const Shape& s, const LayerParams& prm, const DecodePl
                           const DecodeArgs& a, DebugWord* dbg, Profiler* prof, cudaStream_t st) {
     const int g = s.h_q / s.h_kv;
     float* partials = static_cast<float*>(a.ws);
-    float* q_rot = reinterpret_cast<float*>(static_cast<char*>(a.ws) + plan.ws_partials);
+    float* qg = reinterpret_cast<float*>(static_cast<char*>(a.ws) + plan.ws_partials);
+    float* qr = qg + (size_t)a.batch * s.h_q * s.d;
+    float* qsum = qr + (size_t)a.batch * s.h_q * s.d;
     const __nv_bfloat16* q = static_cast<const __nv_bfloat16*>(a.q);
 
     {
         ProfScope ps(prof, OSCAR_KERNEL_QROT, st);
-        if (s.d == 128) q_rotate_kernel<128><<<a.batch * s.h_q, 128, 0, st>>>(q, prm.r_k, q_rot, s.h_q, g);
-        else q_rotate_kernel<64><<<a.batch * s.h_q, 64, 0, st>>>(q, prm.r_k, q_rot, s.h_q, g);
+#define OSCAR_QPREP_CASE(D_, G_) \
+        if (s.d == D_ && s.group == G_) \
+            q_prep_kernel<D_, G_><<<a.batch * s.h_q, D_, 0, st>>>(q, prm.r_k, qg, qr, qsum, s.h_q, g);
+        OSCAR_QPREP_CASE(64, 32)
+        OSCAR_QPREP_CASE(64, 64)
+        OSCAR_QPREP_CASE(128, 32)
+        OSCAR_QPREP_CASE(128, 64)
+        OSCAR_QPREP_CASE(128, 128)
+#undef OSCAR_QPREP_CASE
     }
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
 
     SplitArgs sa{};
-    sa.q_rot = q_rot; sa.q = q;
+    sa.qg = qg; sa.qr = qr; sa.qsum = qsum; sa.q = q;
     sa.int2_pool = a.int2_pool; sa.int2_pages = a.int2_pages;
     sa.int2_tables = a.int2_tables; sa.int2_stride = a.int2_stride;
     sa.hist_len = a.hist_len; sa.max_hist = a.max_hist;
@@ -468,7 +545,11 @@ cudaError_t launch_decode(const Shape& s, const LayerParams& prm, const DecodePl
     sa.bf16_splits = plan.bf16_splits;
     sa.bf16_pages_per_split = (s.sink + s.recent + kPage - 1) / kPage;
     sa.total_splits = plan.total_splits;
-    sa.scale_log2 = s.sm_scale * kLog2e;
+    {
+        const double sl2 = s.sm_scale * 1.4426950408889634073599;
+        sa.scale_log2 = (float)sl2;
+        sa.scale_log2_lo = (float)(sl2 - (double)sa.scale_log2);
+    }
     sa.debug = s.debug; sa.dbg = dbg;
 
     ProfScope ps_split(prof, OSCAR_KERNEL_SPLIT, st);

@@ -24,7 +24,7 @@ struct LayerParams {
 
 struct Shape {
     int h_q, h_kv, d, group, page, sink, recent;
-    float sm_scale;
+    double sm_scale;
     int debug;
 };
 

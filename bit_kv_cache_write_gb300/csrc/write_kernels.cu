@@ -27,6 +27,41 @@ namespace {
 constexpr int kWarps = 4;
 constexpr int kTok = 8;      // tokens per warp iteration (register blocking over R)
 
+// Error-free transformations on fp32 (explicit _rn intrinsics: no contraction).
+__device__ __forceinline__ void two_sum(float a, float b, float& s, float& e) {
+    s = __fadd_rn(a, b);
+    const float bp = __fsub_rn(s, a);
+    e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bp)), __fsub_rn(b, bp));
+}
+
+// x . R[:, c] rounded once to fp32 (double-float accumulation, ~48-bit), computed by the
+// whole warp: lane l takes terms l, l+32, ...; the result is lane 0's, broadcast.
+template <int D>
+__device__ float exact_dot_warp(const float* x, const float* r, int c, int lane) {
+    float hi = 0.0f, lo = 0.0f;
+#pragma unroll
+    for (int k = 0; k < D / 32; ++k) {
+        const int i = lane + 32 * k;
+        const float a = x[i], b = r[i * D + c];
+        const float p = __fmul_rn(a, b);
+        const float pe = __fmaf_rn(a, b, -p);
+        float s, e;
+        two_sum(hi, p, s, e);
+        hi = s;
+        lo = __fadd_rn(lo, __fadd_rn(pe, e));
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const float h2 = __shfl_xor_sync(0xffffffffu, hi, o);
+        const float l2 = __shfl_xor_sync(0xffffffffu, lo, o);
+        float s, e;
+        two_sum(hi, h2, s, e);
+        hi = s;
+        lo = __fadd_rn(__fadd_rn(lo, l2), e);
+    }
+    return __shfl_sync(0xffffffffu, __fadd_rn(hi, lo), 0);
+}
+
 template <int D, int G>
 __global__ void __launch_bounds__(kWarps * 32)
 write_kernel(const float* __restrict__ r_all, const float* __restrict__ t_all,
@@ -121,8 +156,9 @@ write_kernel(const float* __restrict__ r_all, const float* __restrict__ t_all,
             }
         }
 
-#pragma unroll 1
-        for (int t = 0; t < cnt; ++t) {
+#pragma unroll
+        for (int t = 0; t < kTok; ++t) {
+            if (t >= cnt) break;
             const int tok = base + t;
             const int64_t slot = dst_slots[tok];
             const int64_t pg = slot / kPage;
@@ -133,6 +169,15 @@ write_kernel(const float* __restrict__ r_all, const float* __restrict__ t_all,
                 if (s < 0 || s / kPage >= bf16_pages) ok = false;
             }
             if (!ok) continue;   // warp-uniform
+
+            // rigorous bound on the fp32 rotation error of every channel of this token:
+            // |fl(x.R_c) - x.R_c| <= gamma_D * sum_i |x_i R_ic| <= gamma_D * ||x||_2 (R orthogonal)
+            float sq = 0.0f;
+#pragma unroll
+            for (int j = 0; j < CPL; ++j) sq = fmaf(xw[t * D + lane + 32 * j], xw[t * D + lane + 32 * j], sq);
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, o);
+            const float err = 1.01f * (float)(D + 1) * 0x1p-24f * sqrtf(sq * 1.001f);
 
             float xh[CPL];
             float mn = FLT_MAX, mx = -FLT_MAX;
@@ -146,6 +191,44 @@ write_kernel(const float* __restrict__ r_all, const float* __restrict__ t_all,
             for (int o = 1; o < LPG; o <<= 1) {
                 mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
                 mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+            }
+            // The stored zero (fp16 mn) and scale (fp16 (mx-mn)/3) can only be off by more than
+            // one fp16 ulp when |mn| or the range is within ~2^12 error bounds. Then every channel
+            // that may hold the group min (max) is recomputed exactly and the stats are redone.
+            {
+                const float r0 = mx - mn;
+                const bool need_min = fabsf(mn) < 4096.0f * err || r0 < 8192.0f * err;
+                const bool need_max = r0 < 8192.0f * err;
+                uint32_t cand = 0u;
+#pragma unroll
+                for (int j = 0; j < CPL; ++j)
+                    if ((need_min && xh[j] <= mn + 2.0f * err) || (need_max && xh[j] >= mx - 2.0f * err))
+                        cand |= 1u << j;
+                uint32_t lanes = __ballot_sync(0xffffffffu, cand != 0u);
+                if (lanes) {
+                    while (lanes) {
+                        const int src = __ffs(lanes) - 1;
+                        lanes &= lanes - 1;
+                        uint32_t cm = __shfl_sync(0xffffffffu, cand, src);
+                        while (cm) {
+                            const int j = __ffs(cm) - 1;
+                            cm &= cm - 1;
+                            const float ex = exact_dot_warp<D>(xw + t * D, r_s, CPL * src + j, lane);
+#pragma unroll
+                            for (int jj = 0; jj < CPL; ++jj)
+                                if (lane == src && jj == j) xh[jj] = fminf(fmaxf(ex, -thr[jj]), thr[jj]);
+                        }
+                    }
+                    mn = FLT_MAX;
+                    mx = -FLT_MAX;
+#pragma unroll
+                    for (int j = 0; j < CPL; ++j) { mn = fminf(mn, xh[j]); mx = fmaxf(mx, xh[j]); }
+#pragma unroll
+                    for (int o = 1; o < LPG; o <<= 1) {
+                        mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+                        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+                    }
+                }
             }
             const float rng = __fsub_rn(mx, mn);
             const bool degenerate = !(rng >= FLT_MIN);

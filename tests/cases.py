@@ -48,12 +48,18 @@ def compare_int2_head(gpu_pool, ref_pool, geo, slots, kind, h, q):
     sidx = (base + geo.code_bytes + rows * ng * 4)[:, None] + np.arange(ng * 4)[None, :]
     g_sz = np.ascontiguousarray(gpu_pool[sidx]).view(np.uint16).reshape(len(slots), ng, 2)
     r_sz = np.ascontiguousarray(ref_pool[sidx]).view(np.uint16).reshape(len(slots), ng, 2)
-    ulp = np.abs(g_sz.astype(np.int64) - r_sz.astype(np.int64))
-    same_sign = (g_sz >> 15) == (r_sz >> 15)
-    both_zero = ((g_sz & 0x7FFF) == 0) & ((r_sz & 0x7FFF) == 0)
-    ok_sz = (same_sign & (ulp <= 1)) | both_zero
-    assert ok_sz.all(), "%s head %d: scale/zero differ by more than 1 fp16 ulp at %d places" % (
-        kind, h, int((~ok_sz).sum()))
+    def ordered(x):      # fp16 bit patterns on one integer line: adjacent values differ by 1, -0 == +0
+        x = x.astype(np.int64)
+        return np.where(x & 0x8000, -(x & 0x7FFF), x)
+    ok_sz = np.abs(ordered(g_sz) - ordered(r_sz)) <= 1
+    if not ok_sz.all():
+        bad = np.argwhere(~ok_sz)[:5]
+        detail = ["slot %d group %d %s: gpu %r oracle %r" % (
+            slots[i], g, "scale" if j == 0 else "zero",
+            float(g_sz[i, g, j:j + 1].view(np.float16)[0]), float(r_sz[i, g, j:j + 1].view(np.float16)[0]))
+            for i, g, j in bad]
+        raise AssertionError("%s head %d: scale/zero differ by more than 1 fp16 ulp at %d places: %s" % (
+            kind, h, int((~ok_sz).sum()), "; ".join(detail)))
     diff = g_codes.astype(np.int64) - r_codes.astype(np.int64)
     bad = diff != 0
     if not bad.any():
