@@ -52,6 +52,14 @@ oscar_status check_ctx_layer(const oscar_ctx_t* ctx, int layer) {
 
 namespace oscar {
 
+oscar_status record_failure(oscar_status st, const char* fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_last_error, sizeof(g_last_error), fmt, ap);
+    va_end(ap);
+    return st;
+}
+
 LayerParams layer_params(const oscar_ctx* ctx, int layer) {
     const Shape& s = ctx->shape;
     const size_t hdd = (size_t)s.h_kv * s.d * s.d, hd = (size_t)s.h_kv * s.d;

@@ -83,6 +83,9 @@ namespace oscar {
 
 LayerParams layer_params(const oscar_ctx* ctx, int layer);
 
+// Records `st` and a formatted message as the calling thread's last failure; returns st.
+oscar_status record_failure(oscar_status st, const char* fmt, ...);
+
 // ---- write path (write_kernels.cu)
 cudaError_t launch_write(const Shape& s, const LayerParams& p, int num_sms,
                          const void* k, const void* v, const int64_t* slots, int n,

@@ -50,6 +50,8 @@ _SIGS = {
     "oscar_status_string": (ctypes.c_char_p, [_i]),
     "oscar_last_error": (ctypes.c_char_p, []),
     "oscar_debug_error": (_i, [_vp, ctypes.POINTER(_i), ctypes.POINTER(ctypes.c_longlong)]),
+    "oscar_decode_static_workspace": (_i, [_vp, _i, _vp, _vp, _i64, _vp, _i, _vp, _i, _vp, _i64, _vp, _i, _vp,
+                                           _vp, _i, _vp]),
     "oscar_profile_enable": (_i, [_vp, _i]),
     "oscar_profile_read": (_i, [_vp, _i, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_longlong)]),
 }
@@ -183,6 +185,29 @@ def oscar_decode(ctx, layer, q, int2_pool, int2_tables, hist_len, max_hist, bf16
         workspace.numel() * workspace.element_size(), batch, _stream(stream)), "oscar_decode")
 
 
+def oscar_decode_static_workspace(ctx, layer, q, int2_pool, int2_tables, hist_len, max_hist, bf16_pool,
+                                  bf16_tables, bf16_len, out, stream=None):
+    """oscar_decode for callers that cannot allocate: the scratch is the library's static device array.
+
+    Same arguments as oscar_decode without the workspace. The library rejects
+    sizes whose workspace exceeds its fixed maximum. Calls that overlap on the
+    GPU share that array and race.
+    """
+    import torch
+    batch = q.shape[0]
+    i2_pages = int2_pool.numel() // oscar_int2_page_bytes(ctx) if int2_pool is not None else 0
+    bf_pages = bf16_pool.numel() * 2 // oscar_bf16_page_bytes(ctx)
+    _check(lib().oscar_decode_static_workspace(
+        ctx, layer, _dptr(q, torch.bfloat16, "q"),
+        _dptr(int2_pool, torch.uint8, "int2_pool"), i2_pages,
+        _dptr(int2_tables, torch.int32, "int2_tables"), int2_tables.shape[1] if int2_tables is not None else 0,
+        _dptr(hist_len, torch.int32, "hist_len"), int(max_hist),
+        _dptr(bf16_pool, torch.bfloat16, "bf16_pool"), bf_pages,
+        _dptr(bf16_tables, torch.int32, "bf16_tables"), bf16_tables.shape[1],
+        _dptr(bf16_len, torch.int32, "bf16_len"),
+        _dptr(out, torch.float32, "out"), batch, _stream(stream)), "oscar_decode_static_workspace")
+
+
 def oscar_debug_error(ctx):
     """Returns (status, kind, index) and clears the device error word."""
     kind = _i(0)
@@ -237,6 +262,11 @@ class Oscar:
                out, workspace, stream=None):
         oscar_decode(self.ctx, layer, q, int2_pool, int2_tables, hist_len, max_hist, bf16_pool, bf16_tables,
                      bf16_len, out, workspace, stream)
+
+    def decode_static_workspace(self, layer, q, int2_pool, int2_tables, hist_len, max_hist, bf16_pool, bf16_tables,
+                                bf16_len, out, stream=None):
+        oscar_decode_static_workspace(self.ctx, layer, q, int2_pool, int2_tables, hist_len, max_hist, bf16_pool,
+                                      bf16_tables, bf16_len, out, stream)
 
     def int2_page_bytes(self):
         return oscar_int2_page_bytes(self.ctx)

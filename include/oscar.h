@@ -210,6 +210,32 @@ OSCAR_API oscar_status oscar_decode(oscar_ctx_t* ctx, int layer, const void* q,
                           float* out, void* workspace, size_t workspace_bytes,
                           int batch, void* stream);
 
+/* oscar_decode without a caller workspace. The pages have no counterpart for
+ * this call. It exists for callers that cannot allocate device memory:
+ *   - a host engine that only hands the op its input and output buffers;
+ *   - a serving loop whose allocator owns the whole device budget;
+ *   - a decode step recorded under CUDA stream capture, where cudaMalloc is
+ *     not permitted.
+ * The scratch is one static device array of 8 MiB, which every GPU that loads
+ * the library holds until process exit. Arguments and results are those of
+ * oscar_decode, minus the workspace. Sizes whose
+ * oscar_decode_workspace_size(ctx, batch, max_hist) exceeds 8 MiB are rejected
+ * with OSCAR_ERR_WORKSPACE before anything is launched. The call allocates
+ * nothing (no cudaMalloc/cudaFree or allocating library routine).
+ * The first call on a device looks up the array's device address; make that
+ * first call before any stream capture. All calls share the one array, and it
+ * keeps the last call's contents. Calls whose work overlaps on the GPU (e.g.
+ * on two streams at once) race on it and must be serialised by the caller.
+ * Nothing in it has to start at zero. Asynchronous on `stream` like
+ * oscar_decode. */
+OSCAR_API oscar_status oscar_decode_static_workspace(oscar_ctx_t* ctx, int layer, const void* q,
+                                                     const void* int2_pool, int64_t int2_pool_pages,
+                                                     const int32_t* int2_tables, int int2_table_stride,
+                                                     const int32_t* hist_len, int max_hist,
+                                                     const void* bf16_pool, int64_t bf16_pool_pages,
+                                                     const int32_t* bf16_tables, int bf16_table_stride,
+                                                     const int32_t* bf16_len, float* out, int batch, void* stream);
+
 /* Bytes of one INT2 page (all heads, K and V) and of one BF16 page. */
 OSCAR_API size_t oscar_int2_page_bytes(const oscar_ctx_t* ctx);
 OSCAR_API size_t oscar_bf16_page_bytes(const oscar_ctx_t* ctx);
