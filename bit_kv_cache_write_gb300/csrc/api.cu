@@ -6,7 +6,9 @@
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
+#include <algorithm>
 #include <new>
+#include <vector>
 
 #include "oscar_internal.h"
 
@@ -36,7 +38,7 @@ bool fault(const char* what) {
 bool pow2_in(int v, int lo, int hi) { return v >= lo && v <= hi && (v & (v - 1)) == 0; }
 
 size_t layer_floats(const oscar::Shape& s) {
-    return 3 * (size_t)s.h_kv * s.d * s.d + 2 * (size_t)s.h_kv * s.d;
+    return 3 * (size_t)s.h_kv * s.d * s.d + 2 * (size_t)s.h_kv * s.d + (size_t)s.h_kv;
 }
 
 oscar_status check_ctx_layer(const oscar_ctx_t* ctx, int layer) {
@@ -70,6 +72,7 @@ LayerParams layer_params(const oscar_ctx* ctx, int layer) {
     p.r_vt = base + 2 * hdd;
     p.t_k = base + 3 * hdd;
     p.t_v = base + 3 * hdd + hd;
+    p.pv_scale = base + 3 * hdd + 2 * hd;
     return p;
 }
 
@@ -178,6 +181,21 @@ oscar_status oscar_calibrate_upload(oscar_ctx_t* ctx, int layer, const float* R_
     if (e == cudaSuccess) e = cudaMemcpyAsync(const_cast<float*>(p.t_k), T_k, hd * sizeof(float), cudaMemcpyHostToDevice, st);
     if (e == cudaSuccess) e = cudaMemcpyAsync(const_cast<float*>(p.t_v), T_v, hd * sizeof(float), cudaMemcpyHostToDevice, st);
     if (e == cudaSuccess) e = oscar::launch_transpose(p.r_v, const_cast<float*>(p.r_vt), s.h_kv, s.d, st);
+    // Per KV head power of two 2^sigma for the decode's p * s_v operand. Every stored V scale is
+    // fp16((mx - mn) / 3) <= (2/3) max T_v (values are clipped to [-T, T]), so p * s_v * 2^sigma
+    // stays at or below 32752 (fp16) while small weights keep clear of fp16 subnormals.
+    std::vector<float> pvs(s.h_kv);
+    for (int h = 0; h < s.h_kv; ++h) {
+        float tmax = 0.0f;
+        for (int c = 0; c < s.d; ++c) tmax = std::max(tmax, T_v[(size_t)h * s.d + c]);
+        const double smax = std::max(1e-30, (2.0 / 3.0) * (double)tmax * 1.001);
+        int sigma = (int)std::floor(std::log2(32752.0 / smax));
+        sigma = std::min(40, std::max(-40, sigma));
+        pvs[h] = std::ldexp(1.0f, sigma);
+    }
+    if (e == cudaSuccess)
+        e = cudaMemcpyAsync(const_cast<float*>(p.pv_scale), pvs.data(), s.h_kv * sizeof(float),
+                            cudaMemcpyHostToDevice, st);
     if (e == cudaSuccess) e = cudaStreamSynchronize(st);
     if (e != cudaSuccess) return cuda_fail(e, "calibration upload");
     ctx->calibrated[layer] = 1;

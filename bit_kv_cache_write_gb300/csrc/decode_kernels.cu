@@ -2,22 +2,38 @@
 //
 // Method: QbitAI article on OSCAR, serving-pipeline part. At decode, the INT2
 // part unpacks codes, dequantizes with scale/zero point and accumulates in
-// floating point; a BF16 part covers sink and recent; an online-softmax merge
+// floating point. A BF16 part covers sink and recent. An online-softmax merge
 // combines the two. arXiv 2605.17757 abstracts: the kernels keep the paged
 // KV-cache layout and prefix caching (block tables may share pages).
 //
 // Three launches per layer:
-//   1. q_rotate:   q_rot = q @ R_k for every query head (fp32).
-//   2. split:      one CTA per (split, KV head, sequence). INT2 splits stream
-//                  pages of the history; BF16 splits cover sink + recent. Each
-//                  writes a partial (m, l, acc[d]) per query head of the group,
-//                  with m in log2 units.
-//   3. merge:      combines the splits of each query head, un-rotates the INT2
-//                  accumulator by R_v^T and normalises.
+//   1. q_prep: q_rot = q @ R_k for every query head, accumulated as two fp32
+//      (about 48 bits). It is split into three fp16 tensor-core operands on
+//      nested fixed-point grids. Also per-group sums of q_rot.
+//   2. split: one CTA per (split, KV head, sequence).
+//      - INT2 splits stream page blocks into shared memory with bulk async
+//        copies, four stages per warp. They compute q_rot . codes and
+//        p . codes with mma.sync m16n8k16 on the packed codes, and keep an
+//        online softmax.
+//      - BF16 splits handle sink + recent on CUDA cores.
+//      - Each split writes a partial (m, l, acc[d]) per query head of the
+//        group, with m in log2 units.
+//   3. merge: combines the splits of each query head, un-rotates the INT2
+//      accumulator by R_v^T and normalises.
 //
-// Inside an INT2 split, the scale/zero identity
-//   q . (code*s + z) = s * (q . code) + z * sum(q)
-// keeps the dequant out of the inner product, per group.
+// Exactness of the INT2 logits. With codes c in {0..3}, scale s and zero z per
+// group:
+//   q . (c*s + z) = s * (q . c) + z * sum(q).
+// q . c is computed exactly: every q part is an 11-bit integer on a power-of-two
+// grid, so each tensor-core partial sum is an exactly representable fp32. s and
+// z then enter through error-free products. The logit is carried as hi + lo
+// into the softmax exponent, so INT2 logits keep about 1e-7 absolute accuracy
+// even where they are ~30 in log2 units.
+//
+// Unpacking. A packed code pair at bit position p of a 32-bit word becomes an
+// fp16 (sub)normal c * 2^(2p-24) with a single mask (positions 5..7 after one
+// shift by 10). Each position's power of two is folded into the query operand
+// (QK) or into a per-m-step rescale of the output (PV).
 
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -31,10 +47,12 @@ namespace oscar {
 namespace {
 
 constexpr int kWarps = 4;
+constexpr int kStages = 4;
+constexpr long long kWaitCycles = 2000000000LL;   // give up on a page copy after ~1 s
 
 __device__ __forceinline__ float fast_exp2(float x) { return exp2f(x); }
 
-// Error-free transformations on fp32 (no contraction: explicit _rn intrinsics).
+// Error-free transformations on fp32 (explicit _rn intrinsics: no contraction).
 __device__ __forceinline__ void two_sum(float a, float b, float& s, float& e) {
     s = __fadd_rn(a, b);
     const float bp = __fsub_rn(s, a);
@@ -46,69 +64,171 @@ __device__ __forceinline__ void two_prod(float a, float b, float& p, float& e) {
     e = __fmaf_rn(a, b, -p);
 }
 
-// Rotated query prepared for exact INT2 logits. Per query head:
-//   q_rot = q @ R_k accumulated as an unevaluated sum hi + lo of two fp32 (about 48 bits);
-//   qg = hi rounded to a grid of 2^(E-12) where max|hi| < 2^E, so sum_c code_c * qg_c over
-//        d <= 128 channels (codes <= 3) is an integer multiple of the grid below 2^24: exact in fp32;
-//   qr = (hi - qg) + lo, the residual (|qr| <= 2^(E-13));
-//   qsum[g] = sum over group g of q_rot, as hi/lo fp32 from an fp64 reduction.
+__device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};\n"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Position p' and fp16 bit pattern of the code pair at position `pos` (0..7) of word w:
+// c_lo * 2^(2p'-24) in the low half, c_hi * 2^(2p'-24) in the high half.
+__host__ __device__ constexpr int pos_scale(int pos) { return pos <= 4 ? pos : pos - 5; }
+
+template <int POS>
+__device__ __forceinline__ uint32_t code_pair(uint32_t w, uint32_t w10) {
+    if constexpr (POS <= 4) return w & (0x00030003u << (2 * POS));
+    else return w10 & (0x00030003u << (2 * (POS - 5)));
+}
+
+// Code pair at position POS as a normal fp16 pair c * 2^(2p'): the masked bits form the mantissa of
+// 1024 + c * 2^(2p'), then 1024 is subtracted exactly. Normal operands keep the tensor-core products
+// of P.V at full precision (fp16 subnormal operands lose low bits against larger products).
+template <int POS>
+__device__ __forceinline__ uint32_t code_pair_normal(uint32_t w, uint32_t w10) {
+    const uint32_t h = code_pair<POS>(w, w10) | 0x64006400u;
+    const __half2 r = __hsub2(*reinterpret_cast<const __half2*>(&h), __half2(__ushort_as_half(0x6400), __ushort_as_half(0x6400)));
+    return *reinterpret_cast<const uint32_t*>(&r);
+}
+
+__device__ __forceinline__ uint32_t pack_half2(__half lo, __half hi) {
+    return (uint32_t)__half_as_ushort(lo) | ((uint32_t)__half_as_ushort(hi) << 16);
+}
+
+// hi or lo fp16 part of x: hi = fp16(x), lo = fp16((x - hi) * 2^11).
+__device__ __forceinline__ __half split_part(float x, bool lo) {
+    const __half h = __float2half_rn(x);
+    return lo ? __float2half_rn(__fmul_rn(__fsub_rn(x, __half2float(h)), 2048.0f)) : h;
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, int count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" :: "r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" :: "r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" :: "r"(bar), "r"(bytes) : "memory");
+    asm volatile("cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                 :: "r"(dst), "l"(src), "r"(bytes), "r"(bar) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t phase) {
+    uint32_t ok;
+    asm volatile("{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
+                 : "=r"(ok) : "r"(bar), "r"(phase) : "memory");
+    return ok != 0;
+}
+
+// Bounded wait on an mbarrier phase; false if it did not complete within kWaitCycles.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t phase) {
+    if (mbar_test(bar, phase)) return true;
+    const long long t0 = clock64();
+    while (!mbar_test(bar, phase))
+        if (clock64() - t0 > kWaitCycles) return false;
+    return true;
+}
+
+// ---------------------------------------------------------------------------------------------
+// Query preparation
+// ---------------------------------------------------------------------------------------------
+
+// Per query head (one block of D threads):
+//   q_rot[c] = sum_i q_i R[i][c] as hi + lo fp32 (error-free products and sums);
+//   E with max|q_rot| < 2^E; r_hi, r_mid, r_lo integers (|r| <= 2048) with
+//     q_rot = (r_hi + r_mid 2^-11 + r_lo 2^-22) 2^(E-11)  (to ~2^(E-33));
+//   qb[part][c] = r_part * 2^(4 - 2p'(c)) as fp16 (exact), p'(c) the fp16 position of channel c
+//     in the K layout, so that code(c) * 2^(2p'-24) * qb = code * r_part * 2^-20;
+//   kap = 2^(E + 9): S_part = accumulator * kap * 2^(-11 part);
+//   qsum[g] = sum over group g of q_rot (hi, lo).
 template <int D, int G>
 __global__ void q_prep_kernel(const __nv_bfloat16* __restrict__ q, const float* __restrict__ r_k,
-                              float* __restrict__ qg, float* __restrict__ qr, float* __restrict__ qsum,
+                              __half* __restrict__ qb, float* __restrict__ kap, float* __restrict__ qsum,
                               int h_q, int g) {
     constexpr int NG = D / G;
     __shared__ float qs[D];
     __shared__ float wmax[D / 32];
-    __shared__ double part[D];
+    __shared__ double part_s[D];
     const int bh = blockIdx.x;
     const int kv = (bh % h_q) / g;
     const int c = threadIdx.x;
     qs[c] = __bfloat162float(q[(size_t)bh * D + c]);
     __syncthreads();
     const float* r = r_k + (size_t)kv * D * D;
-    float hi = 0.0f, lo = 0.0f;
-#pragma unroll 4
-    for (int i = 0; i < D; ++i) {
-        float p, e, s2, e2;
-        two_prod(qs[i], __ldg(r + i * D + c), p, e);
-        two_sum(hi, p, s2, e2);
-        hi = s2;
-        lo = __fadd_rn(lo, __fadd_rn(e, e2));
+    float hi[4] = {0.f, 0.f, 0.f, 0.f}, lo[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 2
+    for (int i = 0; i < D; i += 4) {
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            float p, e, s2, e2;
+            two_prod(qs[i + u], __ldg(r + (i + u) * D + c), p, e);
+            two_sum(hi[u], p, s2, e2);
+            hi[u] = s2;
+            lo[u] = __fadd_rn(lo[u], __fadd_rn(e, e2));
+        }
+    }
+    float h = 0.0f, l = 0.0f;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+        float s2, e2;
+        two_sum(h, hi[u], s2, e2);
+        h = s2;
+        l = __fadd_rn(l, __fadd_rn(lo[u], e2));
     }
     {
         float s2, e2;
-        two_sum(hi, lo, s2, e2);
-        hi = s2;
-        lo = e2;
+        two_sum(h, l, s2, e2);
+        h = s2;
+        l = e2;
     }
-    float m = fabsf(hi);
+    float m = fabsf(h);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
     if (c % 32 == 0) wmax[c / 32] = m;
-    part[c] = (double)hi + (double)lo;
+    part_s[c] = (double)h + (double)l;
     __syncthreads();
     m = 0.0f;
 #pragma unroll
     for (int w = 0; w < D / 32; ++w) m = fmaxf(m, wmax[w]);
     int ex = 0;
-    frexpf(m, &ex);                                  // m < 2^ex
-    const float grid_hi = m > 0.0f ? rintf(ldexpf(hi, 12 - ex)) : 0.0f;
-    const float gq = ldexpf(grid_hi, ex - 12);
-    qg[(size_t)bh * D + c] = gq;
-    qr[(size_t)bh * D + c] = __fadd_rn(__fsub_rn(hi, gq), lo);
+    frexpf(m * 1.0000005f, &ex);                       // max|q_rot| < 2^ex
+    // r_hi, r_mid, r_lo: successive 11-bit digits of q_rot / 2^(ex-11)
+    const float xh = ldexpf(h, 11 - ex), xl = ldexpf(l, 11 - ex);
+    const float r_hi = rintf(xh);
+    const float rem1 = __fadd_rn(__fsub_rn(xh, r_hi), xl);                // |rem1| <= 0.5 + tiny
+    const float r_mid = rintf(__fmul_rn(rem1, 2048.0f));
+    const float rem2 = __fsub_rn(__fmul_rn(rem1, 2048.0f), r_mid);
+    const float r_lo = rintf(__fmul_rn(rem2, 2048.0f));
+    const int pos = 2 * ((c / 16) % 4) + (c % 4) / 2;                     // K-layout position of channel c
+    const int sh = 4 - 2 * pos_scale(pos);
+    __half* dst = qb + (size_t)bh * 3 * D;
+    const bool any = m > 0.0f;
+    dst[c] = __float2half_rn(any ? ldexpf(r_hi, sh) : 0.0f);
+    dst[D + c] = __float2half_rn(any ? ldexpf(r_mid, sh) : 0.0f);
+    dst[2 * D + c] = __float2half_rn(any ? ldexpf(r_lo, sh) : 0.0f);
+    if (c == 0) kap[bh] = any ? ldexpf(1.0f, ex + 9) : 0.0f;
     if (c < NG) {
         double sum = 0.0;
-        for (int j = 0; j < G; ++j) sum += part[c * G + j];
-        const float sh = (float)sum;
-        qsum[((size_t)bh * NG + c) * 2 + 0] = sh;
-        qsum[((size_t)bh * NG + c) * 2 + 1] = (float)(sum - (double)sh);
+        for (int j = 0; j < G; ++j) sum += part_s[c * G + j];
+        const float sh2 = (float)sum;
+        qsum[((size_t)bh * NG + c) * 2 + 0] = sh2;
+        qsum[((size_t)bh * NG + c) * 2 + 1] = (float)(sum - (double)sh2);
     }
 }
 
+// ---------------------------------------------------------------------------------------------
+// Split kernel
+// ---------------------------------------------------------------------------------------------
+
 struct SplitArgs {
-    const float* qg;              // [B][H_q][D] grid part of q_rot
-    const float* qr;              // [B][H_q][D] residual of q_rot
-    const float* qsum;            // [B][H_q][D/G][2] group sums of q_rot (hi, lo)
+    const __half* qb;             // [B][H_q][3][D] tensor-core query parts
+    const float* kap;             // [B][H_q]
+    const float* qsum;            // [B][H_q][D/G][2]
+    const float* pv_scale;        // [H_kv] 2^sigma for the p * s_v operand
     const __nv_bfloat16* q;       // [B][H_q][D]
     const uint8_t* int2_pool; int64_t int2_pages;
     const int32_t* int2_tables; int int2_stride;
@@ -122,14 +242,376 @@ struct SplitArgs {
     int debug; DebugWord* dbg;
 };
 
-template <int D, int GQ>
-struct WarpState {
-    float m[GQ], l[GQ];
+template <int D, int G, int GQ>
+struct SplitSmem {
+    static constexpr int kBlock = Geo<D, G>::kBlock;
+    static constexpr size_t kDynamic = (size_t)kWarps * kStages * kBlock;
 };
 
+// INT2 history split on tensor cores. Writes this warp's state into acc_s / ml_s.
+template <int D, int G, int GQ>
+__device__ void int2_split(const SplitArgs& a, int split, int kv, int b, uint8_t* stage_base, uint64_t* bars,
+                           float* acc_s, float (*ml_s)[GQ][2]) {
+    using GE = Geo<D, G>;
+    constexpr int NK = D / 16;          // k-steps (QK) = m-steps (PV)
+    constexpr int NG = D / G;
+    constexpr int KPG = G / 16;         // k-steps per group
+    constexpr int NHB = (GQ + 3) / 4;   // blocks of 4 query heads
+    constexpr int KW = NK / 4;          // K words per token in a quad lane's run
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const int gid = lane >> 2, tig = lane & 3;
+    const int h_q = a.h_kv * GQ;
+    const size_t head0 = (size_t)b * h_q + kv * GQ;
+
+    int len = a.hist_len[b];
+    const int cap = min(a.max_hist, a.int2_stride * kPage);
+    if (len < 0 || len > cap) {
+        if (a.debug && threadIdx.x == 0) record_error(&a.dbg->kind, &a.dbg->index, 3, len);
+        len = len < 0 ? 0 : cap;
+    }
+    const int n_pages = (len + kPage - 1) / kPage;
+    const int pg0 = split * a.pages_per_split;
+    const int pg1 = min(n_pages, pg0 + a.pages_per_split);
+    const int first = pg0 + warp;
+    const int n_mine = first < pg1 ? (pg1 - first + kWarps - 1) / kWarps : 0;
+
+    // ---- query operands (constant over pages)
+    uint32_t qB1[NK][NHB][2], qB2[NK][2];
+    float kap_h[NHB], qs_hi[NHB][NG], qs_lo[NHB][NG];
+#pragma unroll
+    for (int hb = 0; hb < NHB; ++hb) {
+        const int h = 4 * hb + (gid >> 1);
+        const int part = gid & 1;
+#pragma unroll
+        for (int kk = 0; kk < NK; ++kk) {
+            uint2 v = make_uint2(0u, 0u);
+            if (h < GQ) v = *reinterpret_cast<const uint2*>(a.qb + ((head0 + h) * 3 + part) * D + 16 * kk + 4 * tig);
+            qB1[kk][hb][0] = v.x;
+            qB1[kk][hb][1] = v.y;
+        }
+        const int hm = 4 * hb + tig;
+        kap_h[hb] = hm < GQ ? a.kap[head0 + hm] : 0.0f;
+#pragma unroll
+        for (int gg = 0; gg < NG; ++gg) {
+            qs_hi[hb][gg] = hm < GQ ? a.qsum[((head0 + hm) * NG + gg) * 2 + 0] : 0.0f;
+            qs_lo[hb][gg] = hm < GQ ? a.qsum[((head0 + hm) * NG + gg) * 2 + 1] : 0.0f;
+        }
+    }
+    {
+        // lo parts: column n = gid carries head gid/2 (first block) or, for GQ = 8 and odd gid, head 4 + gid/2
+        const int h = (GQ == 8 && (gid & 1)) ? 4 + (gid >> 1) : ((gid & 1) ? GQ : (gid >> 1));
+#pragma unroll
+        for (int kk = 0; kk < NK; ++kk) {
+            uint2 v = make_uint2(0u, 0u);
+            if (h < GQ) v = *reinterpret_cast<const uint2*>(a.qb + ((head0 + h) * 3 + 2) * D + 16 * kk + 4 * tig);
+            qB2[kk][0] = v.x;
+            qB2[kk][1] = v.y;
+        }
+    }
+
+    const float pvs = a.pv_scale[kv];
+    float O[NHB][NK][4];
+#pragma unroll
+    for (int hb = 0; hb < NHB; ++hb)
+#pragma unroll
+        for (int mm = 0; mm < NK; ++mm)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) O[hb][mm][e] = 0.0f;
+    float m_run[NHB], l_run[NHB], zacc[NHB][NG];
+#pragma unroll
+    for (int hb = 0; hb < NHB; ++hb) {
+        m_run[hb] = -INFINITY;
+        l_run[hb] = 0.0f;
+#pragma unroll
+        for (int gg = 0; gg < NG; ++gg) zacc[hb][gg] = 0.0f;
+    }
+
+    // ---- page pipeline: kStages bulk copies in flight per warp
+    uint8_t* my_stage = stage_base + (size_t)warp * kStages * GE::kBlock;
+    const uint32_t stage_s = (uint32_t)__cvta_generic_to_shared(my_stage);
+    const uint32_t bar_s = (uint32_t)__cvta_generic_to_shared(bars + warp * kStages);
+    if (lane == 0) {
+        for (int s = 0; s < kStages; ++s) mbar_init(bar_s + 8 * s, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncwarp();
+    const int32_t* table = a.int2_tables + (size_t)b * a.int2_stride;
+    uint32_t valid_mask = 0u;    // bit s: stage s holds a real page
+    auto issue = [&](int j) {
+        const int s = j % kStages;
+        const int32_t phys = table[first + kWarps * j];
+        const bool ok = phys >= 0 && phys < a.int2_pages;
+        if (!ok && a.debug && lane == 0) record_error(&a.dbg->kind, &a.dbg->index, 2, phys);
+        valid_mask = ok ? (valid_mask | (1u << s)) : (valid_mask & ~(1u << s));
+        if (lane == 0) {
+            if (ok)
+                bulk_load(stage_s + s * GE::kBlock, a.int2_pool + ((size_t)phys * a.h_kv + kv) * GE::kBlock,
+                          GE::kBlock, bar_s + 8 * s);
+            else
+                mbar_arrive(bar_s + 8 * s);
+        }
+    };
+    for (int j = 0; j < kStages && j < n_mine; ++j) issue(j);
+
+    bool failed = false;
+    int j = 0;
+    for (; j < n_mine; ++j) {
+        const int s = j % kStages;
+        const uint32_t phase = (j / kStages) & 1;
+        if (!__all_sync(0xffffffffu, mbar_wait(bar_s + 8 * s, phase))) {
+            failed = true;
+            break;
+        }
+        const int pg = first + kWarps * j;
+        const uint8_t* sb = my_stage + s * GE::kBlock;
+        if (valid_mask & (1u << s)) {
+            const int nvalid = min(kPage, len - pg * kPage);
+            const bool v0 = gid < nvalid, v1 = gid + 8 < nvalid;
+
+            // ---- QK^T on tensor cores: A = K codes [16 tokens x 16 channels], B = query parts
+            uint32_t kw0[KW], kw1[KW];
+            if constexpr (KW == 2) {
+                const uint2 u0 = *reinterpret_cast<const uint2*>(sb + gid * GE::kCodeRow + 8 * tig);
+                const uint2 u1 = *reinterpret_cast<const uint2*>(sb + (gid + 8) * GE::kCodeRow + 8 * tig);
+                kw0[0] = u0.x; kw0[1] = u0.y; kw1[0] = u1.x; kw1[1] = u1.y;
+            } else {
+                kw0[0] = *reinterpret_cast<const uint32_t*>(sb + gid * GE::kCodeRow + 4 * tig);
+                kw1[0] = *reinterpret_cast<const uint32_t*>(sb + (gid + 8) * GE::kCodeRow + 4 * tig);
+            }
+            float S1[NG][NHB][4], S2[NG][4];
+#pragma unroll
+            for (int gg = 0; gg < NG; ++gg) {
+#pragma unroll
+                for (int e = 0; e < 4; ++e) S2[gg][e] = 0.0f;
+#pragma unroll
+                for (int hb = 0; hb < NHB; ++hb)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) S1[gg][hb][e] = 0.0f;
+            }
+#pragma unroll
+            for (int kk = 0; kk < NK; ++kk) {
+                const uint32_t w0 = kw0[kk / 4], w1 = kw1[kk / 4];
+                const uint32_t w0s = w0 >> 10, w1s = w1 >> 10;
+                uint32_t A0, A1, A2, A3;
+                switch (kk % 4) {
+                    case 0: A0 = code_pair<0>(w0, w0s); A1 = code_pair<0>(w1, w1s);
+                            A2 = code_pair<1>(w0, w0s); A3 = code_pair<1>(w1, w1s); break;
+                    case 1: A0 = code_pair<2>(w0, w0s); A1 = code_pair<2>(w1, w1s);
+                            A2 = code_pair<3>(w0, w0s); A3 = code_pair<3>(w1, w1s); break;
+                    case 2: A0 = code_pair<4>(w0, w0s); A1 = code_pair<4>(w1, w1s);
+                            A2 = code_pair<5>(w0, w0s); A3 = code_pair<5>(w1, w1s); break;
+                    default: A0 = code_pair<6>(w0, w0s); A1 = code_pair<6>(w1, w1s);
+                             A2 = code_pair<7>(w0, w0s); A3 = code_pair<7>(w1, w1s); break;
+                }
+                const int gg = kk / KPG;
+#pragma unroll
+                for (int hb = 0; hb < NHB; ++hb) mma16816(S1[gg][hb], A0, A1, A2, A3, qB1[kk][hb][0], qB1[kk][hb][1]);
+                mma16816(S2[gg], A0, A1, A2, A3, qB2[kk][0], qB2[kk][1]);
+            }
+
+            // ---- logits (hi + lo, log2 units) for tokens gid and gid+8 of head 4hb + tig
+            const __half2* ksz = reinterpret_cast<const __half2*>(sb + GE::kCodeBytes);
+            const __half2* vsz = reinterpret_cast<const __half2*>(sb + GE::kSeg + GE::kCodeBytes);
+            float Pv[NHB][NG][2];     // p * s_v for the two tokens
+#pragma unroll
+            for (int hb = 0; hb < NHB; ++hb) {
+                float lh[2], ll[2];
+#pragma unroll
+                for (int slot = 0; slot < 2; ++slot) {
+                    const int tok = gid + 8 * slot;
+                    float dh = 0.0f, dl = 0.0f;
+#pragma unroll
+                    for (int gg = 0; gg < NG; ++gg) {
+                        const float s_hi = __fmul_rn(S1[gg][hb][2 * slot], kap_h[hb]);
+                        const float lo_raw = (GQ == 8) ? S2[gg][2 * slot + hb] : S2[gg][2 * slot];
+                        const float s_r = __fmaf_rn(S1[gg][hb][2 * slot + 1], __fmul_rn(kap_h[hb], 0x1p-11f),
+                                                    __fmul_rn(lo_raw, __fmul_rn(kap_h[hb], 0x1p-22f)));
+                        const float2 sz = __half22float2(ksz[tok * NG + gg]);
+                        float p1, e1, p2, e2, t1, e3, t2, e4;
+                        two_prod(sz.x, s_hi, p1, e1);
+                        two_prod(sz.y, qs_hi[hb][gg], p2, e2);
+                        two_sum(p1, p2, t1, e3);
+                        const float low = __fadd_rn(__fadd_rn(e1, e2),
+                                                    __fadd_rn(e3, __fmaf_rn(sz.x, s_r, __fmul_rn(sz.y, qs_lo[hb][gg]))));
+                        two_sum(dh, t1, t2, e4);
+                        dh = t2;
+                        dl = __fadd_rn(dl, __fadd_rn(low, e4));
+                    }
+                    float p_, e_;
+                    two_prod(dh, a.scale_log2, p_, e_);
+                    lh[slot] = p_;
+                    ll[slot] = __fadd_rn(e_, __fmaf_rn(dl, a.scale_log2, __fmul_rn(dh, a.scale_log2_lo)));
+                }
+                const bool ok0 = v0 && (4 * hb + tig < GQ), ok1 = v1 && (4 * hb + tig < GQ);
+                if (!ok0) { lh[0] = -INFINITY; ll[0] = 0.0f; }
+                if (!ok1) { lh[1] = -INFINITY; ll[1] = 0.0f; }
+                // online softmax over the page (lanes sharing tig hold the same head)
+                float mp = fmaxf(lh[0], lh[1]);
+                mp = fmaxf(mp, __shfl_xor_sync(0xffffffffu, mp, 4));
+                mp = fmaxf(mp, __shfl_xor_sync(0xffffffffu, mp, 8));
+                mp = fmaxf(mp, __shfl_xor_sync(0xffffffffu, mp, 16));
+                const float mn = fmaxf(m_run[hb], mp);
+                float p0 = 0.0f, p1 = 0.0f, alpha = 1.0f;
+                if (mn != -INFINITY) {
+                    alpha = fast_exp2(m_run[hb] - mn);
+                    p0 = fast_exp2(__fadd_rn(__fsub_rn(lh[0], mn), ll[0]));
+                    p1 = fast_exp2(__fadd_rn(__fsub_rn(lh[1], mn), ll[1]));
+                    m_run[hb] = mn;
+                }
+                l_run[hb] = __fmaf_rn(l_run[hb], alpha, p0 + p1);
+                if (__any_sync(0xffffffffu, alpha != 1.0f)) {
+#pragma unroll
+                    for (int mm = 0; mm < NK; ++mm)
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) O[hb][mm][e] *= alpha;
+#pragma unroll
+                    for (int gg = 0; gg < NG; ++gg) zacc[hb][gg] *= alpha;
+                }
+#pragma unroll
+                for (int gg = 0; gg < NG; ++gg) {
+                    const float2 s0 = __half22float2(vsz[gid * NG + gg]);
+                    const float2 s1 = __half22float2(vsz[(gid + 8) * NG + gg]);
+                    Pv[hb][gg][0] = ok0 ? fminf(__fmul_rn(__fmul_rn(p0, s0.x), pvs), 65504.0f) : 0.0f;
+                    Pv[hb][gg][1] = ok1 ? fminf(__fmul_rn(__fmul_rn(p1, s1.x), pvs), 65504.0f) : 0.0f;
+                    if (ok0) zacc[hb][gg] = __fmaf_rn(p0, s0.y, zacc[hb][gg]);
+                    if (ok1) zacc[hb][gg] = __fmaf_rn(p1, s1.y, zacc[hb][gg]);
+                }
+            }
+
+            // ---- PV on tensor cores: A = V codes^T [16 channels x 16 tokens], B = p * s_v (hi, lo)
+            uint32_t X01, Y01, X23, Y23;
+            const uint8_t* vc = sb + GE::kSeg;
+            if constexpr (D == 128) {
+                const uint32_t wa = *reinterpret_cast<const uint32_t*>(vc + (2 * tig) * GE::kCodeRow + 4 * gid);
+                const uint32_t wb = *reinterpret_cast<const uint32_t*>(vc + (2 * tig + 1) * GE::kCodeRow + 4 * gid);
+                const uint32_t wc = *reinterpret_cast<const uint32_t*>(vc + (2 * tig + 8) * GE::kCodeRow + 4 * gid);
+                const uint32_t wd = *reinterpret_cast<const uint32_t*>(vc + (2 * tig + 9) * GE::kCodeRow + 4 * gid);
+                X01 = __byte_perm(wa, wb, 0x5410);
+                Y01 = __byte_perm(wa, wb, 0x7632);
+                X23 = __byte_perm(wc, wd, 0x5410);
+                Y23 = __byte_perm(wc, wd, 0x7632);
+            } else {
+                const uint32_t wa = *reinterpret_cast<const uint16_t*>(vc + (2 * tig) * GE::kCodeRow + 2 * gid);
+                const uint32_t wb = *reinterpret_cast<const uint16_t*>(vc + (2 * tig + 1) * GE::kCodeRow + 2 * gid);
+                const uint32_t wc = *reinterpret_cast<const uint16_t*>(vc + (2 * tig + 8) * GE::kCodeRow + 2 * gid);
+                const uint32_t wd = *reinterpret_cast<const uint16_t*>(vc + (2 * tig + 9) * GE::kCodeRow + 2 * gid);
+                X01 = __byte_perm(wa, wb, 0x5410);
+                X23 = __byte_perm(wc, wd, 0x5410);
+                Y01 = X01;
+                Y23 = X23;
+            }
+            const uint32_t X01s = X01 >> 10, Y01s = Y01 >> 10, X23s = X23 >> 10, Y23s = Y23 >> 10;
+            const bool part_lo = gid & 1;
+            const int srcA = 8 * tig + (gid >> 1), srcB = srcA + 4;
+#pragma unroll
+            for (int hb = 0; hb < NHB; ++hb) {
+#pragma unroll
+                for (int gg = 0; gg < NG; ++gg) {
+                    const float a0 = __shfl_sync(0xffffffffu, Pv[hb][gg][0], srcA);
+                    const float a1 = __shfl_sync(0xffffffffu, Pv[hb][gg][1], srcA);
+                    const float b0 = __shfl_sync(0xffffffffu, Pv[hb][gg][0], srcB);
+                    const float b1 = __shfl_sync(0xffffffffu, Pv[hb][gg][1], srcB);
+                    const uint32_t B0 = pack_half2(split_part(a0, part_lo), split_part(b0, part_lo));
+                    const uint32_t B1 = pack_half2(split_part(a1, part_lo), split_part(b1, part_lo));
+#pragma unroll
+                    for (int mm = gg * KPG; mm < (gg + 1) * KPG; ++mm) {
+                        uint32_t A0, A1, A2, A3;
+                        if constexpr (D == 128) {
+                            switch (mm) {
+                                case 0: A0 = code_pair_normal<0>(X01, X01s); A1 = code_pair_normal<0>(Y01, Y01s);
+                                        A2 = code_pair_normal<0>(X23, X23s); A3 = code_pair_normal<0>(Y23, Y23s); break;
+                                case 1: A0 = code_pair_normal<1>(X01, X01s); A1 = code_pair_normal<1>(Y01, Y01s);
+                                        A2 = code_pair_normal<1>(X23, X23s); A3 = code_pair_normal<1>(Y23, Y23s); break;
+                                case 2: A0 = code_pair_normal<2>(X01, X01s); A1 = code_pair_normal<2>(Y01, Y01s);
+                                        A2 = code_pair_normal<2>(X23, X23s); A3 = code_pair_normal<2>(Y23, Y23s); break;
+                                case 3: A0 = code_pair_normal<3>(X01, X01s); A1 = code_pair_normal<3>(Y01, Y01s);
+                                        A2 = code_pair_normal<3>(X23, X23s); A3 = code_pair_normal<3>(Y23, Y23s); break;
+                                case 4: A0 = code_pair_normal<4>(X01, X01s); A1 = code_pair_normal<4>(Y01, Y01s);
+                                        A2 = code_pair_normal<4>(X23, X23s); A3 = code_pair_normal<4>(Y23, Y23s); break;
+                                case 5: A0 = code_pair_normal<5>(X01, X01s); A1 = code_pair_normal<5>(Y01, Y01s);
+                                        A2 = code_pair_normal<5>(X23, X23s); A3 = code_pair_normal<5>(Y23, Y23s); break;
+                                case 6: A0 = code_pair_normal<6>(X01, X01s); A1 = code_pair_normal<6>(Y01, Y01s);
+                                        A2 = code_pair_normal<6>(X23, X23s); A3 = code_pair_normal<6>(Y23, Y23s); break;
+                                default: A0 = code_pair_normal<7>(X01, X01s); A1 = code_pair_normal<7>(Y01, Y01s);
+                                         A2 = code_pair_normal<7>(X23, X23s); A3 = code_pair_normal<7>(Y23, Y23s); break;
+                            }
+                        } else {
+                            // d = 64: rows gid at positions mm, rows gid+8 at positions 4+mm
+                            switch (mm) {
+                                case 0: A0 = code_pair_normal<0>(X01, X01s); A1 = code_pair_normal<4>(X01, X01s);
+                                        A2 = code_pair_normal<0>(X23, X23s); A3 = code_pair_normal<4>(X23, X23s); break;
+                                case 1: A0 = code_pair_normal<1>(X01, X01s); A1 = code_pair_normal<5>(X01, X01s);
+                                        A2 = code_pair_normal<1>(X23, X23s); A3 = code_pair_normal<5>(X23, X23s); break;
+                                case 2: A0 = code_pair_normal<2>(X01, X01s); A1 = code_pair_normal<6>(X01, X01s);
+                                        A2 = code_pair_normal<2>(X23, X23s); A3 = code_pair_normal<6>(X23, X23s); break;
+                                default: A0 = code_pair_normal<3>(X01, X01s); A1 = code_pair_normal<7>(X01, X01s);
+                                         A2 = code_pair_normal<3>(X23, X23s); A3 = code_pair_normal<7>(X23, X23s); break;
+                            }
+                        }
+                        mma16816(O[hb][mm], A0, A1, A2, A3, B0, B1);
+                    }
+                }
+            }
+        }
+        __syncwarp();
+        if (j + kStages < n_mine) issue(j + kStages);
+    }
+    if (failed) {
+        // record the stalled page, then drain the copies still in flight (bounded) before leaving
+        if (lane == 0) record_error(&a.dbg->kind, &a.dbg->index, 4, first + kWarps * j);
+        for (int jj = j; jj < n_mine && jj < j + kStages; ++jj)
+            (void)mbar_wait(bar_s + 8 * (jj % kStages), (jj / kStages) & 1);
+#pragma unroll
+        for (int hb = 0; hb < NHB; ++hb) { m_run[hb] = -INFINITY; l_run[hb] = 0.0f; }
+    }
+
+    // ---- this warp's state -> shared memory (scaled to the CTA max)
+#pragma unroll
+    for (int hb = 0; hb < NHB; ++hb) {
+        float l = l_run[hb];
+        l += __shfl_xor_sync(0xffffffffu, l, 4);
+        l += __shfl_xor_sync(0xffffffffu, l, 8);
+        l += __shfl_xor_sync(0xffffffffu, l, 16);
+        l_run[hb] = l;
+#pragma unroll
+        for (int gg = 0; gg < NG; ++gg) {
+            float z = zacc[hb][gg];
+            z += __shfl_xor_sync(0xffffffffu, z, 4);
+            z += __shfl_xor_sync(0xffffffffu, z, 8);
+            z += __shfl_xor_sync(0xffffffffu, z, 16);
+            zacc[hb][gg] = z;
+        }
+        const int h = 4 * hb + tig;
+        if (h < GQ && gid == 0) { ml_s[warp][h][0] = m_run[hb]; ml_s[warp][h][1] = l_run[hb]; }
+    }
+    __syncthreads();
+#pragma unroll
+    for (int hb = 0; hb < NHB; ++hb) {
+        const int h = 4 * hb + tig;
+        if (h >= GQ) continue;
+        float mm_ = -INFINITY;
+#pragma unroll
+        for (int w2 = 0; w2 < kWarps; ++w2) mm_ = fmaxf(mm_, ml_s[w2][h][0]);
+        const float f = m_run[hb] == -INFINITY ? 0.0f : fast_exp2(m_run[hb] - mm_);
+        if (f == 0.0f) continue;
+#pragma unroll
+        for (int mm = 0; mm < NK; ++mm) {
+            const int gg = mm / KPG;
+            // rows gid and gid+8 of m-step mm carry 2^(2p') of their code position and 2^sigma
+            const int pos0 = mm;
+            const int pos1 = (D == 128) ? mm : 4 + mm;
+            const float sc0 = ldexpf(1.0f, -2 * pos_scale(pos0)) / pvs;
+            const float sc1 = ldexpf(1.0f, -2 * pos_scale(pos1)) / pvs;
+            const float o0 = __fmaf_rn(O[hb][mm][1], 0x1p-11f, O[hb][mm][0]) * sc0 + zacc[hb][gg];
+            const float o1 = __fmaf_rn(O[hb][mm][3], 0x1p-11f, O[hb][mm][2]) * sc1 + zacc[hb][gg];
+            atomicAdd(&acc_s[h * D + 16 * mm + gid], o0 * f);
+            atomicAdd(&acc_s[h * D + 16 * mm + gid + 8], o1 * f);
+        }
+    }
+}
+
 // Online-softmax update for one page of 16 tokens held one token per lane
-// (lanes t and t+16 carry the same logit). Returns p for this lane's token.
-// Logits arrive as hi + lo (lo = 0 for the BF16 segment); m tracks the max of hi.
+// (lanes t and t+16 carry the same logit). Logits arrive as hi + lo.
 template <int GQ>
 __device__ __forceinline__ void softmax_page(float (&lg)[GQ], float (&lgl)[GQ], float (&m)[GQ], float (&l)[GQ],
                                              float (&alpha)[GQ], float (&p)[GQ]) {
@@ -139,7 +621,7 @@ __device__ __forceinline__ void softmax_page(float (&lg)[GQ], float (&lgl)[GQ], 
 #pragma unroll
         for (int o = 1; o < 16; o <<= 1) mp = fmaxf(mp, __shfl_xor_sync(0xffffffffu, mp, o));
         const float mn = fmaxf(m[h], mp);
-        if (mn == -INFINITY) {          // nothing valid yet
+        if (mn == -INFINITY) {
             alpha[h] = 1.0f;
             p[h] = 0.0f;
             continue;
@@ -154,276 +636,137 @@ __device__ __forceinline__ void softmax_page(float (&lg)[GQ], float (&lgl)[GQ], 
     }
 }
 
-template <int D, int G, int GQ>
-__global__ void __launch_bounds__(kWarps * 32)
-split_kernel(SplitArgs a) {
-    constexpr int n = D / 16;
-    constexpr int MPL = n / 2;          // V m-steps owned per lane (INT2)
-    constexpr int CPL = D / 32;         // channels per lane (BF16 PV)
-    constexpr int NG = D / G;
-    using GE = Geo<D, G>;
-
-    __shared__ __align__(16) float qs[GQ * D];     // INT2: grid part of q_rot; BF16: q
-    __shared__ __align__(16) float qrs[GQ * D];    // INT2: residual of q_rot
-    __shared__ float qsum_s[GQ][NG][2];
-    __shared__ float p_s[kWarps][16][GQ];
-    __shared__ float acc_s[GQ * D];
-    __shared__ float ml_s[kWarps][GQ][2];
-
-    const int split = blockIdx.x, kv = blockIdx.y, b = blockIdx.z;
+// BF16 sink/recent split on CUDA cores (<= 320 tokens per sequence).
+template <int D, int GQ>
+__device__ void bf16_split(const SplitArgs& a, int split, int kv, int b, float* qs, float (*p_s)[16][GQ],
+                           float* acc_s, float (*ml_s)[GQ][2]) {
+    constexpr int CPL = D / 32;
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const int t = lane & 15, hf = lane >> 4;
     const int h_q = a.h_kv * GQ;
-    const bool is_int2 = split < a.int2_splits;
-
-    for (int i = threadIdx.x; i < GQ * D; i += blockDim.x) {
-        const size_t qi = ((size_t)b * h_q + kv * GQ) * D + i;
-        qs[i] = is_int2 ? a.qg[qi] : __bfloat162float(a.q[qi]);
-        qrs[i] = is_int2 ? a.qr[qi] : 0.0f;
-        acc_s[i] = 0.0f;
-    }
-    if (threadIdx.x < GQ * NG * 2)
-        (&qsum_s[0][0][0])[threadIdx.x] = a.qsum[((size_t)b * h_q + kv * GQ) * NG * 2 + threadIdx.x];
+    for (int i = threadIdx.x; i < GQ * D; i += blockDim.x)
+        qs[i] = __bfloat162float(a.q[((size_t)b * h_q + kv * GQ) * D + i]);
     __syncthreads();
-
     float m[GQ], l[GQ];
 #pragma unroll
     for (int h = 0; h < GQ; ++h) { m[h] = -INFINITY; l[h] = 0.0f; }
+    const int bs = split - a.int2_splits;
+    int len = a.bf16_len[b];
+    const int cap = min(a.max_bf16, a.bf16_stride * kPage);
+    if (len < 0 || len > cap) {
+        if (a.debug && threadIdx.x == 0) record_error(&a.dbg->kind, &a.dbg->index, 3, len);
+        len = len < 0 ? 0 : cap;
+    }
+    const int n_pages = (len + kPage - 1) / kPage;
+    const int pg0 = bs * a.bf16_pages_per_split;
+    const int pg1 = min(n_pages, pg0 + a.bf16_pages_per_split);
+    float acc[GQ][CPL];
+#pragma unroll
+    for (int h = 0; h < GQ; ++h)
+#pragma unroll
+        for (int j = 0; j < CPL; ++j) acc[h][j] = 0.0f;
 
-    const int t = lane & 15, hf = lane >> 4;
-
-    if (is_int2) {
-        int len = a.hist_len[b];
-        const int cap = min(a.max_hist, a.int2_stride * kPage);
-        if (len < 0 || len > cap) {
-            if (a.debug && threadIdx.x == 0) record_error(&a.dbg->kind, &a.dbg->index, 3, len);
-            len = len < 0 ? 0 : cap;
+    for (int pg = pg0 + warp; pg < pg1; pg += kWarps) {
+        const int32_t phys = a.bf16_tables[(size_t)b * a.bf16_stride + pg];
+        if (phys < 0 || phys >= a.bf16_pages) {
+            if (a.debug && lane == 0) record_error(&a.dbg->kind, &a.dbg->index, 2, phys);
+            continue;
         }
-        const int n_pages = (len + kPage - 1) / kPage;
-        const int pg0 = split * a.pages_per_split;
-        const int pg1 = min(n_pages, pg0 + a.pages_per_split);
-
-        float acc[GQ][MPL];
+        const __nv_bfloat16* kp = a.bf16_pool + (((size_t)phys * a.h_kv + kv) * 2 + 0) * kPage * D;
+        const __nv_bfloat16* vp = kp + kPage * D;
+        const bool valid = pg * kPage + t < len;
+        float lg[GQ];
 #pragma unroll
-        for (int h = 0; h < GQ; ++h)
+        for (int h = 0; h < GQ; ++h) lg[h] = 0.0f;
+        const __nv_bfloat16* krow = kp + t * D + hf * (D / 2);
 #pragma unroll
-            for (int j = 0; j < MPL; ++j) acc[h][j] = 0.0f;
-
-        const int r = lane & 15, mh = lane >> 4;
-        const int vbase = 4 * n * (r % 8) + 2 * n * (r / 8) + 2 * MPL * mh;   // bit offset of this lane's V codes
-
-        for (int pg = pg0 + warp; pg < pg1; pg += kWarps) {
-            const int32_t phys = a.int2_tables[(size_t)b * a.int2_stride + pg];
-            if (phys < 0 || phys >= a.int2_pages) {
-                if (a.debug && lane == 0) record_error(&a.dbg->kind, &a.dbg->index, 2, phys);
-                continue;
-            }
-            const uint8_t* blk = a.int2_pool + ((size_t)phys * a.h_kv + kv) * GE::kBlock;
-            const uint8_t* kseg = blk;
-            const uint8_t* vseg = blk + GE::kSeg;
-            const bool valid = pg * kPage + t < len;
-
-            // ---- QK: lane = (token t, half hf of the K bit runs)
-            uint32_t w[n / 2];
-            if constexpr (D == 128) {
-                const uint4 u = *reinterpret_cast<const uint4*>(kseg + t * GE::kCodeRow + 16 * hf);
-                w[0] = u.x; w[1] = u.y; w[2] = u.z; w[3] = u.w;
-            } else {
-                const uint2 u = *reinterpret_cast<const uint2*>(kseg + t * GE::kCodeRow + 8 * hf);
-                w[0] = u.x; w[1] = u.y;
-            }
-            // S = sum_c code_c * q_rot_c per group: grid part exact, residual in fp32
-            float shi[GQ][NG], slo[GQ][NG];
+        for (int c8 = 0; c8 < D / 2; c8 += 8) {
+            const uint4 u = *reinterpret_cast<const uint4*>(krow + c8);
+            const __nv_bfloat162* k2 = reinterpret_cast<const __nv_bfloat162*>(&u);
 #pragma unroll
-            for (int h = 0; h < GQ; ++h)
-#pragma unroll
-                for (int gg = 0; gg < NG; ++gg) { shi[h][gg] = 0.0f; slo[h][gg] = 0.0f; }
-#pragma unroll
-            for (int tl = 0; tl < 2; ++tl)
-#pragma unroll
-                for (int kk = 0; kk < n; ++kk)
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        const int word = tl * (n / 4) + kk / 4;
-                        const int bit = 16 * (i % 2) + 2 * (2 * (kk % 4) + i / 2);
-                        const float cf = (float)((w[word] >> bit) & 3u);
-                        const int c = 16 * kk + 4 * (2 * hf + tl) + i;
-#pragma unroll
-                        for (int h = 0; h < GQ; ++h) {
-                            shi[h][(16 * kk) / G] = __fmaf_rn(qs[h * D + c], cf, shi[h][(16 * kk) / G]);
-                            slo[h][(16 * kk) / G] = __fmaf_rn(qrs[h * D + c], cf, slo[h][(16 * kk) / G]);
-                        }
-                    }
-            const __half2* ksz = reinterpret_cast<const __half2*>(kseg + GE::kCodeBytes) + t * NG;
-            float lg[GQ], lgl[GQ];
-#pragma unroll
-            for (int h = 0; h < GQ; ++h) {
-                // logit = sm2 * sum_g (s_g * S_g + z_g * Q_g), carried as hi + lo
-                float dh = 0.0f, dl = 0.0f;
-#pragma unroll
-                for (int gg = 0; gg < NG; ++gg) {
-                    const float sh = __fadd_rn(shi[h][gg], __shfl_xor_sync(0xffffffffu, shi[h][gg], 16));
-                    const float sl = __fadd_rn(slo[h][gg], __shfl_xor_sync(0xffffffffu, slo[h][gg], 16));
-                    const float2 sz = __half22float2(ksz[gg]);
-                    float p1, e1, p2, e2, t1, e3, t2, e4;
-                    two_prod(sz.x, sh, p1, e1);
-                    two_prod(sz.y, qsum_s[h][gg][0], p2, e2);
-                    two_sum(p1, p2, t1, e3);
-                    const float low = __fadd_rn(__fadd_rn(e1, e2), __fadd_rn(e3,
-                                      __fmaf_rn(sz.x, sl, __fmul_rn(sz.y, qsum_s[h][gg][1]))));
-                    two_sum(dh, t1, t2, e4);
-                    dh = t2;
-                    dl = __fadd_rn(dl, __fadd_rn(low, e4));
-                }
-                float lh, ll;
-                two_prod(dh, a.scale_log2, lh, ll);
-                ll = __fadd_rn(ll, __fmaf_rn(dl, a.scale_log2, __fmul_rn(dh, a.scale_log2_lo)));
-                lg[h] = valid ? lh : -INFINITY;
-                lgl[h] = valid ? ll : 0.0f;
-            }
-            float alpha[GQ], p[GQ];
-            softmax_page<GQ>(lg, lgl, m, l, alpha, p);
-            if (hf == 0) {
-#pragma unroll
-                for (int h = 0; h < GQ; ++h) p_s[warp][t][h] = p[h];
-            }
-            __syncwarp();
-
-            // ---- PV: lane = (row r, m-steps [MPL*mh, MPL*mh+MPL)) in the rotated basis
-#pragma unroll
-            for (int h = 0; h < GQ; ++h)
-#pragma unroll
-                for (int j = 0; j < MPL; ++j) acc[h][j] *= alpha[h];
-            const __half2* vsz = reinterpret_cast<const __half2*>(vseg + GE::kCodeBytes);
-            const int tmax = min(kPage, len - pg * kPage);
-            for (int tt = 0; tt < tmax; ++tt) {
-                const uint32_t byte = vseg[tt * GE::kCodeRow + vbase / 8];
-                const uint32_t bits = byte >> (vbase % 8);
-#pragma unroll
-                for (int j = 0; j < MPL; ++j) {
-                    const int grp = (16 * (MPL * mh + j) + r) / G;
-                    const float2 sz = __half22float2(vsz[tt * NG + grp]);
-                    const float cf = (float)((bits >> (2 * j)) & 3u);
-                    const float v = fmaf(cf, sz.x, sz.y);
-#pragma unroll
-                    for (int h = 0; h < GQ; ++h) acc[h][j] = fmaf(p_s[warp][tt][h], v, acc[h][j]);
-                }
-            }
-            __syncwarp();
-        }
-        // ---- combine the warps
-#pragma unroll
-        for (int h = 0; h < GQ; ++h)
-            if (lane == 0) { ml_s[warp][h][0] = m[h]; ml_s[warp][h][1] = l[h]; }
-        __syncthreads();
-#pragma unroll
-        for (int h = 0; h < GQ; ++h) {
-            float mm = -INFINITY;
-            for (int w2 = 0; w2 < kWarps; ++w2) mm = fmaxf(mm, ml_s[w2][h][0]);
-            const float f = (m[h] == -INFINITY) ? 0.0f : fast_exp2(m[h] - mm);
-#pragma unroll
-            for (int j = 0; j < MPL; ++j)
-                atomicAdd(&acc_s[h * D + 16 * (MPL * mh + j) + r], acc[h][j] * f);
-        }
-    } else {
-        // ---------------- BF16 sink/recent split
-        const int bs = split - a.int2_splits;
-        int len = a.bf16_len[b];
-        const int cap = min(a.max_bf16, a.bf16_stride * kPage);
-        if (len < 0 || len > cap) {
-            if (a.debug && threadIdx.x == 0) record_error(&a.dbg->kind, &a.dbg->index, 3, len);
-            len = len < 0 ? 0 : cap;
-        }
-        const int n_pages = (len + kPage - 1) / kPage;
-        const int pg0 = bs * a.bf16_pages_per_split;
-        const int pg1 = min(n_pages, pg0 + a.bf16_pages_per_split);
-        float acc[GQ][CPL];
-#pragma unroll
-        for (int h = 0; h < GQ; ++h)
-#pragma unroll
-            for (int j = 0; j < CPL; ++j) acc[h][j] = 0.0f;
-
-        for (int pg = pg0 + warp; pg < pg1; pg += kWarps) {
-            const int32_t phys = a.bf16_tables[(size_t)b * a.bf16_stride + pg];
-            if (phys < 0 || phys >= a.bf16_pages) {
-                if (a.debug && lane == 0) record_error(&a.dbg->kind, &a.dbg->index, 2, phys);
-                continue;
-            }
-            const __nv_bfloat16* kp = a.bf16_pool + (((size_t)phys * a.h_kv + kv) * 2 + 0) * kPage * D;
-            const __nv_bfloat16* vp = kp + kPage * D;
-            const bool valid = pg * kPage + t < len;
-            float lg[GQ];
-#pragma unroll
-            for (int h = 0; h < GQ; ++h) lg[h] = 0.0f;
-            const __nv_bfloat16* krow = kp + t * D + hf * (D / 2);
-#pragma unroll
-            for (int c8 = 0; c8 < D / 2; c8 += 8) {
-                const uint4 u = *reinterpret_cast<const uint4*>(krow + c8);
-                const __nv_bfloat162* k2 = reinterpret_cast<const __nv_bfloat162*>(&u);
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float2 kf = __bfloat1622float2(k2[e]);
-                    const int c = hf * (D / 2) + c8 + 2 * e;
-#pragma unroll
-                    for (int h = 0; h < GQ; ++h)
-                        lg[h] = fmaf(qs[h * D + c], kf.x, fmaf(qs[h * D + c + 1], kf.y, lg[h]));
-                }
-            }
-            float lgl[GQ];
-#pragma unroll
-            for (int h = 0; h < GQ; ++h) {
-                lg[h] += __shfl_xor_sync(0xffffffffu, lg[h], 16);
-                float lh, ll;
-                two_prod(lg[h], a.scale_log2, lh, ll);
-                ll = __fmaf_rn(lg[h], a.scale_log2_lo, ll);
-                lg[h] = valid ? lh : -INFINITY;
-                lgl[h] = valid ? ll : 0.0f;
-            }
-            float alpha[GQ], p[GQ];
-            softmax_page<GQ>(lg, lgl, m, l, alpha, p);
-            if (hf == 0) {
-#pragma unroll
-                for (int h = 0; h < GQ; ++h) p_s[warp][t][h] = p[h];
-            }
-            __syncwarp();
-#pragma unroll
-            for (int h = 0; h < GQ; ++h)
-#pragma unroll
-                for (int j = 0; j < CPL; ++j) acc[h][j] *= alpha[h];
-            const int tmax = min(kPage, len - pg * kPage);
-            for (int tt = 0; tt < tmax; ++tt) {
-                float v[CPL];
-                if constexpr (CPL == 4) {
-                    const uint2 u = *reinterpret_cast<const uint2*>(vp + tt * D + 4 * lane);
-                    const float2 a0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.x));
-                    const float2 a1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.y));
-                    v[0] = a0.x; v[1] = a0.y; v[2] = a1.x; v[3] = a1.y;
-                } else {
-                    const float2 a0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(vp + tt * D + 2 * lane));
-                    v[0] = a0.x; v[1] = a0.y;
-                }
+            for (int e = 0; e < 4; ++e) {
+                const float2 kf = __bfloat1622float2(k2[e]);
+                const int c = hf * (D / 2) + c8 + 2 * e;
 #pragma unroll
                 for (int h = 0; h < GQ; ++h)
-#pragma unroll
-                    for (int j = 0; j < CPL; ++j) acc[h][j] = fmaf(p_s[warp][tt][h], v[j], acc[h][j]);
+                    lg[h] = fmaf(qs[h * D + c], kf.x, fmaf(qs[h * D + c + 1], kf.y, lg[h]));
             }
-            __syncwarp();
         }
-#pragma unroll
-        for (int h = 0; h < GQ; ++h)
-            if (lane == 0) { ml_s[warp][h][0] = m[h]; ml_s[warp][h][1] = l[h]; }
-        __syncthreads();
+        float lgl[GQ];
 #pragma unroll
         for (int h = 0; h < GQ; ++h) {
-            float mm = -INFINITY;
-            for (int w2 = 0; w2 < kWarps; ++w2) mm = fmaxf(mm, ml_s[w2][h][0]);
-            const float f = (m[h] == -INFINITY) ? 0.0f : fast_exp2(m[h] - mm);
-#pragma unroll
-            for (int j = 0; j < CPL; ++j) atomicAdd(&acc_s[h * D + CPL * lane + j], acc[h][j] * f);
+            lg[h] += __shfl_xor_sync(0xffffffffu, lg[h], 16);
+            float lh, ll;
+            two_prod(lg[h], a.scale_log2, lh, ll);
+            ll = __fmaf_rn(lg[h], a.scale_log2_lo, ll);
+            lg[h] = valid ? lh : -INFINITY;
+            lgl[h] = valid ? ll : 0.0f;
         }
+        float alpha[GQ], p[GQ];
+        softmax_page<GQ>(lg, lgl, m, l, alpha, p);
+        if (hf == 0) {
+#pragma unroll
+            for (int h = 0; h < GQ; ++h) p_s[warp][t][h] = p[h];
+        }
+        __syncwarp();
+#pragma unroll
+        for (int h = 0; h < GQ; ++h)
+#pragma unroll
+            for (int j = 0; j < CPL; ++j) acc[h][j] *= alpha[h];
+        const int tmax = min(kPage, len - pg * kPage);
+        for (int tt = 0; tt < tmax; ++tt) {
+            float v[CPL];
+            if constexpr (CPL == 4) {
+                const uint2 u = *reinterpret_cast<const uint2*>(vp + tt * D + 4 * lane);
+                const float2 a0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.x));
+                const float2 a1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.y));
+                v[0] = a0.x; v[1] = a0.y; v[2] = a1.x; v[3] = a1.y;
+            } else {
+                const float2 a0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(vp + tt * D + 2 * lane));
+                v[0] = a0.x; v[1] = a0.y;
+            }
+#pragma unroll
+            for (int h = 0; h < GQ; ++h)
+#pragma unroll
+                for (int j = 0; j < CPL; ++j) acc[h][j] = fmaf(p_s[warp][tt][h], v[j], acc[h][j]);
+        }
+        __syncwarp();
     }
+#pragma unroll
+    for (int h = 0; h < GQ; ++h)
+        if (lane == 0) { ml_s[warp][h][0] = m[h]; ml_s[warp][h][1] = l[h]; }
+    __syncthreads();
+#pragma unroll
+    for (int h = 0; h < GQ; ++h) {
+        float mm = -INFINITY;
+        for (int w2 = 0; w2 < kWarps; ++w2) mm = fmaxf(mm, ml_s[w2][h][0]);
+        const float f = (m[h] == -INFINITY) ? 0.0f : fast_exp2(m[h] - mm);
+#pragma unroll
+        for (int j = 0; j < CPL; ++j) atomicAdd(&acc_s[h * D + CPL * lane + j], acc[h][j] * f);
+    }
+}
+
+template <int D, int G, int GQ>
+__global__ void __launch_bounds__(kWarps * 32, 3)
+split_kernel(SplitArgs a) {
+    extern __shared__ __align__(128) uint8_t dyn_smem[];
+    __shared__ __align__(8) uint64_t bars[kWarps * kStages];
+    __shared__ __align__(16) float acc_s[GQ * D];
+    __shared__ float ml_s[kWarps][GQ][2];
+    __shared__ float p_s[kWarps][16][GQ];
+
+    const int split = blockIdx.x, kv = blockIdx.y, b = blockIdx.z;
+    const int h_q = a.h_kv * GQ;
+    for (int i = threadIdx.x; i < GQ * D; i += blockDim.x) acc_s[i] = 0.0f;
     __syncthreads();
 
-    // ---- write the partial of each query head of the group
+    if (split < a.int2_splits)
+        int2_split<D, G, GQ>(a, split, kv, b, dyn_smem, bars, acc_s, ml_s);
+    else
+        bf16_split<D, GQ>(a, split, kv, b, reinterpret_cast<float*>(dyn_smem), p_s, acc_s, ml_s);
+    __syncthreads();
+
+    // ---- the partial of each query head of the group
     for (int h = 0; h < GQ; ++h) {
         float mm = -INFINITY;
         for (int w2 = 0; w2 < kWarps; ++w2) mm = fmaxf(mm, ml_s[w2][h][0]);
@@ -438,27 +781,45 @@ split_kernel(SplitArgs a) {
     }
 }
 
+// Merge of all splits of one query head: block of D threads; split weights in parallel.
 template <int D>
 __global__ void merge_kernel(const float* __restrict__ partials, const float* __restrict__ r_vt,
                              float* __restrict__ out, int h_q, int g, int int2_splits, int total_splits) {
+    extern __shared__ float w_s[];     // [total_splits]
     __shared__ float acc_rot[D];
+    __shared__ float red[D / 32];
     const int bh = blockIdx.x;
     const int kv = (bh % h_q) / g;
     const int c = threadIdx.x;
     const float* part = partials + (size_t)bh * total_splits * (D + 2);
+    float mloc = -INFINITY;
+    for (int s = c; s < total_splits; s += D) mloc = fmaxf(mloc, part[(size_t)s * (D + 2)]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mloc = fmaxf(mloc, __shfl_xor_sync(0xffffffffu, mloc, o));
+    if (c % 32 == 0) red[c / 32] = mloc;
+    __syncthreads();
     float mm = -INFINITY;
-    for (int s = 0; s < total_splits; ++s) mm = fmaxf(mm, part[(size_t)s * (D + 2)]);
-    float L = 0.0f, ai = 0.0f, ab = 0.0f;
-    if (mm != -INFINITY) {
-        for (int s = 0; s < total_splits; ++s) {
-            const float* ps = part + (size_t)s * (D + 2);
-            if (ps[0] == -INFINITY) continue;
-            const float w = fast_exp2(ps[0] - mm);
-            L = fmaf(ps[1], w, L);
-            if (s < int2_splits) ai = fmaf(ps[2 + c], w, ai);
-            else ab = fmaf(ps[2 + c], w, ab);
-        }
+#pragma unroll
+    for (int w = 0; w < D / 32; ++w) mm = fmaxf(mm, red[w]);
+    __syncthreads();
+    float lloc = 0.0f;
+    for (int s = c; s < total_splits; s += D) {
+        const float ms = part[(size_t)s * (D + 2)];
+        const float w = (mm == -INFINITY || ms == -INFINITY) ? 0.0f : fast_exp2(ms - mm);
+        w_s[s] = w;
+        lloc = fmaf(part[(size_t)s * (D + 2) + 1], w, lloc);
     }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) lloc += __shfl_xor_sync(0xffffffffu, lloc, o);
+    if (c % 32 == 0) red[c / 32] = lloc;
+    __syncthreads();
+    float L = 0.0f;
+#pragma unroll
+    for (int w = 0; w < D / 32; ++w) L += red[w];
+    float ai = 0.0f, ab = 0.0f;
+#pragma unroll 4
+    for (int s = 0; s < int2_splits; ++s) ai = fmaf(part[(size_t)s * (D + 2) + 2 + c], w_s[s], ai);
+    for (int s = int2_splits; s < total_splits; ++s) ab = fmaf(part[(size_t)s * (D + 2) + 2 + c], w_s[s], ab);
     acc_rot[c] = ai;
     __syncthreads();
     const float* rt = r_vt + (size_t)kv * D * D;
@@ -470,8 +831,12 @@ __global__ void merge_kernel(const float* __restrict__ partials, const float* __
 
 template <int D, int G, int GQ>
 cudaError_t launch_split(const SplitArgs& a, int batch, cudaStream_t st) {
+    auto kern = split_kernel<D, G, GQ>;
+    const size_t smem = SplitSmem<D, G, GQ>::kDynamic;
+    static cudaError_t attr = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (attr != cudaSuccess) return attr;
     dim3 grid(a.total_splits, a.h_kv, batch);
-    split_kernel<D, G, GQ><<<grid, kWarps * 32, 0, st>>>(a);
+    kern<<<grid, kWarps * 32, smem, st>>>(a);
     return cudaGetLastError();
 }
 
@@ -494,6 +859,7 @@ DecodePlan plan_decode(const Shape& s, int num_sms, int batch, int max_hist) {
     DecodePlan p{};
     const int max_pages = (max_hist + kPage - 1) / kPage;
     const int units = batch * s.h_kv;
+    // about four CTAs of 4 warps per SM in one wave
     int splits = units > 0 ? (4 * num_sms + units - 1) / units : 1;
     if (splits < 1) splits = 1;
     if (max_pages > 0 && splits > max_pages) splits = max_pages;
@@ -503,7 +869,8 @@ DecodePlan plan_decode(const Shape& s, int num_sms, int batch, int max_hist) {
     p.bf16_splits = 1;
     p.total_splits = p.int2_splits + p.bf16_splits;
     p.ws_partials = align256((size_t)batch * s.h_q * p.total_splits * (s.d + 2) * sizeof(float));
-    p.ws_qrot = align256((size_t)batch * s.h_q * (2 * s.d + 2 * (s.d / s.group)) * sizeof(float));
+    p.ws_qrot = align256((size_t)batch * s.h_q * (3 * s.d * sizeof(__half) + sizeof(float) +
+                                                 2 * (s.d / s.group) * sizeof(float)) + 256);
     p.ws_total = p.ws_partials + p.ws_qrot;
     return p;
 }
@@ -512,16 +879,18 @@ cudaError_t launch_decode(const Shape& s, const LayerParams& prm, const DecodePl
                           const DecodeArgs& a, DebugWord* dbg, Profiler* prof, cudaStream_t st) {
     const int g = s.h_q / s.h_kv;
     float* partials = static_cast<float*>(a.ws);
-    float* qg = reinterpret_cast<float*>(static_cast<char*>(a.ws) + plan.ws_partials);
-    float* qr = qg + (size_t)a.batch * s.h_q * s.d;
-    float* qsum = qr + (size_t)a.batch * s.h_q * s.d;
+    char* qbase = static_cast<char*>(a.ws) + plan.ws_partials;
+    const size_t nh = (size_t)a.batch * s.h_q;
+    __half* qb = reinterpret_cast<__half*>(qbase);
+    float* kap = reinterpret_cast<float*>(qbase + align256(nh * 3 * s.d * sizeof(__half)));
+    float* qsum = kap + nh;
     const __nv_bfloat16* q = static_cast<const __nv_bfloat16*>(a.q);
 
     {
         ProfScope ps(prof, OSCAR_KERNEL_QROT, st);
 #define OSCAR_QPREP_CASE(D_, G_) \
         if (s.d == D_ && s.group == G_) \
-            q_prep_kernel<D_, G_><<<a.batch * s.h_q, D_, 0, st>>>(q, prm.r_k, qg, qr, qsum, s.h_q, g);
+            q_prep_kernel<D_, G_><<<a.batch * s.h_q, D_, 0, st>>>(q, prm.r_k, qb, kap, qsum, s.h_q, g);
         OSCAR_QPREP_CASE(64, 32)
         OSCAR_QPREP_CASE(64, 64)
         OSCAR_QPREP_CASE(128, 32)
@@ -533,7 +902,7 @@ cudaError_t launch_decode(const Shape& s, const LayerParams& prm, const DecodePl
     if (e != cudaSuccess) return e;
 
     SplitArgs sa{};
-    sa.qg = qg; sa.qr = qr; sa.qsum = qsum; sa.q = q;
+    sa.qb = qb; sa.kap = kap; sa.qsum = qsum; sa.q = q; sa.pv_scale = prm.pv_scale;
     sa.int2_pool = a.int2_pool; sa.int2_pages = a.int2_pages;
     sa.int2_tables = a.int2_tables; sa.int2_stride = a.int2_stride;
     sa.hist_len = a.hist_len; sa.max_hist = a.max_hist;
@@ -566,13 +935,13 @@ cudaError_t launch_decode(const Shape& s, const LayerParams& prm, const DecodePl
     if (e != cudaSuccess) return e;
 
     ProfScope ps_merge(prof, OSCAR_KERNEL_MERGE, st);
-
+    const size_t msmem = (size_t)plan.total_splits * sizeof(float);
     if (s.d == 128)
-        merge_kernel<128><<<a.batch * s.h_q, 128, 0, st>>>(partials, prm.r_vt, a.out, s.h_q, g,
-                                                           plan.int2_splits, plan.total_splits);
+        merge_kernel<128><<<a.batch * s.h_q, 128, msmem, st>>>(partials, prm.r_vt, a.out, s.h_q, g,
+                                                               plan.int2_splits, plan.total_splits);
     else
-        merge_kernel<64><<<a.batch * s.h_q, 64, 0, st>>>(partials, prm.r_vt, a.out, s.h_q, g,
-                                                         plan.int2_splits, plan.total_splits);
+        merge_kernel<64><<<a.batch * s.h_q, 64, msmem, st>>>(partials, prm.r_vt, a.out, s.h_q, g,
+                                                             plan.int2_splits, plan.total_splits);
     return cudaGetLastError();
 }
 

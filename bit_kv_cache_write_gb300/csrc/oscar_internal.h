@@ -20,6 +20,7 @@ struct LayerParams {
     const float* r_vt;     // [H_kv][d][d], r_vt[h][i][c] = r_v[h][c][i]
     const float* t_k;      // [H_kv][d]
     const float* t_v;      // [H_kv][d]
+    const float* pv_scale; // [H_kv] 2^sigma with (2/3) max T_v * 2^sigma <= 32752: keeps p * s_v * 2^sigma in fp16
 };
 
 struct Shape {
