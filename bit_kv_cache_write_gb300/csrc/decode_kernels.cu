@@ -39,6 +39,7 @@
 #include <cuda_fp16.h>
 #include <cfloat>
 #include <cmath>
+#include <type_traits>
 
 #include "layout.cuh"
 #include "oscar_internal.h"
@@ -146,38 +147,44 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t phase) {
 //   kap = 2^(E + 9): S_part = accumulator * kap * 2^(-11 part);
 //   qsum[g] = sum over group g of q_rot (hi, lo).
 template <int D, int G>
-__global__ void q_prep_kernel(const __nv_bfloat16* __restrict__ q, const float* __restrict__ r_k,
-                              __half* __restrict__ qb, float* __restrict__ kap, float* __restrict__ qsum,
-                              int h_q, int g) {
+__global__ void __launch_bounds__(4 * D)
+q_prep_kernel(const __nv_bfloat16* __restrict__ q, const float* __restrict__ r_k,
+              __half* __restrict__ qb, float* __restrict__ kap, float* __restrict__ qsum, int h_q, int g) {
     constexpr int NG = D / G;
+    constexpr int Q4 = D / 4;                      // terms per thread: four threads per output channel
     __shared__ float qs[D];
+    __shared__ float hi_s[4][D], lo_s[4][D];
     __shared__ float wmax[D / 32];
-    __shared__ double part_s[D];
+    __shared__ double gsum[D / 32];
     const int bh = blockIdx.x;
     const int kv = (bh % h_q) / g;
-    const int c = threadIdx.x;
-    qs[c] = __bfloat162float(q[(size_t)bh * D + c]);
+    const int c = threadIdx.x % D, quarter = threadIdx.x / D;
+    if (threadIdx.x < D) qs[c] = __bfloat162float(q[(size_t)bh * D + c]);
     __syncthreads();
-    const float* r = r_k + (size_t)kv * D * D;
-    float hi[4] = {0.f, 0.f, 0.f, 0.f}, lo[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 2
-    for (int i = 0; i < D; i += 4) {
+    const float* r = r_k + (size_t)kv * D * D + (size_t)quarter * Q4 * D + c;
+    float rv[Q4];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            float p, e, s2, e2;
-            two_prod(qs[i + u], __ldg(r + (i + u) * D + c), p, e);
-            two_sum(hi[u], p, s2, e2);
-            hi[u] = s2;
-            lo[u] = __fadd_rn(lo[u], __fadd_rn(e, e2));
-        }
+    for (int i = 0; i < Q4; ++i) rv[i] = __ldg(r + (size_t)i * D);       // all loads in flight at once
+    float hi = 0.0f, lo = 0.0f;
+#pragma unroll
+    for (int i = 0; i < Q4; ++i) {
+        float p, e, s2, e2;
+        two_prod(qs[quarter * Q4 + i], rv[i], p, e);
+        two_sum(hi, p, s2, e2);
+        hi = s2;
+        lo = __fadd_rn(lo, __fadd_rn(e, e2));
     }
+    hi_s[quarter][c] = hi;
+    lo_s[quarter][c] = lo;
+    __syncthreads();
+    if (quarter != 0) return;
     float h = 0.0f, l = 0.0f;
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
         float s2, e2;
-        two_sum(h, hi[u], s2, e2);
+        two_sum(h, hi_s[u][c], s2, e2);
         h = s2;
-        l = __fadd_rn(l, __fadd_rn(lo[u], e2));
+        l = __fadd_rn(l, __fadd_rn(lo_s[u][c], e2));
     }
     {
         float s2, e2;
@@ -185,12 +192,16 @@ __global__ void q_prep_kernel(const __nv_bfloat16* __restrict__ q, const float* 
         h = s2;
         l = e2;
     }
+    // warp max |q_rot| and warp fp64 sums (a warp's 32 channels lie inside one group, G >= 32)
     float m = fabsf(h);
+    double sum = (double)h + (double)l;
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-    if (c % 32 == 0) wmax[c / 32] = m;
-    part_s[c] = (double)h + (double)l;
-    __syncthreads();
+    for (int o = 16; o > 0; o >>= 1) {
+        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+        sum += __shfl_xor_sync(0xffffffffu, sum, o);
+    }
+    if (c % 32 == 0) { wmax[c / 32] = m; gsum[c / 32] = sum; }
+    asm volatile("bar.sync 1, %0;" :: "r"(D) : "memory");     // the D threads of quarter 0 only
     m = 0.0f;
 #pragma unroll
     for (int w = 0; w < D / 32; ++w) m = fmaxf(m, wmax[w]);
@@ -212,11 +223,12 @@ __global__ void q_prep_kernel(const __nv_bfloat16* __restrict__ q, const float* 
     dst[2 * D + c] = __float2half_rn(any ? ldexpf(r_lo, sh) : 0.0f);
     if (c == 0) kap[bh] = any ? ldexpf(1.0f, ex + 9) : 0.0f;
     if (c < NG) {
-        double sum = 0.0;
-        for (int j = 0; j < G; ++j) sum += part_s[c * G + j];
-        const float sh2 = (float)sum;
+        double gs = 0.0;
+#pragma unroll
+        for (int w = 0; w < G / 32; ++w) gs += gsum[c * (G / 32) + w];
+        const float sh2 = (float)gs;
         qsum[((size_t)bh * NG + c) * 2 + 0] = sh2;
-        qsum[((size_t)bh * NG + c) * 2 + 1] = (float)(sum - (double)sh2);
+        qsum[((size_t)bh * NG + c) * 2 + 1] = (float)(gs - (double)sh2);
     }
 }
 
@@ -248,6 +260,45 @@ struct SplitSmem {
     static constexpr size_t kDynamic = (size_t)kWarps * kStages * kBlock;
 };
 
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// d = 128 / d = 64 code pair selection for the V operand of m-step mm: rows gid (R0, R2) and
+// rows gid+8 (R1, R3); d = 128 takes both from position mm of the low / high half-words, d = 64
+// from positions mm and 4+mm of one half-word.
+template <int D, int MM>
+__device__ __forceinline__ void v_operand(uint32_t X01, uint32_t X01s, uint32_t Y01, uint32_t Y01s, uint32_t X23,
+                                          uint32_t X23s, uint32_t Y23, uint32_t Y23s, uint32_t& A0, uint32_t& A1,
+                                          uint32_t& A2, uint32_t& A3) {
+    if constexpr (D == 128) {
+        A0 = code_pair_normal<MM>(X01, X01s); A1 = code_pair_normal<MM>(Y01, Y01s);
+        A2 = code_pair_normal<MM>(X23, X23s); A3 = code_pair_normal<MM>(Y23, Y23s);
+    } else {
+        A0 = code_pair_normal<MM>(X01, X01s); A1 = code_pair_normal<4 + MM>(X01, X01s);
+        A2 = code_pair_normal<MM>(X23, X23s); A3 = code_pair_normal<4 + MM>(X23, X23s);
+    }
+}
+
+template <int D, int KK>
+__device__ __forceinline__ void k_operand(const uint32_t (&kw0)[2], const uint32_t (&kw1)[2], uint32_t& A0,
+                                          uint32_t& A1, uint32_t& A2, uint32_t& A3) {
+    constexpr int W = KK / 4, P = 2 * (KK % 4);
+    const uint32_t w0 = kw0[W], w1 = kw1[W];
+    A0 = code_pair<P>(w0, w0 >> 10); A1 = code_pair<P>(w1, w1 >> 10);
+    A2 = code_pair<P + 1>(w0, w0 >> 10); A3 = code_pair<P + 1>(w1, w1 >> 10);
+}
+
+template <int N, typename F>
+__device__ __forceinline__ void static_for(F&& f) {
+    if constexpr (N > 0) {
+        static_for<N - 1>(f);
+        f(std::integral_constant<int, N - 1>{});
+    }
+}
+
 // INT2 history split on tensor cores. Writes this warp's state into acc_s / ml_s.
 template <int D, int G, int GQ>
 __device__ void int2_split(const SplitArgs& a, int split, int kv, int b, uint8_t* stage_base, uint64_t* bars,
@@ -257,7 +308,6 @@ __device__ void int2_split(const SplitArgs& a, int split, int kv, int b, uint8_t
     constexpr int NG = D / G;
     constexpr int KPG = G / 16;         // k-steps per group
     constexpr int NHB = (GQ + 3) / 4;   // blocks of 4 query heads
-    constexpr int KW = NK / 4;          // K words per token in a quad lane's run
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const int gid = lane >> 2, tig = lane & 3;
     const int h_q = a.h_kv * GQ;
@@ -274,10 +324,15 @@ __device__ void int2_split(const SplitArgs& a, int split, int kv, int b, uint8_t
     const int pg1 = min(n_pages, pg0 + a.pages_per_split);
     const int first = pg0 + warp;
     const int n_mine = first < pg1 ? (pg1 - first + kWarps - 1) / kWarps : 0;
+    const int32_t* table = a.int2_tables + (size_t)b * a.int2_stride;
+    // page ids of this warp, 32 at a time across the lanes: chunk c (pages 32c .. 32c+31 of the warp)
+    // lives in ids0 (c even) or ids1 (c odd) and is refilled with chunk c+2 once all its pages are issued
+    int32_t ids0 = lane < n_mine ? table[first + kWarps * lane] : -1;
+    int32_t ids1 = lane + 32 < n_mine ? table[first + kWarps * (lane + 32)] : -1;
 
     // ---- query operands (constant over pages)
     uint32_t qB1[NK][NHB][2], qB2[NK][2];
-    float kap_h[NHB], qs_hi[NHB][NG], qs_lo[NHB][NG];
+    float kap_h[NHB], kap_m[NHB], kap_l[NHB], qs_hi[NHB][NG], qs_lo[NHB][NG];
 #pragma unroll
     for (int hb = 0; hb < NHB; ++hb) {
         const int h = 4 * hb + (gid >> 1);
@@ -291,6 +346,8 @@ __device__ void int2_split(const SplitArgs& a, int split, int kv, int b, uint8_t
         }
         const int hm = 4 * hb + tig;
         kap_h[hb] = hm < GQ ? a.kap[head0 + hm] : 0.0f;
+        kap_m[hb] = kap_h[hb] * 0x1p-11f;
+        kap_l[hb] = kap_h[hb] * 0x1p-22f;
 #pragma unroll
         for (int gg = 0; gg < NG; ++gg) {
             qs_hi[hb][gg] = hm < GQ ? a.qsum[((head0 + hm) * NG + gg) * 2 + 0] : 0.0f;
@@ -308,8 +365,9 @@ __device__ void int2_split(const SplitArgs& a, int split, int kv, int b, uint8_t
             qB2[kk][1] = v.y;
         }
     }
-
     const float pvs = a.pv_scale[kv];
+    const float sl2 = a.scale_log2, sl2_lo = a.scale_log2_lo;
+
     float O[NHB][NK][4];
 #pragma unroll
     for (int hb = 0; hb < NHB; ++hb)
@@ -335,11 +393,10 @@ __device__ void int2_split(const SplitArgs& a, int split, int kv, int b, uint8_t
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncwarp();
-    const int32_t* table = a.int2_tables + (size_t)b * a.int2_stride;
     uint32_t valid_mask = 0u;    // bit s: stage s holds a real page
     auto issue = [&](int j) {
         const int s = j % kStages;
-        const int32_t phys = table[first + kWarps * j];
+        const int32_t phys = __shfl_sync(0xffffffffu, ((j >> 5) & 1) ? ids1 : ids0, j & 31);
         const bool ok = phys >= 0 && phys < a.int2_pages;
         if (!ok && a.debug && lane == 0) record_error(&a.dbg->kind, &a.dbg->index, 2, phys);
         valid_mask = ok ? (valid_mask | (1u << s)) : (valid_mask & ~(1u << s));
@@ -369,14 +426,15 @@ __device__ void int2_split(const SplitArgs& a, int split, int kv, int b, uint8_t
             const bool v0 = gid < nvalid, v1 = gid + 8 < nvalid;
 
             // ---- QK^T on tensor cores: A = K codes [16 tokens x 16 channels], B = query parts
-            uint32_t kw0[KW], kw1[KW];
-            if constexpr (KW == 2) {
+            uint32_t kw0[2], kw1[2];
+            if constexpr (D == 128) {
                 const uint2 u0 = *reinterpret_cast<const uint2*>(sb + gid * GE::kCodeRow + 8 * tig);
                 const uint2 u1 = *reinterpret_cast<const uint2*>(sb + (gid + 8) * GE::kCodeRow + 8 * tig);
                 kw0[0] = u0.x; kw0[1] = u0.y; kw1[0] = u1.x; kw1[1] = u1.y;
             } else {
                 kw0[0] = *reinterpret_cast<const uint32_t*>(sb + gid * GE::kCodeRow + 4 * tig);
                 kw1[0] = *reinterpret_cast<const uint32_t*>(sb + (gid + 8) * GE::kCodeRow + 4 * tig);
+                kw0[1] = kw1[1] = 0u;
             }
             float S1[NG][NHB][4], S2[NG][4];
 #pragma unroll
@@ -388,31 +446,20 @@ __device__ void int2_split(const SplitArgs& a, int split, int kv, int b, uint8_t
 #pragma unroll
                     for (int e = 0; e < 4; ++e) S1[gg][hb][e] = 0.0f;
             }
-#pragma unroll
-            for (int kk = 0; kk < NK; ++kk) {
-                const uint32_t w0 = kw0[kk / 4], w1 = kw1[kk / 4];
-                const uint32_t w0s = w0 >> 10, w1s = w1 >> 10;
+            static_for<NK>([&](auto kkc) {
+                constexpr int kk = decltype(kkc)::value;
                 uint32_t A0, A1, A2, A3;
-                switch (kk % 4) {
-                    case 0: A0 = code_pair<0>(w0, w0s); A1 = code_pair<0>(w1, w1s);
-                            A2 = code_pair<1>(w0, w0s); A3 = code_pair<1>(w1, w1s); break;
-                    case 1: A0 = code_pair<2>(w0, w0s); A1 = code_pair<2>(w1, w1s);
-                            A2 = code_pair<3>(w0, w0s); A3 = code_pair<3>(w1, w1s); break;
-                    case 2: A0 = code_pair<4>(w0, w0s); A1 = code_pair<4>(w1, w1s);
-                            A2 = code_pair<5>(w0, w0s); A3 = code_pair<5>(w1, w1s); break;
-                    default: A0 = code_pair<6>(w0, w0s); A1 = code_pair<6>(w1, w1s);
-                             A2 = code_pair<7>(w0, w0s); A3 = code_pair<7>(w1, w1s); break;
-                }
-                const int gg = kk / KPG;
+                k_operand<D, kk>(kw0, kw1, A0, A1, A2, A3);
+                constexpr int gg = kk / KPG;
 #pragma unroll
                 for (int hb = 0; hb < NHB; ++hb) mma16816(S1[gg][hb], A0, A1, A2, A3, qB1[kk][hb][0], qB1[kk][hb][1]);
                 mma16816(S2[gg], A0, A1, A2, A3, qB2[kk][0], qB2[kk][1]);
-            }
+            });
 
             // ---- logits (hi + lo, log2 units) for tokens gid and gid+8 of head 4hb + tig
             const __half2* ksz = reinterpret_cast<const __half2*>(sb + GE::kCodeBytes);
             const __half2* vsz = reinterpret_cast<const __half2*>(sb + GE::kSeg + GE::kCodeBytes);
-            float Pv[NHB][NG][2];     // p * s_v for the two tokens
+            uint32_t Pv[NHB][NG][2];     // p * s_v * 2^sigma per token slot, as (hi, lo) fp16 pair
 #pragma unroll
             for (int hb = 0; hb < NHB; ++hb) {
                 float lh[2], ll[2];
@@ -422,25 +469,30 @@ __device__ void int2_split(const SplitArgs& a, int split, int kv, int b, uint8_t
                     float dh = 0.0f, dl = 0.0f;
 #pragma unroll
                     for (int gg = 0; gg < NG; ++gg) {
-                        const float s_hi = __fmul_rn(S1[gg][hb][2 * slot], kap_h[hb]);
                         const float lo_raw = (GQ == 8) ? S2[gg][2 * slot + hb] : S2[gg][2 * slot];
-                        const float s_r = __fmaf_rn(S1[gg][hb][2 * slot + 1], __fmul_rn(kap_h[hb], 0x1p-11f),
-                                                    __fmul_rn(lo_raw, __fmul_rn(kap_h[hb], 0x1p-22f)));
+                        const float s_hi = __fmul_rn(S1[gg][hb][2 * slot], kap_h[hb]);
+                        const float s_r = __fmaf_rn(S1[gg][hb][2 * slot + 1], kap_m[hb], __fmul_rn(lo_raw, kap_l[hb]));
                         const float2 sz = __half22float2(ksz[tok * NG + gg]);
-                        float p1, e1, p2, e2, t1, e3, t2, e4;
+                        float p1, e1, p2, e2, t1, e3;
                         two_prod(sz.x, s_hi, p1, e1);
                         two_prod(sz.y, qs_hi[hb][gg], p2, e2);
                         two_sum(p1, p2, t1, e3);
                         const float low = __fadd_rn(__fadd_rn(e1, e2),
                                                     __fadd_rn(e3, __fmaf_rn(sz.x, s_r, __fmul_rn(sz.y, qs_lo[hb][gg]))));
-                        two_sum(dh, t1, t2, e4);
-                        dh = t2;
-                        dl = __fadd_rn(dl, __fadd_rn(low, e4));
+                        if (NG == 1) {
+                            dh = t1;
+                            dl = low;
+                        } else {
+                            float t2, e4;
+                            two_sum(dh, t1, t2, e4);
+                            dh = t2;
+                            dl = __fadd_rn(dl, __fadd_rn(low, e4));
+                        }
                     }
                     float p_, e_;
-                    two_prod(dh, a.scale_log2, p_, e_);
+                    two_prod(dh, sl2, p_, e_);
                     lh[slot] = p_;
-                    ll[slot] = __fadd_rn(e_, __fmaf_rn(dl, a.scale_log2, __fmul_rn(dh, a.scale_log2_lo)));
+                    ll[slot] = __fadd_rn(e_, __fmaf_rn(dl, sl2, __fmul_rn(dh, sl2_lo)));
                 }
                 const bool ok0 = v0 && (4 * hb + tig < GQ), ok1 = v1 && (4 * hb + tig < GQ);
                 if (!ok0) { lh[0] = -INFINITY; ll[0] = 0.0f; }
@@ -453,9 +505,9 @@ __device__ void int2_split(const SplitArgs& a, int split, int kv, int b, uint8_t
                 const float mn = fmaxf(m_run[hb], mp);
                 float p0 = 0.0f, p1 = 0.0f, alpha = 1.0f;
                 if (mn != -INFINITY) {
-                    alpha = fast_exp2(m_run[hb] - mn);
-                    p0 = fast_exp2(__fadd_rn(__fsub_rn(lh[0], mn), ll[0]));
-                    p1 = fast_exp2(__fadd_rn(__fsub_rn(lh[1], mn), ll[1]));
+                    alpha = ex2(m_run[hb] - mn);
+                    p0 = ex2(__fadd_rn(__fsub_rn(lh[0], mn), ll[0]));
+                    p1 = ex2(__fadd_rn(__fsub_rn(lh[1], mn), ll[1]));
                     m_run[hb] = mn;
                 }
                 l_run[hb] = __fmaf_rn(l_run[hb], alpha, p0 + p1);
@@ -471,8 +523,11 @@ __device__ void int2_split(const SplitArgs& a, int split, int kv, int b, uint8_t
                 for (int gg = 0; gg < NG; ++gg) {
                     const float2 s0 = __half22float2(vsz[gid * NG + gg]);
                     const float2 s1 = __half22float2(vsz[(gid + 8) * NG + gg]);
-                    Pv[hb][gg][0] = ok0 ? fminf(__fmul_rn(__fmul_rn(p0, s0.x), pvs), 65504.0f) : 0.0f;
-                    Pv[hb][gg][1] = ok1 ? fminf(__fmul_rn(__fmul_rn(p1, s1.x), pvs), 65504.0f) : 0.0f;
+                    const float x0 = ok0 ? fminf(__fmul_rn(__fmul_rn(p0, s0.x), pvs), 65504.0f) : 0.0f;
+                    const float x1 = ok1 ? fminf(__fmul_rn(__fmul_rn(p1, s1.x), pvs), 65504.0f) : 0.0f;
+                    const __half h0 = __float2half_rn(x0), h1 = __float2half_rn(x1);
+                    Pv[hb][gg][0] = pack_half2(h0, __float2half_rn(__fmul_rn(__fsub_rn(x0, __half2float(h0)), 2048.0f)));
+                    Pv[hb][gg][1] = pack_half2(h1, __float2half_rn(__fmul_rn(__fsub_rn(x1, __half2float(h1)), 2048.0f)));
                     if (ok0) zacc[hb][gg] = __fmaf_rn(p0, s0.y, zacc[hb][gg]);
                     if (ok1) zacc[hb][gg] = __fmaf_rn(p1, s1.y, zacc[hb][gg]);
                 }
@@ -501,60 +556,40 @@ __device__ void int2_split(const SplitArgs& a, int split, int kv, int b, uint8_t
                 Y23 = X23;
             }
             const uint32_t X01s = X01 >> 10, Y01s = Y01 >> 10, X23s = X23 >> 10, Y23s = Y23 >> 10;
-            const bool part_lo = gid & 1;
+            // the (hi, lo) part this lane's B column needs: hi for even gid, lo for odd gid
+            const uint32_t sel = (gid & 1) ? 0x7632u : 0x5410u;
             const int srcA = 8 * tig + (gid >> 1), srcB = srcA + 4;
+            uint32_t Bf[NHB][NG][2];
 #pragma unroll
-            for (int hb = 0; hb < NHB; ++hb) {
+            for (int hb = 0; hb < NHB; ++hb)
 #pragma unroll
                 for (int gg = 0; gg < NG; ++gg) {
-                    const float a0 = __shfl_sync(0xffffffffu, Pv[hb][gg][0], srcA);
-                    const float a1 = __shfl_sync(0xffffffffu, Pv[hb][gg][1], srcA);
-                    const float b0 = __shfl_sync(0xffffffffu, Pv[hb][gg][0], srcB);
-                    const float b1 = __shfl_sync(0xffffffffu, Pv[hb][gg][1], srcB);
-                    const uint32_t B0 = pack_half2(split_part(a0, part_lo), split_part(b0, part_lo));
-                    const uint32_t B1 = pack_half2(split_part(a1, part_lo), split_part(b1, part_lo));
-#pragma unroll
-                    for (int mm = gg * KPG; mm < (gg + 1) * KPG; ++mm) {
-                        uint32_t A0, A1, A2, A3;
-                        if constexpr (D == 128) {
-                            switch (mm) {
-                                case 0: A0 = code_pair_normal<0>(X01, X01s); A1 = code_pair_normal<0>(Y01, Y01s);
-                                        A2 = code_pair_normal<0>(X23, X23s); A3 = code_pair_normal<0>(Y23, Y23s); break;
-                                case 1: A0 = code_pair_normal<1>(X01, X01s); A1 = code_pair_normal<1>(Y01, Y01s);
-                                        A2 = code_pair_normal<1>(X23, X23s); A3 = code_pair_normal<1>(Y23, Y23s); break;
-                                case 2: A0 = code_pair_normal<2>(X01, X01s); A1 = code_pair_normal<2>(Y01, Y01s);
-                                        A2 = code_pair_normal<2>(X23, X23s); A3 = code_pair_normal<2>(Y23, Y23s); break;
-                                case 3: A0 = code_pair_normal<3>(X01, X01s); A1 = code_pair_normal<3>(Y01, Y01s);
-                                        A2 = code_pair_normal<3>(X23, X23s); A3 = code_pair_normal<3>(Y23, Y23s); break;
-                                case 4: A0 = code_pair_normal<4>(X01, X01s); A1 = code_pair_normal<4>(Y01, Y01s);
-                                        A2 = code_pair_normal<4>(X23, X23s); A3 = code_pair_normal<4>(Y23, Y23s); break;
-                                case 5: A0 = code_pair_normal<5>(X01, X01s); A1 = code_pair_normal<5>(Y01, Y01s);
-                                        A2 = code_pair_normal<5>(X23, X23s); A3 = code_pair_normal<5>(Y23, Y23s); break;
-                                case 6: A0 = code_pair_normal<6>(X01, X01s); A1 = code_pair_normal<6>(Y01, Y01s);
-                                        A2 = code_pair_normal<6>(X23, X23s); A3 = code_pair_normal<6>(Y23, Y23s); break;
-                                default: A0 = code_pair_normal<7>(X01, X01s); A1 = code_pair_normal<7>(Y01, Y01s);
-                                         A2 = code_pair_normal<7>(X23, X23s); A3 = code_pair_normal<7>(Y23, Y23s); break;
-                            }
-                        } else {
-                            // d = 64: rows gid at positions mm, rows gid+8 at positions 4+mm
-                            switch (mm) {
-                                case 0: A0 = code_pair_normal<0>(X01, X01s); A1 = code_pair_normal<4>(X01, X01s);
-                                        A2 = code_pair_normal<0>(X23, X23s); A3 = code_pair_normal<4>(X23, X23s); break;
-                                case 1: A0 = code_pair_normal<1>(X01, X01s); A1 = code_pair_normal<5>(X01, X01s);
-                                        A2 = code_pair_normal<1>(X23, X23s); A3 = code_pair_normal<5>(X23, X23s); break;
-                                case 2: A0 = code_pair_normal<2>(X01, X01s); A1 = code_pair_normal<6>(X01, X01s);
-                                        A2 = code_pair_normal<2>(X23, X23s); A3 = code_pair_normal<6>(X23, X23s); break;
-                                default: A0 = code_pair_normal<3>(X01, X01s); A1 = code_pair_normal<7>(X01, X01s);
-                                         A2 = code_pair_normal<3>(X23, X23s); A3 = code_pair_normal<7>(X23, X23s); break;
-                            }
-                        }
-                        mma16816(O[hb][mm], A0, A1, A2, A3, B0, B1);
-                    }
+                    const uint32_t a0 = __shfl_sync(0xffffffffu, Pv[hb][gg][0], srcA);
+                    const uint32_t a1 = __shfl_sync(0xffffffffu, Pv[hb][gg][1], srcA);
+                    const uint32_t b0 = __shfl_sync(0xffffffffu, Pv[hb][gg][0], srcB);
+                    const uint32_t b1 = __shfl_sync(0xffffffffu, Pv[hb][gg][1], srcB);
+                    Bf[hb][gg][0] = __byte_perm(a0, b0, sel);
+                    Bf[hb][gg][1] = __byte_perm(a1, b1, sel);
                 }
-            }
+            static_for<NK>([&](auto mc) {
+                constexpr int mm = decltype(mc)::value;
+                constexpr int gg = mm / KPG;
+                uint32_t A0, A1, A2, A3;
+                v_operand<D, mm>(X01, X01s, Y01, Y01s, X23, X23s, Y23, Y23s, A0, A1, A2, A3);
+#pragma unroll
+                for (int hb = 0; hb < NHB; ++hb) mma16816(O[hb][mm], A0, A1, A2, A3, Bf[hb][gg][0], Bf[hb][gg][1]);
+            });
         }
         __syncwarp();
-        if (j + kStages < n_mine) issue(j + kStages);
+        if (j + kStages < n_mine) {
+            const int ji = j + kStages;
+            issue(ji);
+            if ((ji & 31) == 31) {                // chunk ji/32 fully issued: load chunk ji/32 + 2 into its slot
+                const int nj = ji + 33 + lane;
+                const int32_t v = nj < n_mine ? table[first + kWarps * nj] : -1;
+                if ((ji >> 5) & 1) ids1 = v; else ids0 = v;
+            }
+        }
     }
     if (failed) {
         // record the stalled page, then drain the copies still in flight (bounded) before leaving
@@ -747,7 +782,7 @@ __device__ void bf16_split(const SplitArgs& a, int split, int kv, int b, float* 
 }
 
 template <int D, int G, int GQ>
-__global__ void __launch_bounds__(kWarps * 32, 3)
+__global__ void __launch_bounds__(kWarps * 32, GQ == 8 ? 2 : 4)
 split_kernel(SplitArgs a) {
     extern __shared__ __align__(128) uint8_t dyn_smem[];
     __shared__ __align__(8) uint64_t bars[kWarps * kStages];
@@ -781,29 +816,32 @@ split_kernel(SplitArgs a) {
     }
 }
 
-// Merge of all splits of one query head: block of D threads; split weights in parallel.
+// Merge of all splits of one query head. Block of 4*D threads: thread (c, quarter) sums a quarter of
+// the splits for channel c and a quarter of the un-rotation terms, so its loads are independent.
 template <int D>
-__global__ void merge_kernel(const float* __restrict__ partials, const float* __restrict__ r_vt,
-                             float* __restrict__ out, int h_q, int g, int int2_splits, int total_splits) {
+__global__ void __launch_bounds__(4 * D)
+merge_kernel(const float* __restrict__ partials, const float* __restrict__ r_vt,
+             float* __restrict__ out, int h_q, int g, int int2_splits, int total_splits) {
     extern __shared__ float w_s[];     // [total_splits]
     __shared__ float acc_rot[D];
-    __shared__ float red[D / 32];
+    __shared__ float part_i[4][D], part_b[4][D];
+    __shared__ float red[4 * D / 32];
     const int bh = blockIdx.x;
     const int kv = (bh % h_q) / g;
-    const int c = threadIdx.x;
+    const int tid = threadIdx.x, c = tid % D, quarter = tid / D;
     const float* part = partials + (size_t)bh * total_splits * (D + 2);
     float mloc = -INFINITY;
-    for (int s = c; s < total_splits; s += D) mloc = fmaxf(mloc, part[(size_t)s * (D + 2)]);
+    for (int s = tid; s < total_splits; s += 4 * D) mloc = fmaxf(mloc, part[(size_t)s * (D + 2)]);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) mloc = fmaxf(mloc, __shfl_xor_sync(0xffffffffu, mloc, o));
-    if (c % 32 == 0) red[c / 32] = mloc;
+    if (tid % 32 == 0) red[tid / 32] = mloc;
     __syncthreads();
     float mm = -INFINITY;
 #pragma unroll
-    for (int w = 0; w < D / 32; ++w) mm = fmaxf(mm, red[w]);
+    for (int w = 0; w < 4 * D / 32; ++w) mm = fmaxf(mm, red[w]);
     __syncthreads();
     float lloc = 0.0f;
-    for (int s = c; s < total_splits; s += D) {
+    for (int s = tid; s < total_splits; s += 4 * D) {
         const float ms = part[(size_t)s * (D + 2)];
         const float w = (mm == -INFINITY || ms == -INFINITY) ? 0.0f : fast_exp2(ms - mm);
         w_s[s] = w;
@@ -811,22 +849,36 @@ __global__ void merge_kernel(const float* __restrict__ partials, const float* __
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) lloc += __shfl_xor_sync(0xffffffffu, lloc, o);
-    if (c % 32 == 0) red[c / 32] = lloc;
+    if (tid % 32 == 0) red[tid / 32] = lloc;
     __syncthreads();
     float L = 0.0f;
 #pragma unroll
-    for (int w = 0; w < D / 32; ++w) L += red[w];
+    for (int w = 0; w < 4 * D / 32; ++w) L += red[w];
     float ai = 0.0f, ab = 0.0f;
-#pragma unroll 4
-    for (int s = 0; s < int2_splits; ++s) ai = fmaf(part[(size_t)s * (D + 2) + 2 + c], w_s[s], ai);
-    for (int s = int2_splits; s < total_splits; ++s) ab = fmaf(part[(size_t)s * (D + 2) + 2 + c], w_s[s], ab);
-    acc_rot[c] = ai;
-    __syncthreads();
-    const float* rt = r_vt + (size_t)kv * D * D;
-    float o = 0.0f;
 #pragma unroll 8
-    for (int i = 0; i < D; ++i) o = fmaf(acc_rot[i], __ldg(rt + i * D + c), o);
-    out[(size_t)bh * D + c] = L > 0.0f ? (o + ab) / L : 0.0f;
+    for (int s = quarter; s < total_splits; s += 4) {
+        const float v = part[(size_t)s * (D + 2) + 2 + c] * w_s[s];
+        if (s < int2_splits) ai += v; else ab += v;
+    }
+    part_i[quarter][c] = ai;
+    part_b[quarter][c] = ab;
+    __syncthreads();
+    if (quarter == 0) acc_rot[c] = (part_i[0][c] + part_i[1][c]) + (part_i[2][c] + part_i[3][c]);
+    __syncthreads();
+    const float* rt = r_vt + (size_t)kv * D * D + (size_t)quarter * (D / 4) * D + c;
+    float rv[D / 4];
+#pragma unroll
+    for (int i = 0; i < D / 4; ++i) rv[i] = __ldg(rt + (size_t)i * D);
+    float o = 0.0f;
+#pragma unroll
+    for (int i = 0; i < D / 4; ++i) o = fmaf(acc_rot[quarter * (D / 4) + i], rv[i], o);
+    part_i[quarter][c] = o;
+    __syncthreads();
+    if (quarter == 0) {
+        const float oi = (part_i[0][c] + part_i[1][c]) + (part_i[2][c] + part_i[3][c]);
+        const float ob = (part_b[0][c] + part_b[1][c]) + (part_b[2][c] + part_b[3][c]);
+        out[(size_t)bh * D + c] = L > 0.0f ? (oi + ob) / L : 0.0f;
+    }
 }
 
 template <int D, int G, int GQ>
@@ -853,14 +905,50 @@ cudaError_t dispatch_gq(int gq, const SplitArgs& a, int batch, cudaStream_t st) 
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
+// Resident split CTAs per SM for the shape (queried once per instantiation).
+template <int D, int G, int GQ>
+int split_occupancy() {
+    static int occ = [] {
+        int n = 0;
+        auto kern = split_kernel<D, G, GQ>;
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SplitSmem<D, G, GQ>::kDynamic);
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, kWarps * 32, SplitSmem<D, G, GQ>::kDynamic) !=
+            cudaSuccess || n < 1) {
+            cudaGetLastError();
+            n = 1;
+        }
+        return n;
+    }();
+    return occ;
+}
+
+template <int D, int G>
+int occupancy_gq(int gq) {
+    switch (gq) {
+        case 1: return split_occupancy<D, G, 1>();
+        case 2: return split_occupancy<D, G, 2>();
+        case 4: return split_occupancy<D, G, 4>();
+        default: return split_occupancy<D, G, 8>();
+    }
+}
+
+int split_ctas_per_sm(const Shape& s) {
+    const int gq = s.h_q / s.h_kv;
+    if (s.d == 64) return s.group == 32 ? occupancy_gq<64, 32>(gq) : occupancy_gq<64, 64>(gq);
+    if (s.group == 32) return occupancy_gq<128, 32>(gq);
+    if (s.group == 64) return occupancy_gq<128, 64>(gq);
+    return occupancy_gq<128, 128>(gq);
+}
+
 }  // namespace
 
 DecodePlan plan_decode(const Shape& s, int num_sms, int batch, int max_hist) {
     DecodePlan p{};
     const int max_pages = (max_hist + kPage - 1) / kPage;
     const int units = batch * s.h_kv;
-    // about four CTAs of 4 warps per SM in one wave
-    int splits = units > 0 ? (4 * num_sms + units - 1) / units : 1;
+    // one wave: units * (INT2 splits + 1 BF16 split) resident CTAs
+    const int slots = split_ctas_per_sm(s) * num_sms;
+    int splits = units > 0 ? slots / units - 1 : 1;
     if (splits < 1) splits = 1;
     if (max_pages > 0 && splits > max_pages) splits = max_pages;
     if (max_pages == 0) splits = 1;
@@ -890,7 +978,7 @@ cudaError_t launch_decode(const Shape& s, const LayerParams& prm, const DecodePl
         ProfScope ps(prof, OSCAR_KERNEL_QROT, st);
 #define OSCAR_QPREP_CASE(D_, G_) \
         if (s.d == D_ && s.group == G_) \
-            q_prep_kernel<D_, G_><<<a.batch * s.h_q, D_, 0, st>>>(q, prm.r_k, qb, kap, qsum, s.h_q, g);
+            q_prep_kernel<D_, G_><<<a.batch * s.h_q, 4 * D_, 0, st>>>(q, prm.r_k, qb, kap, qsum, s.h_q, g);
         OSCAR_QPREP_CASE(64, 32)
         OSCAR_QPREP_CASE(64, 64)
         OSCAR_QPREP_CASE(128, 32)
@@ -937,10 +1025,10 @@ cudaError_t launch_decode(const Shape& s, const LayerParams& prm, const DecodePl
     ProfScope ps_merge(prof, OSCAR_KERNEL_MERGE, st);
     const size_t msmem = (size_t)plan.total_splits * sizeof(float);
     if (s.d == 128)
-        merge_kernel<128><<<a.batch * s.h_q, 128, msmem, st>>>(partials, prm.r_vt, a.out, s.h_q, g,
+        merge_kernel<128><<<a.batch * s.h_q, 4 * 128, msmem, st>>>(partials, prm.r_vt, a.out, s.h_q, g,
                                                                plan.int2_splits, plan.total_splits);
     else
-        merge_kernel<64><<<a.batch * s.h_q, 64, msmem, st>>>(partials, prm.r_vt, a.out, s.h_q, g,
+        merge_kernel<64><<<a.batch * s.h_q, 4 * 64, msmem, st>>>(partials, prm.r_vt, a.out, s.h_q, g,
                                                              plan.int2_splits, plan.total_splits);
     return cudaGetLastError();
 }

@@ -25,7 +25,7 @@ namespace oscar {
 namespace {
 
 constexpr int kWarps = 4;
-constexpr int kTok = 8;      // tokens per warp iteration (register blocking over R)
+constexpr long long kWaitCycles = 2000000000LL;   // give up on the R copy after ~1 s
 
 // Error-free transformations on fp32 (explicit _rn intrinsics: no contraction).
 __device__ __forceinline__ void two_sum(float a, float b, float& s, float& e) {
@@ -62,7 +62,24 @@ __device__ float exact_dot_warp(const float* x, const float* r, int c, int lane)
     return __shfl_sync(0xffffffffu, __fadd_rn(hi, lo), 0);
 }
 
-template <int D, int G>
+__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t phase) {
+    uint32_t ok;
+    asm volatile("{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
+                 : "=r"(ok) : "r"(bar), "r"(phase) : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t phase) {
+    if (mbar_test(bar, phase)) return true;
+    const long long t0 = clock64();
+    while (!mbar_test(bar, phase))
+        if (clock64() - t0 > kWaitCycles) return false;
+    return true;
+}
+
+// kTok: tokens each warp rotates per iteration (register blocking over R); 8 for bulk writes,
+// 1 when there are few tokens (demote).
+template <int D, int G, int kTok>
 __global__ void __launch_bounds__(kWarps * 32)
 write_kernel(const float* __restrict__ r_all, const float* __restrict__ t_all,
              const __nv_bfloat16* __restrict__ k_in, const __nv_bfloat16* __restrict__ v_in,
@@ -84,9 +101,19 @@ write_kernel(const float* __restrict__ r_all, const float* __restrict__ t_all,
     const int kind = blockIdx.z;                        // 0 = K, 1 = V
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
 
+    // R of this (head, K|V) -> shared memory with one bulk async copy (bounded wait)
+    __shared__ __align__(8) uint64_t rbar;
     const float* r_g = r_all + ((size_t)kind * h_kv + head) * D * D;
-    for (int i = threadIdx.x; i < D * D / 4; i += blockDim.x)
-        reinterpret_cast<float4*>(r_s)[i] = __ldg(reinterpret_cast<const float4*>(r_g) + i);
+    const uint32_t rbar_s = (uint32_t)__cvta_generic_to_shared(&rbar);
+    if (threadIdx.x == 0) {
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" :: "r"(rbar_s) : "memory");
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" :: "r"(rbar_s), "r"(D * D * 4) : "memory");
+        asm volatile("cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                     :: "r"((uint32_t)__cvta_generic_to_shared(r_s)), "l"(r_g), "r"(D * D * 4), "r"(rbar_s) : "memory");
+    }
+    __syncthreads();
 
     float thr[CPL];
     const float* t_g = t_all + ((size_t)kind * h_kv + head) * D;
@@ -100,7 +127,11 @@ write_kernel(const float* __restrict__ r_all, const float* __restrict__ t_all,
         const int c = CPL * lane + j;
         off[j] = kind == 0 ? k_bit_offset(c, D) : v_bit_offset(c, D);
     }
-    __syncthreads();
+    if (!__all_sync(0xffffffffu, mbar_wait(rbar_s, 0))) {
+        if (lane == 0) record_error(&dbg->kind, &dbg->index, 4, -1);
+        (void)mbar_wait(rbar_s, 0);      // bounded again: the copy may still be in flight
+        return;
+    }
 
     const int per_cta = (n + gridDim.x - 1) / gridDim.x;
     const int t_begin = blockIdx.x * per_cta;
@@ -268,23 +299,23 @@ write_kernel(const float* __restrict__ r_all, const float* __restrict__ t_all,
     }
 }
 
-template <int D, int G>
-cudaError_t launch_write_t(const Shape& s, const LayerParams& p, int num_sms,
-                           const void* k, const void* v, const int64_t* slots, int n,
-                           const void* bf16_pool, int64_t bf16_pages, const int64_t* src_slots,
-                           void* int2_pool, int64_t int2_pages, DebugWord* dbg, Profiler* prof,
-                           cudaStream_t st) {
+template <int D, int G, int kTok>
+cudaError_t launch_write_tok(const Shape& s, const LayerParams& p, int num_sms,
+                             const void* k, const void* v, const int64_t* slots, int n,
+                             const void* bf16_pool, int64_t bf16_pages, const int64_t* src_slots,
+                             void* int2_pool, int64_t int2_pages, DebugWord* dbg, Profiler* prof,
+                             cudaStream_t st) {
     const size_t smem = (size_t)(D * D + kWarps * kTok * D) * sizeof(float);
-    auto kern = write_kernel<D, G>;
+    auto kern = write_kernel<D, G, kTok>;
     // Opt in to the large dynamic shared memory once per process (outside any stream capture:
     // the first call of a shape happens before a caller can capture it).
     static cudaError_t attr = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (attr != cudaSuccess) return attr;
     // K and V rotations/thresholds sit back to back: r_k then r_v, t_k then t_v.
     const int pairs = s.h_kv * 2;
-    const int want_ctas = 2 * num_sms;
-    int gx = (want_ctas + pairs - 1) / pairs;
-    const int max_gx = (n + kWarps * kTok - 1) / (kWarps * kTok);
+    const int per_cta = kWarps * kTok;
+    const int max_gx = (n + per_cta - 1) / per_cta;
+    int gx = kTok == 1 ? max_gx : (2 * num_sms + pairs - 1) / pairs;
     gx = gx < 1 ? 1 : (gx > max_gx ? max_gx : gx);
     dim3 grid(gx, s.h_kv, 2);
     ProfScope ps(prof, OSCAR_KERNEL_WRITE, st);
@@ -293,6 +324,20 @@ cudaError_t launch_write_t(const Shape& s, const LayerParams& p, int num_sms,
         slots, n, s.h_kv, static_cast<const __nv_bfloat16*>(bf16_pool), bf16_pages, src_slots,
         static_cast<uint8_t*>(int2_pool), int2_pages, s.debug, dbg);
     return cudaGetLastError();
+}
+
+template <int D, int G>
+cudaError_t launch_write_t(const Shape& s, const LayerParams& p, int num_sms,
+                           const void* k, const void* v, const int64_t* slots, int n,
+                           const void* bf16_pool, int64_t bf16_pages, const int64_t* src_slots,
+                           void* int2_pool, int64_t int2_pages, DebugWord* dbg, Profiler* prof,
+                           cudaStream_t st) {
+    // few tokens: one per warp, one CTA per 4 tokens (latency); many: 8 per warp (R reuse)
+    if (n <= 64 * num_sms)
+        return launch_write_tok<D, G, 1>(s, p, num_sms, k, v, slots, n, bf16_pool, bf16_pages, src_slots,
+                                         int2_pool, int2_pages, dbg, prof, st);
+    return launch_write_tok<D, G, 8>(s, p, num_sms, k, v, slots, n, bf16_pool, bf16_pages, src_slots,
+                                     int2_pool, int2_pages, dbg, prof, st);
 }
 
 __global__ void transpose_kernel(const float* __restrict__ src, float* __restrict__ dst, int d) {
