@@ -103,6 +103,11 @@ __device__ __forceinline__ __half split_part(float x, bool lo) {
     return lo ? __float2half_rn(__fmul_rn(__fsub_rn(x, __half2float(h)), 2048.0f)) : h;
 }
 
+// Programmatic dependent launch: wait for the preceding grid in the stream (a no-op without the
+// launch attribute), and let the next grid start its prologue.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 __device__ __forceinline__ void mbar_init(uint32_t bar, int count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" :: "r"(bar), "r"(count) : "memory");
 }
@@ -159,6 +164,8 @@ q_prep_kernel(const __nv_bfloat16* __restrict__ q, const float* __restrict__ r_k
     const int bh = blockIdx.x;
     const int kv = (bh % h_q) / g;
     const int c = threadIdx.x % D, quarter = threadIdx.x / D;
+    pdl_wait();
+    pdl_trigger();
     if (threadIdx.x < D) qs[c] = __bfloat162float(q[(size_t)bh * D + c]);
     __syncthreads();
     const float* r = r_k + (size_t)kv * D * D + (size_t)quarter * Q4 * D + c;
@@ -330,44 +337,6 @@ __device__ void int2_split(const SplitArgs& a, int split, int kv, int b, uint8_t
     int32_t ids0 = lane < n_mine ? table[first + kWarps * lane] : -1;
     int32_t ids1 = lane + 32 < n_mine ? table[first + kWarps * (lane + 32)] : -1;
 
-    // ---- query operands (constant over pages)
-    uint32_t qB1[NK][NHB][2], qB2[NK][2];
-    float kap_h[NHB], kap_m[NHB], kap_l[NHB], qs_hi[NHB][NG], qs_lo[NHB][NG];
-#pragma unroll
-    for (int hb = 0; hb < NHB; ++hb) {
-        const int h = 4 * hb + (gid >> 1);
-        const int part = gid & 1;
-#pragma unroll
-        for (int kk = 0; kk < NK; ++kk) {
-            uint2 v = make_uint2(0u, 0u);
-            if (h < GQ) v = *reinterpret_cast<const uint2*>(a.qb + ((head0 + h) * 3 + part) * D + 16 * kk + 4 * tig);
-            qB1[kk][hb][0] = v.x;
-            qB1[kk][hb][1] = v.y;
-        }
-        const int hm = 4 * hb + tig;
-        kap_h[hb] = hm < GQ ? a.kap[head0 + hm] : 0.0f;
-        kap_m[hb] = kap_h[hb] * 0x1p-11f;
-        kap_l[hb] = kap_h[hb] * 0x1p-22f;
-#pragma unroll
-        for (int gg = 0; gg < NG; ++gg) {
-            qs_hi[hb][gg] = hm < GQ ? a.qsum[((head0 + hm) * NG + gg) * 2 + 0] : 0.0f;
-            qs_lo[hb][gg] = hm < GQ ? a.qsum[((head0 + hm) * NG + gg) * 2 + 1] : 0.0f;
-        }
-    }
-    {
-        // lo parts: column n = gid carries head gid/2 (first block) or, for GQ = 8 and odd gid, head 4 + gid/2
-        const int h = (GQ == 8 && (gid & 1)) ? 4 + (gid >> 1) : ((gid & 1) ? GQ : (gid >> 1));
-#pragma unroll
-        for (int kk = 0; kk < NK; ++kk) {
-            uint2 v = make_uint2(0u, 0u);
-            if (h < GQ) v = *reinterpret_cast<const uint2*>(a.qb + ((head0 + h) * 3 + 2) * D + 16 * kk + 4 * tig);
-            qB2[kk][0] = v.x;
-            qB2[kk][1] = v.y;
-        }
-    }
-    const float pvs = a.pv_scale[kv];
-    const float sl2 = a.scale_log2, sl2_lo = a.scale_log2_lo;
-
     float O[NHB][NK][4];
 #pragma unroll
     for (int hb = 0; hb < NHB; ++hb)
@@ -409,6 +378,48 @@ __device__ void int2_split(const SplitArgs& a, int split, int kv, int b, uint8_t
         }
     };
     for (int j = 0; j < kStages && j < n_mine; ++j) issue(j);
+
+    // the query operands come from q_prep: wait for it (the page copies above are already in flight)
+    pdl_wait();
+    pdl_trigger();
+    // ---- query operands (constant over pages)
+    uint32_t qB1[NK][NHB][2], qB2[NK][2];
+    float kap_h[NHB], kap_m[NHB], kap_l[NHB], qs_hi[NHB][NG], qs_lo[NHB][NG];
+#pragma unroll
+    for (int hb = 0; hb < NHB; ++hb) {
+        const int h = 4 * hb + (gid >> 1);
+        const int part = gid & 1;
+#pragma unroll
+        for (int kk = 0; kk < NK; ++kk) {
+            uint2 v = make_uint2(0u, 0u);
+            if (h < GQ) v = *reinterpret_cast<const uint2*>(a.qb + ((head0 + h) * 3 + part) * D + 16 * kk + 4 * tig);
+            qB1[kk][hb][0] = v.x;
+            qB1[kk][hb][1] = v.y;
+        }
+        const int hm = 4 * hb + tig;
+        kap_h[hb] = hm < GQ ? a.kap[head0 + hm] : 0.0f;
+        kap_m[hb] = kap_h[hb] * 0x1p-11f;
+        kap_l[hb] = kap_h[hb] * 0x1p-22f;
+#pragma unroll
+        for (int gg = 0; gg < NG; ++gg) {
+            qs_hi[hb][gg] = hm < GQ ? a.qsum[((head0 + hm) * NG + gg) * 2 + 0] : 0.0f;
+            qs_lo[hb][gg] = hm < GQ ? a.qsum[((head0 + hm) * NG + gg) * 2 + 1] : 0.0f;
+        }
+    }
+    {
+        // lo parts: column n = gid carries head gid/2 (first block) or, for GQ = 8 and odd gid, head 4 + gid/2
+        const int h = (GQ == 8 && (gid & 1)) ? 4 + (gid >> 1) : ((gid & 1) ? GQ : (gid >> 1));
+#pragma unroll
+        for (int kk = 0; kk < NK; ++kk) {
+            uint2 v = make_uint2(0u, 0u);
+            if (h < GQ) v = *reinterpret_cast<const uint2*>(a.qb + ((head0 + h) * 3 + 2) * D + 16 * kk + 4 * tig);
+            qB2[kk][0] = v.x;
+            qB2[kk][1] = v.y;
+        }
+    }
+    const float pvs = a.pv_scale[kv];
+    const float sl2 = a.scale_log2, sl2_lo = a.scale_log2_lo;
+
 
     bool failed = false;
     int j = 0;
@@ -795,10 +806,13 @@ split_kernel(SplitArgs a) {
     for (int i = threadIdx.x; i < GQ * D; i += blockDim.x) acc_s[i] = 0.0f;
     __syncthreads();
 
-    if (split < a.int2_splits)
+    if (split < a.int2_splits) {
         int2_split<D, G, GQ>(a, split, kv, b, dyn_smem, bars, acc_s, ml_s);
-    else
+    } else {
+        pdl_wait();
+        pdl_trigger();
         bf16_split<D, GQ>(a, split, kv, b, reinterpret_cast<float*>(dyn_smem), p_s, acc_s, ml_s);
+    }
     __syncthreads();
 
     // ---- the partial of each query head of the group
@@ -829,6 +843,13 @@ merge_kernel(const float* __restrict__ partials, const float* __restrict__ r_vt,
     const int bh = blockIdx.x;
     const int kv = (bh % h_q) / g;
     const int tid = threadIdx.x, c = tid % D, quarter = tid / D;
+    // R_v^T terms of this thread (constant calibration data) before waiting for the split kernel
+    const float* rt = r_vt + (size_t)kv * D * D + (size_t)quarter * (D / 4) * D + c;
+    float rv[D / 4];
+#pragma unroll
+    for (int i = 0; i < D / 4; ++i) rv[i] = __ldg(rt + (size_t)i * D);
+    pdl_wait();
+    pdl_trigger();
     const float* part = partials + (size_t)bh * total_splits * (D + 2);
     float mloc = -INFINITY;
     for (int s = tid; s < total_splits; s += 4 * D) mloc = fmaxf(mloc, part[(size_t)s * (D + 2)]);
@@ -865,10 +886,6 @@ merge_kernel(const float* __restrict__ partials, const float* __restrict__ r_vt,
     __syncthreads();
     if (quarter == 0) acc_rot[c] = (part_i[0][c] + part_i[1][c]) + (part_i[2][c] + part_i[3][c]);
     __syncthreads();
-    const float* rt = r_vt + (size_t)kv * D * D + (size_t)quarter * (D / 4) * D + c;
-    float rv[D / 4];
-#pragma unroll
-    for (int i = 0; i < D / 4; ++i) rv[i] = __ldg(rt + (size_t)i * D);
     float o = 0.0f;
 #pragma unroll
     for (int i = 0; i < D / 4; ++i) o = fmaf(acc_rot[quarter * (D / 4) + i], rv[i], o);
@@ -888,8 +905,7 @@ cudaError_t launch_split(const SplitArgs& a, int batch, cudaStream_t st) {
     static cudaError_t attr = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (attr != cudaSuccess) return attr;
     dim3 grid(a.total_splits, a.h_kv, batch);
-    kern<<<grid, kWarps * 32, smem, st>>>(a);
-    return cudaGetLastError();
+    return launch_pdl(kern, grid, dim3(kWarps * 32), smem, st, a);
 }
 
 template <int D, int G>
@@ -904,6 +920,23 @@ cudaError_t dispatch_gq(int gq, const SplitArgs& a, int batch, cudaStream_t st) 
 }
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+// Launch with programmatic stream serialization: the kernel may start while the previous grid in the
+// stream finishes; every kernel here waits (griddepcontrol.wait) before touching its predecessors' data.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, args...);
+}
 
 // Resident split CTAs per SM for the shape (queried once per instantiation).
 template <int D, int G, int GQ>
@@ -974,11 +1007,12 @@ cudaError_t launch_decode(const Shape& s, const LayerParams& prm, const DecodePl
     float* qsum = kap + nh;
     const __nv_bfloat16* q = static_cast<const __nv_bfloat16*>(a.q);
 
+    cudaError_t e = cudaSuccess;
     {
         ProfScope ps(prof, OSCAR_KERNEL_QROT, st);
 #define OSCAR_QPREP_CASE(D_, G_) \
         if (s.d == D_ && s.group == G_) \
-            q_prep_kernel<D_, G_><<<a.batch * s.h_q, 4 * D_, 0, st>>>(q, prm.r_k, qb, kap, qsum, s.h_q, g);
+            e = launch_pdl(q_prep_kernel<D_, G_>, dim3(a.batch * s.h_q), dim3(4 * D_), 0, st, q, prm.r_k, qb, kap, qsum, s.h_q, g);
         OSCAR_QPREP_CASE(64, 32)
         OSCAR_QPREP_CASE(64, 64)
         OSCAR_QPREP_CASE(128, 32)
@@ -986,7 +1020,6 @@ cudaError_t launch_decode(const Shape& s, const LayerParams& prm, const DecodePl
         OSCAR_QPREP_CASE(128, 128)
 #undef OSCAR_QPREP_CASE
     }
-    cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
 
     SplitArgs sa{};
@@ -1025,12 +1058,10 @@ cudaError_t launch_decode(const Shape& s, const LayerParams& prm, const DecodePl
     ProfScope ps_merge(prof, OSCAR_KERNEL_MERGE, st);
     const size_t msmem = (size_t)plan.total_splits * sizeof(float);
     if (s.d == 128)
-        merge_kernel<128><<<a.batch * s.h_q, 4 * 128, msmem, st>>>(partials, prm.r_vt, a.out, s.h_q, g,
-                                                               plan.int2_splits, plan.total_splits);
-    else
-        merge_kernel<64><<<a.batch * s.h_q, 4 * 64, msmem, st>>>(partials, prm.r_vt, a.out, s.h_q, g,
-                                                             plan.int2_splits, plan.total_splits);
-    return cudaGetLastError();
+        return launch_pdl(merge_kernel<128>, dim3(a.batch * s.h_q), dim3(4 * 128), msmem, st, (const float*)partials,
+                          prm.r_vt, a.out, s.h_q, g, plan.int2_splits, plan.total_splits);
+    return launch_pdl(merge_kernel<64>, dim3(a.batch * s.h_q), dim3(4 * 64), msmem, st, (const float*)partials,
+                      prm.r_vt, a.out, s.h_q, g, plan.int2_splits, plan.total_splits);
 }
 
 }  // namespace oscar

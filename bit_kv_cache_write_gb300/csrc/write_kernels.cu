@@ -120,6 +120,12 @@ write_kernel(const float* __restrict__ r_all, const float* __restrict__ t_all,
 #pragma unroll
     for (int j = 0; j < CPL; ++j) thr[j] = __ldg(t_g + CPL * lane + j);
 
+    // programmatic dependent launch: R and T are calibration data, staged above while the preceding
+    // grid may still run; wait for it before touching token data or the pools (a no-op without the
+    // launch attribute), then let the next grid start its prologue
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+
     // bit offset of each of this lane's channels inside the packed row
     int off[CPL];
 #pragma unroll
@@ -319,11 +325,20 @@ cudaError_t launch_write_tok(const Shape& s, const LayerParams& p, int num_sms,
     gx = gx < 1 ? 1 : (gx > max_gx ? max_gx : gx);
     dim3 grid(gx, s.h_kv, 2);
     ProfScope ps(prof, OSCAR_KERNEL_WRITE, st);
-    kern<<<grid, kWarps * 32, smem, st>>>(
-        p.r_k, p.t_k, static_cast<const __nv_bfloat16*>(k), static_cast<const __nv_bfloat16*>(v),
-        slots, n, s.h_kv, static_cast<const __nv_bfloat16*>(bf16_pool), bf16_pages, src_slots,
-        static_cast<uint8_t*>(int2_pool), int2_pages, s.debug, dbg);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(kWarps * 32);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute la[1];
+    la[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    la[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = la;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, p.r_k, p.t_k, static_cast<const __nv_bfloat16*>(k),
+                              static_cast<const __nv_bfloat16*>(v), slots, n, s.h_kv,
+                              static_cast<const __nv_bfloat16*>(bf16_pool), bf16_pages, src_slots,
+                              static_cast<uint8_t*>(int2_pool), int2_pages, s.debug, dbg);
 }
 
 template <int D, int G>
