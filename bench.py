@@ -197,6 +197,75 @@ class GpuWorkload:
     launches_per_step_per_layer = 4     # write (demote), q rotation, split, merge
 
 
+def write_bytes(cfg, n):
+    """Write-path bytes per call: BF16 K/V rows read + packed INT2 codes and fp16 scale/zero written."""
+    d, g, h = cfg["d"], cfg["group"], cfg["h_kv"]
+    return n * h * 2 * (d * 2 + d // 4 + 4 * (d // g))
+
+
+def bench_write(dev, steps, warmup):
+    """Bulk write of 131,072 prefill tokens x 8 KV heads (K and V) into a paged INT2 cache, and the
+    steady-state demote of one token for each of 256 sequences. Device-resident inputs larger than
+    L2; CUDA events on the launching stream."""
+    import numpy as np
+    import torch
+    from bit_kv_cache_write_gb300 import calibration, synth
+    from bit_kv_cache_write_gb300 import oscar as O
+
+    cfg = workload_cfg("bulk_write_131k")
+    n, d, h_kv, group = cfg["tokens"], cfg["d"], cfg["h_kv"], cfg["group"]
+    ctx = O.Oscar(n_layers=1, n_q_heads=cfg["h_q"], n_kv_heads=h_kv, head_dim=d, group=group)
+    li = synth.LayerInputs(cfg, 0)
+    q_cal, k_cal, v_cal = li.calibration()
+    rk, rv, tk, tv = calibration.calibrate_layer(q_cal, k_cal, v_cal, d ** -0.5, cfg["clip_ratio"])
+    ctx.calibrate_upload(0, rk, rv, tk, tv)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(li.seed)
+    km = torch.from_numpy(li.k_prof.mult).to(dev)
+    vm = torch.from_numpy(li.v_prof.mult).to(dev)
+    k = (torch.randn(n, h_kv, d, generator=gen, device=dev) * km).to(torch.bfloat16)
+    v = (torch.randn(n, h_kv, d, generator=gen, device=dev) * vm).to(torch.bfloat16)
+    pages = synth.pages_for(n)
+    perm = torch.from_numpy(synth.page_permutation(li.seed, "bulk", pages).astype(np.int64)).to(dev)
+    t = torch.arange(n, device=dev)
+    slots = perm[t // P] * P + t % P
+    pool = torch.zeros(pages * ctx.int2_page_bytes(), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def timed(fn, reps):
+        for _ in range(warmup):
+            fn()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(reps):
+            fn()
+        b.record(stream)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) * 1e3 / reps
+
+    us = timed(lambda: ctx.write_tokens(0, k, v, slots, pool), steps)
+    nbytes = write_bytes(cfg, n)
+    peak, peak_kind = measured_peak()
+    bulk = {"workload": "bulk_write_131k", "tokens": n, "kv_heads": h_kv, "head_dim": d, "group": group,
+            "us_per_call": us, "tokens_per_s": n / (us * 1e-6), "algorithmic_bytes": nbytes,
+            "roofline": {"bound": "hbm", "achieved": nbytes / (us * 1e-6) / 1e9, "peak": peak,
+                         "peak_kind": peak_kind, "unit": "GB/s", "frac": nbytes / (us * 1e-6) / 1e9 / peak,
+                         "traffic": kernel_traffic("write", "bulk_write_131k")},
+            "l2": "inputs larger than L2 (%.0f MB of K/V rows)" % (n * h_kv * d * 4 / 1e6)}
+
+    # demote: one token per sequence for 256 sequences, from BF16 recent pages into INT2 slots
+    nb = cfg["demote_batch"]
+    bf = (torch.randn(nb, h_kv, 2, P, d, generator=gen, device=dev)
+          * torch.stack([km, vm], dim=1)[None, :, :, None, :]).to(torch.bfloat16).contiguous()
+    src = torch.arange(nb, device=dev, dtype=torch.int64) * P          # row 0 of each sequence's oldest page
+    dst = perm[:nb] * P + 3
+    us_d = timed(lambda: ctx.demote_recent(0, bf, src, pool, dst), steps)
+    demote = {"batch": nb, "us_per_call": us_d, "tokens_per_s": nb / (us_d * 1e-6),
+              "algorithmic_bytes": write_bytes(cfg, nb)}
+    return {"bulk": bulk, "demote": demote}
+
+
 def kernel_traffic(kernel, workload):
     """DRAM bytes per launch from a committed ncu summary, if it was taken on the current kernel source."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
@@ -293,6 +362,8 @@ def main():
     ap.add_argument("--layers", type=int, default=0, help="override the layer count (0: the workload's)")
     ap.add_argument("--oracle-hist", type=int, default=24_992, help="INT2 tokens in the oracle's bounded sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-write", action="store_true", help="skip the bulk-write / demote measurement")
+    ap.add_argument("--only-write", action="store_true", help="print only the bulk-write / demote measurement")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
 
@@ -311,6 +382,11 @@ def main():
     import __graft_entry__
     __graft_entry__.build()
     from bit_kv_cache_write_gb300 import oscar as O
+
+    if args.only_write:
+        if rank == 0:
+            print(json.dumps({"write": bench_write(dev, args.steps, args.warmup)}))
+        return 0
 
     layers = args.layers or cfg["layers"]
     wl = GpuWorkload(cfg, layers, dev, seed_offset=1000 * rank)
@@ -392,6 +468,8 @@ def main():
                                   "decode all %d query heads), fp64 NumPy" % (reps, args.oracle_hist,
                                                                               case.bf16_lens[0], cfg["h_q"])}
 
+    write = bench_write(dev, max(args.steps, 5), args.warmup) if rank == 0 and not args.no_write else None
+
     if rank == 0:
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -415,6 +493,7 @@ def main():
                     "d2h_bytes_per_step": out_host.numel() * 4},
             "gpu_launches": args.steps * layers * GpuWorkload.launches_per_step_per_layer,
             "cpu_baseline": cpu_baseline,
+            "write": write,
         }
         print(json.dumps(line))
     if world > 1:
