@@ -128,8 +128,8 @@ typedef struct oscar_ctx oscar_ctx_t;
 
 /* Create a context on the current CUDA device.
  * Validates cfg, then allocates the per-layer calibration buffers
- * (n_layers * (3 * H_kv * d * d + 2 * H_kv * d) * 4 bytes, plus fp16 splits of R)
- * and the error word. On failure *out is NULL.
+ * (n_layers * (3 * H_kv * d * d + 2 * H_kv * d + H_kv) * 4 bytes: R_k, R_v, R_v^T,
+ * T_k, T_v and one P.V exponent per KV head) and the error word. On failure *out is NULL.
  * Blocking: returns after the allocations complete. */
 OSCAR_API oscar_status oscar_create(const oscar_config_t* cfg, oscar_ctx_t** out);
 
@@ -267,7 +267,9 @@ OSCAR_API const char* oscar_last_error(void);
 /* Read and clear the device error word (debug_bounds mode).
  * Synchronizes the device. Returns OSCAR_OK if nothing was recorded, otherwise
  * OSCAR_ERR_BOUNDS, with *kind set to the check that failed (1 slot, 2 page
- * id, 3 length) and *index to the offending value (either pointer may be NULL). */
+ * id, 3 length, 4 a page copy that did not land within its bounded wait) and
+ * *index to the offending value (either pointer may be NULL). Kind 4 is
+ * recorded in every mode; kinds 1-3 only with debug_bounds. */
 OSCAR_API oscar_status oscar_debug_error(oscar_ctx_t* ctx, int* kind, long long* index);
 
 #ifdef __cplusplus
