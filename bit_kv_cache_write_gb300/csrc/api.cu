@@ -73,6 +73,8 @@ LayerParams layer_params(const oscar_ctx* ctx, int layer) {
     p.t_k = base + 3 * hdd;
     p.t_v = base + 3 * hdd + hd;
     p.pv_scale = base + 3 * hdd + 2 * hd;
+    p.r_img = ctx->r_img + layer * ctx->r_img_elems;
+    p.r_kt = ctx->r_kt + layer * hdd;
     return p;
 }
 
@@ -136,10 +138,25 @@ oscar_status oscar_create(const oscar_config_t* cfg, oscar_ctx_t** out) {
         return fail(OSCAR_ERR_NO_MEMORY, "cudaMalloc of %zu calibration bytes: %s",
                     ctx->params_floats * sizeof(float), cudaGetErrorString(e));
     }
+    ctx->r_img_elems = 2 * (size_t)s.h_kv * oscar::kRotationPieces * s.d * s.d;
+    e = cudaMalloc(&ctx->r_img, ctx->r_img_elems * c.n_layers * sizeof(uint16_t));
+    if (e == cudaSuccess) {
+        e = cudaMalloc(&ctx->r_kt, (size_t)s.h_kv * s.d * s.d * c.n_layers * sizeof(float));
+        if (e != cudaSuccess) cudaFree(ctx->r_img);
+    }
+    if (e != cudaSuccess) {
+        cudaFree(ctx->params);
+        delete ctx;
+        cudaGetLastError();
+        return fail(OSCAR_ERR_NO_MEMORY, "cudaMalloc of %zu rotation-image bytes: %s",
+                    ctx->r_img_elems * c.n_layers * sizeof(uint16_t), cudaGetErrorString(e));
+    }
     e = cudaMalloc(&ctx->dbg, sizeof(oscar::DebugWord));
     if (e == cudaSuccess) e = cudaMemset(ctx->dbg, 0, sizeof(oscar::DebugWord));
     if (e != cudaSuccess) {
         cudaFree(ctx->params);
+        cudaFree(ctx->r_img);
+        cudaFree(ctx->r_kt);
         delete ctx;
         cudaGetLastError();
         return fail(OSCAR_ERR_NO_MEMORY, "cudaMalloc of the error word: %s", cudaGetErrorString(e));
@@ -153,6 +170,8 @@ void oscar_destroy(oscar_ctx_t* ctx) {
     for (auto& v : ctx->prof.pending)
         for (auto& pr : v) { cudaEventDestroy(pr.first); cudaEventDestroy(pr.second); }
     cudaFree(ctx->params);
+    cudaFree(ctx->r_img);
+    cudaFree(ctx->r_kt);
     cudaFree(ctx->dbg);
     delete ctx;
 }
@@ -181,6 +200,7 @@ oscar_status oscar_calibrate_upload(oscar_ctx_t* ctx, int layer, const float* R_
     if (e == cudaSuccess) e = cudaMemcpyAsync(const_cast<float*>(p.t_k), T_k, hd * sizeof(float), cudaMemcpyHostToDevice, st);
     if (e == cudaSuccess) e = cudaMemcpyAsync(const_cast<float*>(p.t_v), T_v, hd * sizeof(float), cudaMemcpyHostToDevice, st);
     if (e == cudaSuccess) e = oscar::launch_transpose(p.r_v, const_cast<float*>(p.r_vt), s.h_kv, s.d, st);
+    if (e == cudaSuccess) e = oscar::launch_transpose(p.r_k, const_cast<float*>(p.r_kt), s.h_kv, s.d, st);
     // Per KV head power of two 2^sigma for the decode's p * s_v operand. Every stored V scale is
     // fp16((mx - mn) / 3) <= (2/3) max T_v (values are clipped to [-T, T]), so p * s_v * 2^sigma
     // stays at or below 32752 (fp16) while small weights keep clear of fp16 subnormals.
@@ -195,6 +215,13 @@ oscar_status oscar_calibrate_upload(oscar_ctx_t* ctx, int layer, const float* R_
     }
     if (e == cudaSuccess)
         e = cudaMemcpyAsync(const_cast<float*>(p.pv_scale), pvs.data(), s.h_kv * sizeof(float),
+                            cudaMemcpyHostToDevice, st);
+    // bf16 pieces of R_k and R_v as tensor-core operand images for the bulk write
+    std::vector<uint16_t> img(ctx->r_img_elems);
+    oscar::build_rotation_images(R_k, s.h_kv, s.d, img.data());
+    oscar::build_rotation_images(R_v, s.h_kv, s.d, img.data() + ctx->r_img_elems / 2);
+    if (e == cudaSuccess)
+        e = cudaMemcpyAsync(const_cast<uint16_t*>(p.r_img), img.data(), ctx->r_img_elems * sizeof(uint16_t),
                             cudaMemcpyHostToDevice, st);
     if (e == cudaSuccess) e = cudaStreamSynchronize(st);
     if (e != cudaSuccess) return cuda_fail(e, "calibration upload");

@@ -21,6 +21,8 @@ struct LayerParams {
     const float* t_k;      // [H_kv][d]
     const float* t_v;      // [H_kv][d]
     const float* pv_scale; // [H_kv] 2^sigma with (2/3) max T_v * 2^sigma <= 32752: keeps p * s_v * 2^sigma in fp16
+    const uint16_t* r_img; // [K,V][H_kv][3][d*d] bf16 pieces of R as tensor-core operand images
+    const float* r_kt;     // [H_kv][d][d], r_kt[h][c][i] = r_k[h][i][c] (exact recompute of the bulk write)
 };
 
 struct Shape {
@@ -75,6 +77,9 @@ struct oscar_ctx {
     int num_sms;
     float* params;                 // all layers' parameters
     size_t params_floats;
+    uint16_t* r_img;               // all layers' bf16 rotation images (tensor-core bulk write)
+    size_t r_img_elems;            // per layer
+    float* r_kt;                   // all layers' R_k^T, [layers][H_kv][d][d]
     std::vector<char> calibrated;  // per layer
     oscar::DebugWord* dbg;         // device error word
     oscar::Profiler prof;
@@ -94,6 +99,19 @@ cudaError_t launch_write(const Shape& s, const LayerParams& p, int num_sms,
                          void* int2_pool, int64_t int2_pages, DebugWord* dbg, Profiler* prof, cudaStream_t st);
 
 cudaError_t launch_transpose(const float* src, float* dst, int h, int d, cudaStream_t st);
+
+// ---- tensor-core bulk write (write_tc.cu)
+constexpr int kTcMinTokens = 512;     // below this the CUDA-core kernel is used
+constexpr int kRotationPieces = 3;    // bf16 pieces of R in the operand images
+
+// Whether a write of n tokens from k/v into int2_pool can take the tcgen05 path.
+bool write_tc_eligible(const Shape& s, const void* k, const void* v, const void* int2_pool, int n);
+cudaError_t launch_write_tc(const Shape& s, const LayerParams& p, int num_sms, const void* k, const void* v,
+                            const int64_t* slots, int n, void* int2_pool, int64_t int2_pages, DebugWord* dbg,
+                            Profiler* prof, cudaStream_t st);
+// Host: the bf16 pieces of h_kv rotations r[h][i][j] (fp32) as swizzled K-major operand images,
+// out[h][piece][d*d].
+void build_rotation_images(const float* r, int h_kv, int d, uint16_t* out);
 
 // ---- decode path (decode_kernels.cu)
 struct DecodePlan {

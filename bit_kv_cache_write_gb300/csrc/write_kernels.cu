@@ -17,6 +17,8 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cfloat>
+#include <cstdlib>
+#include <cstring>
 
 #include "layout.cuh"
 #include "oscar_internal.h"
@@ -373,6 +375,12 @@ cudaError_t launch_write(const Shape& s, const LayerParams& p, int num_sms,
                          const void* bf16_pool, int64_t bf16_pages, const int64_t* src_slots,
                          void* int2_pool, int64_t int2_pages, DebugWord* dbg, Profiler* prof,
                          cudaStream_t st) {
+    // many tokens straight from K/V rows: the tcgen05 kernel (OSCAR_WRITE_PATH=cuda keeps the
+    // CUDA-core kernel, for comparisons)
+    const char* path = std::getenv("OSCAR_WRITE_PATH");
+    const bool force_cuda = path && std::strcmp(path, "cuda") == 0;
+    if (!src_slots && !force_cuda && write_tc_eligible(s, k, v, int2_pool, n))
+        return launch_write_tc(s, p, num_sms, k, v, slots, n, int2_pool, int2_pages, dbg, prof, st);
 #define OSCAR_WRITE_CASE(D_, G_)                                                              \
     if (s.d == D_ && s.group == G_)                                                           \
         return launch_write_t<D_, G_>(s, p, num_sms, k, v, slots, n, bf16_pool, bf16_pages,   \

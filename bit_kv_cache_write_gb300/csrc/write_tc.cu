@@ -1,0 +1,716 @@
+// Bulk write on the tcgen05 tensor cores: rotate -> clip -> group scale/zero ->
+// 2-bit quantize -> pack, for many tokens at once.
+//
+// Method: QbitAI article on OSCAR, serving-pipeline part (rotate, clip,
+// quantize, pack four codes per byte, scale and zero point per group) and
+// section "OSCAR aligns the rotation with attention" (the fixed per-layer
+// rotation R and clip thresholds).
+//
+// The rotation of a tile of 128 tokens is a GEMM, X[128 x d] . R[d x d]. X is
+// bf16, loaded by TMA with a 128-byte swizzle. R is held in shared memory as
+// three bf16 pieces, R ~= R1 + R2 + R3 (24 significant bits): bf16 x bf16
+// products are exact in fp32, so the rotation keeps fp32-level accuracy. One
+// thread issues tcgen05.mma into an fp32 accumulator in tensor memory, small
+// pieces first. Two accumulators alternate between two epilogue warp-groups, so
+// the MMAs of tile i+1 overlap the epilogue of tile i. Each epilogue thread owns one token row (one TMEM lane).
+// It clips the row, takes the group min/max, decides the codes in fp32 exactly
+// as the CUDA-core kernel does, and stores the packed row and its scale/zero
+// into the paged cache.
+//
+// Error bound of the tensor-core rotation. Within one MMA step the products are
+// aligned to the largest term and truncated about 24 bits below it, and the sum
+// is truncated to fp32. So a step errs by at most ~18 * 2^-23 * M, with M bounded
+// by sum_i |x_i R_ic| <= ||x||_2 (R orthogonal). Only the d/16 steps of the
+// leading piece carry a full-size M. When that bound could move the stored zero
+// or scale by more than one fp16 ulp, the candidate min/max channels are
+// recomputed with a double-float dot product (the whole warp, one channel at a time, over a
+// row of R^T), as on the CUDA-core path, and written back into the accumulator column.
+//
+// Roles: warp 0 loads (TMA), warp 1 allocates tensor memory and issues the MMAs,
+// warps 2..9 run the epilogue as two warp-groups that take alternate tiles, each with its own
+// accumulator (warp w reads TMEM lanes 32*(w%4) .. +31). Every
+// mbarrier wait is bounded. A role that gives up sets a shared flag and records
+// kind 4 in the error word. The others then stop, and the copies and MMAs still
+// in flight are drained (bounded) before tensor memory is freed.
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cfloat>
+#include <cstring>
+
+#include "layout.cuh"
+#include "oscar_internal.h"
+
+namespace oscar {
+namespace {
+
+constexpr int kTile = 128;                     // tokens per tile (UMMA M)
+constexpr int kPieces = kRotationPieces;       // bf16 pieces of R
+constexpr int kStages = 3;                     // X tile buffers
+constexpr int kGroups = 2;                     // epilogue warp-groups, one fp32 accumulator each
+constexpr int kEpiWarps = 4 * kGroups;
+constexpr int kThreads = 32 * (2 + kEpiWarps);
+constexpr long long kWaitCycles = 2000000000LL;
+
+template <int D>
+struct TcLayout {
+    static constexpr int kPieceBytes = D * D * 2;          // one piece, SW128 K-major image
+    static constexpr int kTileBytes = kTile * D * 2;       // one X tile
+    static constexpr int kHalves = D / 64;                 // 128-byte swizzle atoms along K
+    static constexpr int kOffB = 0;
+    static constexpr int kOffA = kOffB + kPieces * kPieceBytes;
+    static constexpr int kOffT = kOffA + kStages * kTileBytes;
+    static constexpr int kOffBar = kOffT + D * 4;
+    static constexpr int kBars = 2 * kStages + 2 * kGroups + 1;   // full, empty, acc_full[], acc_empty[], b_full
+    static constexpr int kOffMisc = kOffBar + kBars * 8;
+    static constexpr int kBytes = kOffMisc + 16;
+    static constexpr size_t kDynamic = (size_t)kBytes + 1024;
+    static constexpr int kTmemCols = kGroups * D;
+};
+
+// ---- small PTX helpers ------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, int count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" :: "r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" :: "r"(bar) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" :: "r"(bar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t phase) {
+    uint32_t ok;
+    asm volatile("{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
+                 : "=r"(ok) : "r"(bar), "r"(phase) : "memory");
+    return ok != 0;
+}
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t phase) {
+    if (mbar_test(bar, phase)) return true;
+    const long long t0 = clock64();
+    while (!mbar_test(bar, phase))
+        if (clock64() - t0 > kWaitCycles) return false;
+    return true;
+}
+
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                 :: "r"(dst), "l"(src), "r"(bytes), "r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
+        :: "r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// Shared-memory matrix descriptor: K-major operand, 128-byte swizzle, 8-row groups 1024 B apart.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+    uint64_t d = (uint64_t)((saddr & 0x3FFFFu) >> 4);
+    d |= (uint64_t)1 << 16;                  // leading-dimension offset (unused for swizzled K-major)
+    d |= (uint64_t)(1024 >> 4) << 32;        // stride-dimension offset
+    d |= (uint64_t)1 << 46;                  // descriptor version
+    d |= (uint64_t)2 << 61;                  // 128-byte swizzle
+    return d;
+}
+
+// Instruction descriptor, kind::f16: bf16 A and B, fp32 accumulator, both K-major.
+__host__ __device__ constexpr uint32_t idesc_bf16(int m, int n) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
+}
+
+__device__ __forceinline__ void umma_ss(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+    asm volatile("{ .reg .pred p; setp.ne.b32 p, %4, 0; tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p; }"
+                 :: "r"(d_tmem), "l"(a), "l"(b), "r"(idesc), "r"(acc) : "memory");
+}
+__device__ __forceinline__ void umma_commit(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" :: "r"(bar) : "memory");
+}
+
+// 32 consecutive fp32 columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
+    uint32_t r[32];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ float tmem_ld1(uint32_t taddr) {
+    uint32_t r;
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];" : "=r"(r) : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+    return __uint_as_float(r);
+}
+__device__ __forceinline__ void tmem_st1(uint32_t taddr, float v) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" :: "r"(taddr), "r"(__float_as_uint(v)) : "memory");
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// ---- epilogue ---------------------------------------------------------------------------------
+
+__device__ __forceinline__ void two_sum(float a, float b, float& s, float& e) {
+    s = __fadd_rn(a, b);
+    const float bp = __fsub_rn(s, a);
+    e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bp)), __fsub_rn(b, bp));
+}
+
+// x . R[:, c] with a double-float accumulation, rounded once to fp32, computed by the whole
+// warp: rt is row c of R^T (d contiguous floats); lane l takes terms 4l .. 4l+3 (d = 128) or
+// 2l .. 2l+1 (d = 64). The result is returned on every lane.
+template <int D>
+__device__ __forceinline__ float warp_exact_dot(const __nv_bfloat16* __restrict__ x, const float* __restrict__ rt,
+                                                int lane) {
+    constexpr int PER = D / 32;
+    float xs[PER], rs[PER];
+    if constexpr (PER == 4) {
+        const float4 r4 = *reinterpret_cast<const float4*>(rt + 4 * lane);
+        const uint2 xb = *reinterpret_cast<const uint2*>(x + 4 * lane);
+        rs[0] = r4.x; rs[1] = r4.y; rs[2] = r4.z; rs[3] = r4.w;
+        xs[0] = __uint_as_float(xb.x << 16); xs[1] = __uint_as_float(xb.x & 0xFFFF0000u);
+        xs[2] = __uint_as_float(xb.y << 16); xs[3] = __uint_as_float(xb.y & 0xFFFF0000u);
+    } else {
+        const float2 r2 = *reinterpret_cast<const float2*>(rt + 2 * lane);
+        const uint32_t xb = *reinterpret_cast<const uint32_t*>(x + 2 * lane);
+        rs[0] = r2.x; rs[1] = r2.y;
+        xs[0] = __uint_as_float(xb << 16); xs[1] = __uint_as_float(xb & 0xFFFF0000u);
+    }
+    float hi = 0.0f, lo = 0.0f;
+#pragma unroll
+    for (int j = 0; j < PER; ++j) {
+        const float p = __fmul_rn(xs[j], rs[j]);
+        const float pe = __fmaf_rn(xs[j], rs[j], -p);
+        float t, e;
+        two_sum(hi, p, t, e);
+        hi = t;
+        lo = __fadd_rn(lo, __fadd_rn(pe, e));
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const float h2 = __shfl_xor_sync(0xffffffffu, hi, o);
+        const float l2 = __shfl_xor_sync(0xffffffffu, lo, o);
+        float t, e;
+        two_sum(hi, h2, t, e);
+        hi = t;
+        lo = __fadd_rn(__fadd_rn(lo, l2), e);
+    }
+    return __fadd_rn(hi, lo);
+}
+
+__host__ __device__ constexpr int bit_offset(int kind, int c, int d) {
+    return kind == 0 ? k_bit_offset(c, d) : v_bit_offset(c, d);
+}
+
+// Sum over the channels packed into word w of (0x4B400000 << bit). The float bits of
+// 1.5 * 2^23 + code are 0x4B400000 + code, so adding (bits << bit) for every channel and
+// subtracting this constant leaves the codes in place (all mod 2^32).
+__host__ __device__ constexpr uint32_t pack_bias(int kind, int w, int d) {
+    uint32_t b = 0u;
+    for (int c = 0; c < d; ++c) {
+        const int o = bit_offset(kind, c, d);
+        if (o / 32 == w) b += 0x4B400000u << (o % 32);
+    }
+    return b;
+}
+
+template <int KIND, int D, int W = 0>
+__device__ __forceinline__ void init_words(uint32_t* words) {
+    if constexpr (W < D / 16) {
+        constexpr uint32_t bias = pack_bias(KIND, W, D);
+        words[W] = 0u - bias;
+        init_words<KIND, D, W + 1>(words);
+    }
+}
+
+// Packs one row's clipped values (32-column chunk ch at a time) into words and stores the row.
+template <int D, int G, int KIND>
+__device__ __forceinline__ void pack_chunk(const float (&v)[32], int ch, const float* mn, const float* inv,
+                                           uint32_t* words) {
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+        const int c = 32 * ch + j, g = c / G;
+        // u in [0, 3 + tiny]: adding 1.5 * 2^23 rounds it half-to-even onto the integer grid
+        const float u = __fmul_rn(__fsub_rn(v[j], mn[g]), inv[g]);
+        const uint32_t bits = __float_as_uint(__fadd_rn(u, 12582912.0f));
+        const int off = bit_offset(KIND, c, D);
+        words[off >> 5] += bits << (off & 31);
+    }
+}
+
+template <int D, int G>
+__device__ __forceinline__ void store_row(const uint32_t* words, const float* mn, const float* mx, int64_t slot,
+                                          int head, int h_kv, int kind, uint8_t* __restrict__ int2_pool) {
+    using GE = Geo<D, G>;
+    constexpr int NG = D / G;
+    const int64_t pg = slot / kPage;
+    uint8_t* seg = int2_pool + ((size_t)pg * h_kv + head) * GE::kBlock + (size_t)kind * GE::kSeg;
+    const int row = (int)(slot % kPage);
+    uint32_t* dst = reinterpret_cast<uint32_t*>(seg + row * GE::kCodeRow);
+#pragma unroll
+    for (int w = 0; w < D / 16; w += 4)
+        *reinterpret_cast<uint4*>(dst + w) = make_uint4(words[w], words[w + 1], words[w + 2], words[w + 3]);
+    __half2* szd = reinterpret_cast<__half2*>(seg + GE::kCodeBytes) + row * NG;
+#pragma unroll
+    for (int g = 0; g < NG; ++g)
+        szd[g] = __halves2half2(__float2half_rn(__fdiv_rn(__fsub_rn(mx[g], mn[g]), 3.0f)), __float2half_rn(mn[g]));
+}
+
+template <int D, int G>
+__device__ __forceinline__ void group_inv(const float* mn, const float* mx, float* inv) {
+#pragma unroll
+    for (int g = 0; g < D / G; ++g) {
+        const float rng = __fsub_rn(mx[g], mn[g]);
+        inv[g] = !(rng >= FLT_MIN) ? 0.0f : __fdiv_rn(3.0f, rng);       // degenerate group: codes 0
+    }
+}
+
+template <int NG>
+struct GroupStats {
+    float mn[NG], mx[NG];
+};
+
+// Rare path for a whole warp-tile: some row has a group whose stored zero or scale could be off
+// by more than one fp16 ulp. Every channel that may hold such a group's min (max) is recomputed
+// exactly by the whole warp and written back into the row's accumulator column; the group stats
+// are redone from the other channels and the exact ones. Pass 2 then reads the corrected row.
+template <int D, int G>
+__device__ __noinline__ GroupStats<D / G> exact_fixup(uint32_t tacc, const float* __restrict__ t_s, int tok,
+                                                       bool need, float err, GroupStats<D / G> st, int head, int h_kv,
+                                                       const __nv_bfloat16* __restrict__ x_base,
+                                                       const float* __restrict__ rt_head, int lane) {
+    constexpr int NG = D / G;
+    constexpr int NCH = D / 32;
+    bool need_min[NG], need_max[NG];
+    float lo_cut[NG], hi_cut[NG];
+    GroupStats<NG> nc;                              // stats over the non-candidate channels
+#pragma unroll
+    for (int g = 0; g < NG; ++g) {
+        const float r0 = st.mx[g] - st.mn[g];
+        need_min[g] = need && (fabsf(st.mn[g]) < 4096.0f * err || r0 < 8192.0f * err);
+        need_max[g] = need && r0 < 8192.0f * err;
+        lo_cut[g] = st.mn[g] + 2.0f * err;
+        hi_cut[g] = st.mx[g] - 2.0f * err;
+        nc.mn[g] = FLT_MAX;
+        nc.mx[g] = -FLT_MAX;
+    }
+    uint32_t cand[NCH];
+#pragma unroll
+    for (int ch = 0; ch < NCH; ++ch) {
+        float v[32];
+        tmem_ld32(tacc + 32 * ch, v);
+        tmem_wait_ld();
+        uint32_t cm = 0u;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+            const int c = 32 * ch + j, g = c / G;
+            const float xh = fminf(fmaxf(v[j], -t_s[c]), t_s[c]);
+            if ((need_min[g] && xh <= lo_cut[g]) || (need_max[g] && xh >= hi_cut[g])) {
+                cm |= 1u << j;
+            } else {
+                nc.mn[g] = fminf(nc.mn[g], xh);
+                nc.mx[g] = fmaxf(nc.mx[g], xh);
+            }
+        }
+        cand[ch] = cm;
+    }
+    uint32_t need_lanes = __ballot_sync(0xffffffffu, need);
+    while (need_lanes) {
+        const int src = __ffs(need_lanes) - 1;
+        need_lanes &= need_lanes - 1;
+        const int src_tok = __shfl_sync(0xffffffffu, tok, src);
+        const __nv_bfloat16* xr = x_base + ((size_t)src_tok * h_kv + head) * D;
+#pragma unroll
+        for (int ch = 0; ch < NCH; ++ch) {
+            uint32_t cm = __shfl_sync(0xffffffffu, cand[ch], src);
+            while (cm) {
+                const int c = 32 * ch + __ffs(cm) - 1;
+                cm &= cm - 1;
+                const float ex = warp_exact_dot<D>(xr, rt_head + (size_t)c * D, lane);
+                const float exc = fminf(fmaxf(ex, -t_s[c]), t_s[c]);
+                float cur = tmem_ld1(tacc + c);     // every lane its own row's column c
+                if (lane == src) {
+                    cur = exc;
+#pragma unroll
+                    for (int g = 0; g < NG; ++g)
+                        if (c / G == g) { nc.mn[g] = fminf(nc.mn[g], exc); nc.mx[g] = fmaxf(nc.mx[g], exc); }
+                }
+                tmem_st1(tacc + c, cur);
+            }
+        }
+    }
+    return need ? nc : st;
+}
+
+// Epilogue of one tile for one warp: lane = token row, its fp32 row in TMEM at tacc. Two passes
+// over 32-column chunks (clip + group stats, then codes) keep few values live. Rows past n or with
+// a bad slot (ok false) take part in the warp-wide steps but store nothing. Arrives on acc_empty
+// once the accumulator has been read for the last time.
+template <int D, int G, int KIND>
+__device__ __forceinline__ void epilogue_tile(uint32_t tacc, uint32_t acc_empty, const float* __restrict__ t_s,
+                                              int tok, int64_t slot, bool ok, int head, int h_kv,
+                                              const __nv_bfloat16* __restrict__ x_base,
+                                              const float* __restrict__ rt_head, uint8_t* __restrict__ int2_pool,
+                                              int lane) {
+    constexpr int NG = D / G;
+    constexpr int NCH = D / 32;
+
+    // ---- pass 1: clip, group min/max, ||x|| (rotation preserves the norm)
+    float mn[NG], mx[NG];
+#pragma unroll
+    for (int g = 0; g < NG; ++g) { mn[g] = FLT_MAX; mx[g] = -FLT_MAX; }
+    float sq0 = 0.0f, sq1 = 0.0f;
+    // not unrolled over chunks: the compiler would otherwise keep several chunks live
+#pragma unroll 1
+    for (int ch = 0; ch < NCH; ++ch) {
+        float v[32];
+        tmem_ld32(tacc + 32 * ch, v);
+        tmem_wait_ld();
+        float cmn = FLT_MAX, cmx = -FLT_MAX;
+#pragma unroll
+        for (int j = 0; j < 32; j += 4) {
+            const float4 t = *reinterpret_cast<const float4*>(t_s + 32 * ch + j);
+            sq0 = fmaf(v[j], v[j], sq0);
+            sq1 = fmaf(v[j + 1], v[j + 1], sq1);
+            sq0 = fmaf(v[j + 2], v[j + 2], sq0);
+            sq1 = fmaf(v[j + 3], v[j + 3], sq1);
+            const float a0 = fminf(fmaxf(v[j], -t.x), t.x), a1 = fminf(fmaxf(v[j + 1], -t.y), t.y);
+            const float a2 = fminf(fmaxf(v[j + 2], -t.z), t.z), a3 = fminf(fmaxf(v[j + 3], -t.w), t.w);
+            cmn = fminf(fminf(cmn, a0), fminf(fminf(a1, a2), a3));
+            cmx = fmaxf(fmaxf(cmx, a0), fmaxf(fmaxf(a1, a2), a3));
+        }
+        // a 32-channel chunk lies inside one group (G >= 32)
+#pragma unroll
+        for (int g = 0; g < NG; ++g)
+            if ((32 * ch) / G == g) { mn[g] = fminf(mn[g], cmn); mx[g] = fmaxf(mx[g], cmx); }
+    }
+    const float err = 1.01f * (float)(D / 16) * 18.0f * 0x1p-23f * sqrtf((sq0 + sq1) * 1.002f);
+    bool need = false;
+#pragma unroll
+    for (int g = 0; g < NG; ++g) need |= ok && (fabsf(mn[g]) < 4096.0f * err || (mx[g] - mn[g]) < 8192.0f * err);
+    if (__any_sync(0xffffffffu, need)) {
+        GroupStats<NG> st;
+#pragma unroll
+        for (int g = 0; g < NG; ++g) { st.mn[g] = mn[g]; st.mx[g] = mx[g]; }
+        st = exact_fixup<D, G>(tacc, t_s, tok, need, err, st, head, h_kv, x_base, rt_head, lane);
+#pragma unroll
+        for (int g = 0; g < NG; ++g) { mn[g] = st.mn[g]; mx[g] = st.mx[g]; }
+    }
+
+    // ---- pass 2: codes in fp32, packed in place
+    float inv[NG];
+    group_inv<D, G>(mn, mx, inv);
+    uint32_t words[D / 16];
+    init_words<KIND, D>(words);
+#pragma unroll
+    for (int ch = 0; ch < NCH; ++ch) {
+        float v[32];
+        tmem_ld32(tacc + 32 * ch, v);
+        tmem_wait_ld();
+        if (ch == NCH - 1) {
+            tc_fence_before();
+            mbar_arrive(acc_empty);
+        }
+#pragma unroll
+        for (int j = 0; j < 32; j += 4) {
+            const float4 t = *reinterpret_cast<const float4*>(t_s + 32 * ch + j);
+            v[j] = fminf(fmaxf(v[j], -t.x), t.x);
+            v[j + 1] = fminf(fmaxf(v[j + 1], -t.y), t.y);
+            v[j + 2] = fminf(fmaxf(v[j + 2], -t.z), t.z);
+            v[j + 3] = fminf(fmaxf(v[j + 3], -t.w), t.w);
+        }
+        pack_chunk<D, G, KIND>(v, ch, mn, inv, words);
+    }
+    if (ok) store_row<D, G>(words, mn, mx, slot, head, h_kv, KIND, int2_pool);
+}
+
+template <int D, int G>
+__global__ void __maxnreg__(168)
+write_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_v,
+                const uint16_t* __restrict__ r_img, const float* __restrict__ r_kt, const float* __restrict__ r_vt,
+                const float* __restrict__ t_all,
+                const __nv_bfloat16* __restrict__ k_in, const __nv_bfloat16* __restrict__ v_in,
+                const int64_t* __restrict__ dst_slots, int n, int h_kv, uint8_t* __restrict__ int2_pool,
+                int64_t int2_pages, int debug, DebugWord* dbg) {
+    using L = TcLayout<D>;
+    extern __shared__ uint8_t smem_raw[];
+    // 1024-byte aligned base (pointer arithmetic keeps the shared address space visible)
+    uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    const int head = blockIdx.y, kind = blockIdx.z;
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const int n_tiles = (n + kTile - 1) / kTile;
+    const int my_tiles = (int)blockIdx.x < n_tiles ? (n_tiles - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
+
+    const uint32_t sb = smem_u32(smem);
+    const uint32_t b_s = sb + L::kOffB, a_s = sb + L::kOffA;
+    float* t_s = reinterpret_cast<float*>(smem + L::kOffT);
+    const uint32_t bar0 = sb + L::kOffBar;
+    auto full = [&](int s) { return bar0 + 8 * s; };
+    auto empty = [&](int s) { return bar0 + 8 * (kStages + s); };
+    auto acc_full = [&](int a) { return bar0 + 8 * (2 * kStages + a); };
+    auto acc_empty = [&](int a) { return bar0 + 8 * (2 * kStages + kGroups + a); };
+    const uint32_t b_full = bar0 + 8 * (2 * kStages + 2 * kGroups);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kOffMisc);
+    volatile int* fail = reinterpret_cast<volatile int*>(smem + L::kOffMisc + 4);
+    const size_t pair = (size_t)kind * h_kv + head;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) { mbar_init(full(s), 1); mbar_init(empty(s), 1); }
+        for (int a = 0; a < kGroups; ++a) { mbar_init(acc_full(a), 1); mbar_init(acc_empty(a), 128); }
+        mbar_init(b_full, 1);
+        *fail = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        // the three pieces of this pair's R: calibration data, loaded before waiting on the
+        // preceding grid
+        mbar_expect_tx(b_full, kPieces * L::kPieceBytes);
+        for (int p = 0; p < kPieces; ++p)
+            bulk_load(b_s + p * L::kPieceBytes, r_img + (pair * kPieces + p) * (size_t)(D * D), L::kPieceBytes, b_full);
+    }
+    for (int i = threadIdx.x; i < D; i += kThreads) t_s[i] = t_all[pair * D + i];
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
+                     :: "r"(smem_u32(tmem_slot)), "r"(L::kTmemCols) : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    // programmatic dependent launch: token rows, slots and the pool may come from the preceding grid
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+
+    if (warp == 0) {
+        // ---- TMA producer
+        if (lane == 0) {
+            const CUtensorMap* map = kind == 0 ? &map_k : &map_v;
+            int issued = 0;
+            for (int i = 0; i < my_tiles; ++i) {
+                if (*fail) break;
+                const int s = i % kStages;
+                if (!mbar_wait(empty(s), ((i / kStages) & 1) ^ 1)) {
+                    *fail = 1;
+                    record_error(&dbg->kind, &dbg->index, 4, i);
+                    break;
+                }
+                const int tile = (int)blockIdx.x + i * (int)gridDim.x;
+                mbar_expect_tx(full(s), L::kTileBytes);
+#pragma unroll
+                for (int h = 0; h < L::kHalves; ++h)
+                    tma_load_2d(a_s + s * L::kTileBytes + h * (kTile * 128), map, head * D + 64 * h, tile * kTile, full(s));
+                issued = i + 1;
+            }
+            // drain: every issued tile's copy must land before the CTA may leave
+            for (int j = issued - kStages < 0 ? 0 : issued - kStages; j < issued; ++j)
+                (void)mbar_wait(full(j % kStages), (j / kStages) & 1);
+        }
+    } else if (warp == 1) {
+        // ---- MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t idesc = idesc_bf16(kTile, D);
+            int issued = 0;
+            bool ok = mbar_wait(b_full, 0);
+            if (!ok) {
+                *fail = 1;
+                record_error(&dbg->kind, &dbg->index, 4, -1);
+            }
+            for (int i = 0; ok && i < my_tiles; ++i) {
+                if (*fail) break;
+                const int s = i % kStages, a = i % kGroups;
+                if (!mbar_wait(acc_empty(a), ((i / kGroups) & 1) ^ 1) || !mbar_wait(full(s), (i / kStages) & 1)) {
+                    *fail = 1;
+                    record_error(&dbg->kind, &dbg->index, 4, i);
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d_tmem = tmem + a * D;
+                uint32_t accum = 0;
+#pragma unroll
+                for (int p = kPieces - 1; p >= 0; --p) {
+#pragma unroll
+                    for (int ks = 0; ks < D / 16; ++ks) {
+                        const uint32_t aa = a_s + s * L::kTileBytes + (ks / 4) * (kTile * 128) + (ks % 4) * 32;
+                        const uint32_t bb = b_s + p * L::kPieceBytes + (ks / 4) * (D * 128) + (ks % 4) * 32;
+                        umma_ss(d_tmem, sw128_desc(aa), sw128_desc(bb), idesc, accum);
+                        accum = 1;
+                    }
+                }
+                umma_commit(empty(s));
+                umma_commit(acc_full(a));
+                issued = i + 1;
+            }
+            // drain: the last commit covers every MMA issued before it
+            if (issued > 0) (void)mbar_wait(acc_full((issued - 1) % kGroups), ((issued - 1) / kGroups) & 1);
+        }
+    } else {
+        // ---- epilogue: warp-group e takes local tiles e, e + kGroups, ... with accumulator e;
+        // thread = token row = TMEM lane 32*(warp%4) + lane
+        const int e = (warp - 2) / 4;
+        const int q = warp % 4;
+        const int m = 32 * q + lane;
+        const __nv_bfloat16* x_base = kind == 0 ? k_in : v_in;
+        const float* rt_head = (kind == 0 ? r_kt : r_vt) + (size_t)head * D * D;
+        for (int i = e; i < my_tiles; i += kGroups) {
+            const int tok = ((int)blockIdx.x + i * (int)gridDim.x) * kTile + m;
+            bool ok = tok < n;
+            const int64_t slot = ok ? dst_slots[tok] : -1;        // issued before the wait
+            const bool got = mbar_wait(acc_full(e), (i / kGroups) & 1);
+            const int stop = *fail;
+            if (__any_sync(0xffffffffu, !got || stop)) {       // warp-uniform exit
+                if (lane == 0) {
+                    *fail = 1;
+                    record_error(&dbg->kind, &dbg->index, 4, i);
+                }
+                break;
+            }
+            tc_fence_after();
+            if (ok && (slot < 0 || slot / kPage >= int2_pages)) {
+                if (debug) record_error(&dbg->kind, &dbg->index, 1, slot);
+                ok = false;
+            }
+            const uint32_t tacc = tmem + e * D + ((uint32_t)(32 * q) << 16);
+            if (kind == 0)
+                epilogue_tile<D, G, 0>(tacc, acc_empty(e), t_s, tok, slot, ok, head, h_kv, x_base, rt_head, int2_pool, lane);
+            else
+                epilogue_tile<D, G, 1>(tacc, acc_empty(e), t_s, tok, slot, ok, head, h_kv, x_base, rt_head, int2_pool, lane);
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" :: "r"(tmem), "r"(L::kTmemCols) : "memory");
+    }
+}
+
+// ---- host side ------------------------------------------------------------------------------
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            p = nullptr;
+        return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }();
+    return fn;
+}
+
+// [n][h_kv * d] bf16 rows, boxes of 64 channels x 128 tokens, 128-byte swizzle.
+bool make_row_map(CUtensorMap* map, const void* base, int n, int h_kv, int d) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[2] = {(cuuint64_t)h_kv * d, (cuuint64_t)n};
+    const cuuint64_t strides[1] = {(cuuint64_t)h_kv * d * 2};
+    const cuuint32_t box[2] = {64, (cuuint32_t)kTile};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int D, int G>
+cudaError_t launch_tc(const Shape& s, const LayerParams& p, int num_sms, const void* k, const void* v,
+                      const int64_t* slots, int n, void* int2_pool, int64_t int2_pages, DebugWord* dbg,
+                      Profiler* prof, cudaStream_t st) {
+    using L = TcLayout<D>;
+    auto kern = write_tc_kernel<D, G>;
+    static cudaError_t attr = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L::kDynamic);
+    if (attr != cudaSuccess) return attr;
+    CUtensorMap mk, mv;
+    if (!make_row_map(&mk, k, n, s.h_kv, D) || !make_row_map(&mv, v, n, s.h_kv, D)) return cudaErrorInvalidValue;
+    const int pairs = 2 * s.h_kv;
+    const int n_tiles = (n + kTile - 1) / kTile;
+    int gx = num_sms / pairs;
+    gx = gx < 1 ? 1 : (gx > n_tiles ? n_tiles : gx);
+    ProfScope ps(prof, OSCAR_KERNEL_WRITE, st);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(gx, s.h_kv, 2);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = L::kDynamic;
+    cfg.stream = st;
+    cudaLaunchAttribute la[1];
+    la[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    la[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = la;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, mk, mv, p.r_img, p.r_kt, p.r_vt, p.t_k, static_cast<const __nv_bfloat16*>(k),
+                              static_cast<const __nv_bfloat16*>(v), slots, n, s.h_kv,
+                              static_cast<uint8_t*>(int2_pool), int2_pages, s.debug, dbg);
+}
+
+// bf16 (round to nearest even) of a finite float, as raw bits.
+uint16_t bf16_bits(float x) {
+    uint32_t u;
+    std::memcpy(&u, &x, 4);
+    u += 0x7FFFu + ((u >> 16) & 1u);
+    return (uint16_t)(u >> 16);
+}
+float bf16_value(uint16_t b) {
+    const uint32_t u = (uint32_t)b << 16;
+    float x;
+    std::memcpy(&x, &u, 4);
+    return x;
+}
+
+}  // namespace
+
+bool write_tc_eligible(const Shape& s, const void* k, const void* v, const void* int2_pool, int n) {
+    if (n < kTcMinTokens || (s.d != 64 && s.d != 128)) return false;
+    // TMA row maps need 16-byte aligned bases; the epilogue stores 16-byte code rows
+    if ((reinterpret_cast<uintptr_t>(k) | reinterpret_cast<uintptr_t>(v) | reinterpret_cast<uintptr_t>(int2_pool)) & 15)
+        return false;
+    return encode_fn() != nullptr;
+}
+
+cudaError_t launch_write_tc(const Shape& s, const LayerParams& p, int num_sms, const void* k, const void* v,
+                            const int64_t* slots, int n, void* int2_pool, int64_t int2_pages, DebugWord* dbg,
+                            Profiler* prof, cudaStream_t st) {
+#define OSCAR_TC_CASE(D_, G_) \
+    if (s.d == D_ && s.group == G_) return launch_tc<D_, G_>(s, p, num_sms, k, v, slots, n, int2_pool, int2_pages, dbg, prof, st);
+    OSCAR_TC_CASE(64, 32)
+    OSCAR_TC_CASE(64, 64)
+    OSCAR_TC_CASE(128, 32)
+    OSCAR_TC_CASE(128, 64)
+    OSCAR_TC_CASE(128, 128)
+#undef OSCAR_TC_CASE
+    return cudaErrorInvalidValue;
+}
+
+void build_rotation_images(const float* r, int h_kv, int d, uint16_t* out) {
+    // out[h][piece][image]: B[n = output channel j][k = input channel i] = piece(R[i][j]), K-major,
+    // 128-byte swizzle atoms of 8 rows x 64 channels (16-byte chunk index XOR row % 8)
+    for (int h = 0; h < h_kv; ++h) {
+        const float* rh = r + (size_t)h * d * d;
+        uint16_t* oh = out + (size_t)h * kPieces * d * d;
+        for (int i = 0; i < d; ++i)
+            for (int j = 0; j < d; ++j) {
+                float rest = rh[(size_t)i * d + j];
+                const int half = i / 64, kk = i % 64, chunk = kk / 8, e = kk % 8;
+                const size_t off =
+                    ((size_t)half * d * 128 + (size_t)j * 128 + (size_t)((chunk ^ (j % 8)) * 16) + e * 2) / 2;
+                for (int pce = 0; pce < kPieces; ++pce) {
+                    const uint16_t b = bf16_bits(rest);
+                    oh[(size_t)pce * d * d + off] = b;
+                    rest -= bf16_value(b);
+                }
+            }
+    }
+}
+
+}  // namespace oscar

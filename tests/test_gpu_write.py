@@ -3,6 +3,10 @@
 Bar: packed codes bit-exact except off-by-one codes whose oracle ratio lies
 within 1e-5 of a rounding boundary; scale and zero within 1 fp16 ulp; no byte
 outside the written rows changes.
+
+Writes of at least 512 tokens straight from K/V rows run on the tcgen05 kernel,
+smaller writes and demotes on the CUDA-core kernel; OSCAR_WRITE_PATH=cuda keeps
+every write on the CUDA-core kernel.
 """
 
 import numpy as np
@@ -28,10 +32,13 @@ def bf16(a, dev):
 
 
 WRITE_CASES = [
-    ("tiny", {}, 1000),
+    ("tiny", {}, 1000),                                          # tensor cores, d=64 G=32
+    ("tiny", dict(group=64), 600),                               # tensor cores, d=64 G=64
     ("tiny", dict(group=64), 257),
-    ("qwen3_8b_bs1_100k", {}, 777),
-    ("qwen3_4b_b64_32k", {}, 1024),
+    ("qwen3_8b_bs1_100k", {}, 777),                              # tensor cores, ragged last tile
+    ("qwen3_8b_bs1_100k", {}, 4100),                             # several tiles per CTA
+    ("qwen3_4b_b64_32k", {}, 1024),                              # tensor cores, G=64, Laplace rows
+    ("qwen3_8b_bs1_100k", dict(group=32), 1300),                 # tensor cores, G=32
     ("qwen3_8b_bs1_100k", dict(group=32), 333),
     ("qwen3_8b_bs1_100k", dict(group=64, h_kv=2, h_q=4), 5),
     ("tiny", {}, 1),
@@ -57,6 +64,33 @@ def test_write_tokens_parity(cuda, name, over, n):
     torch.cuda.synchronize()
     flips = cases.compare_int2(pool.cpu().numpy(), ref, geo, slots, info)
     print("tolerated boundary flips:", flips)
+
+
+@pytest.mark.parametrize("name,n", [("qwen3_8b_bs1_100k", 2000), ("tiny", 700)])
+def test_tensor_core_and_cuda_core_writes_agree(cuda, monkeypatch, name, n):
+    """Both write kernels against the oracle, and against each other (codes may differ only by
+    tolerated boundary flips; scale/zero by at most one fp16 ulp each)."""
+    cfg = cases.workload(name)
+    li, (rk, rv, tk, tv) = cases.calibration(cfg)
+    geo = layout.Int2Geometry(cfg["d"], cfg["group"], cfg["h_kv"])
+    n_pages = synth.pages_for(n) + 3
+    slots = synth.rng_for(li.seed, "both").permutation(n_pages * P)[:n].astype(np.int64)
+    k, v = li.kv("both", n)
+    ref = np.zeros(n_pages * geo.page_bytes, np.uint8)
+    info = cache.write_tokens(ref, geo, k, v, slots, rk, rv, tk, tv)
+    ctx = make_ctx(cfg)
+    ctx.calibrate_upload(0, rk, rv, tk, tv)
+    out = {}
+    for path in ("tc", "cuda"):
+        if path == "cuda":
+            monkeypatch.setenv("OSCAR_WRITE_PATH", "cuda")
+        pool = torch.zeros(n_pages * geo.page_bytes, dtype=torch.uint8, device=cuda)
+        ctx.write_tokens(0, bf16(k, cuda), bf16(v, cuda), torch.from_numpy(slots).to(cuda), pool)
+        torch.cuda.synchronize()
+        out[path] = pool.cpu().numpy()
+        cases.compare_int2(out[path], ref, geo, slots, info)
+    differ = int(np.count_nonzero(out["tc"] != out["cuda"]))
+    print("bytes that differ between the two kernels:", differ)
 
 
 def test_write_twice_is_idempotent_and_n0_is_noop(cuda):
@@ -150,6 +184,26 @@ def test_debug_bounds_records_bad_slot(cuda):
     # the valid tokens were still written
     got = pool.cpu().numpy()
     c, s, z = layout.read_int2_token(got, geo, 17, 0, "k")
+    assert float(np.abs(s.astype(np.float64)).max()) > 0
+
+
+def test_debug_bounds_on_the_tensor_core_path(cuda):
+    cfg = cases.workload("qwen3_8b_bs1_100k")
+    li, (rk, rv, tk, tv) = cases.calibration(cfg)
+    geo = layout.Int2Geometry(cfg["d"], cfg["group"], cfg["h_kv"])
+    n = 600
+    ctx = make_ctx(cfg, debug=1)
+    ctx.calibrate_upload(0, rk, rv, tk, tv)
+    k, v = li.kv("dbg-tc", n)
+    n_pages = synth.pages_for(n)
+    slots = torch.arange(n, dtype=torch.int64, device=cuda)
+    slots[300] = (n_pages + 7) * P + 2                  # past the pool
+    pool = torch.zeros(n_pages * geo.page_bytes, dtype=torch.uint8, device=cuda)
+    ctx.write_tokens(0, bf16(k, cuda), bf16(v, cuda), slots, pool)
+    st, kind, index = ctx.debug_error()
+    assert st == -5 and kind == 1 and index == (n_pages + 7) * P + 2
+    got = pool.cpu().numpy()
+    c, s, z = layout.read_int2_token(got, geo, 299, 0, "k")
     assert float(np.abs(s.astype(np.float64)).max()) > 0
 
 
