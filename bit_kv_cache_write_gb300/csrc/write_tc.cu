@@ -19,12 +19,13 @@
 //
 // Error bound of the tensor-core rotation. Within one MMA step the products are
 // aligned to the largest term and truncated about 24 bits below it, and the sum
-// is truncated to fp32. So a step errs by at most ~18 * 2^-23 * M, with M bounded
+// is truncated to fp32. So a step errs by at most 9 * 2^-23 * M (16 products each
+// off by under 2^-24 M, plus the final truncation), with M bounded
 // by sum_i |x_i R_ic| <= ||x||_2 (R orthogonal). Only the d/16 steps of the
 // leading piece carry a full-size M. When that bound could move the stored zero
 // or scale by more than one fp16 ulp, the candidate min/max channels are
-// recomputed with a double-float dot product (the whole warp, one channel at a time, over a
-// row of R^T), as on the CUDA-core path, and written back into the accumulator column.
+// recomputed with a double-float dot product over a row of R^T (batches of 8 channels spread over
+// the warp), as on the CUDA-core path. Those exact values set the stored zero and scale.
 //
 // Roles: warp 0 loads (TMA), warp 1 allocates tensor memory and issues the MMAs,
 // warps 2..9 run the epilogue as two warp-groups that take alternate tiles, each with its own
@@ -49,7 +50,8 @@ namespace {
 constexpr int kTile = 128;                     // tokens per tile (UMMA M)
 constexpr int kPieces = kRotationPieces;       // bf16 pieces of R
 constexpr int kStages = 3;                     // X tile buffers
-constexpr int kGroups = 2;                     // epilogue warp-groups, one fp32 accumulator each
+constexpr int kGroups = 2;                     // epilogue warp-groups
+constexpr int kAccs = 4;                       // fp32 accumulators in TMEM (kAccs / kGroups per group)
 constexpr int kEpiWarps = 4 * kGroups;
 constexpr int kThreads = 32 * (2 + kEpiWarps);
 constexpr long long kWaitCycles = 2000000000LL;
@@ -63,11 +65,11 @@ struct TcLayout {
     static constexpr int kOffA = kOffB + kPieces * kPieceBytes;
     static constexpr int kOffT = kOffA + kStages * kTileBytes;
     static constexpr int kOffBar = kOffT + D * 4;
-    static constexpr int kBars = 2 * kStages + 2 * kGroups + 1;   // full, empty, acc_full[], acc_empty[], b_full
+    static constexpr int kBars = 2 * kStages + 2 * kAccs + 1;     // full, empty, acc_full[], acc_empty[], b_full
     static constexpr int kOffMisc = kOffBar + kBars * 8;
     static constexpr int kBytes = kOffMisc + 16;
     static constexpr size_t kDynamic = (size_t)kBytes + 1024;
-    static constexpr int kTmemCols = kGroups * D;
+    static constexpr int kTmemCols = kAccs * D;
 };
 
 // ---- small PTX helpers ------------------------------------------------------------------------
@@ -148,65 +150,12 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
     for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
-__device__ __forceinline__ float tmem_ld1(uint32_t taddr) {
-    uint32_t r;
-    asm volatile("tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];" : "=r"(r) : "r"(taddr));
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-    return __uint_as_float(r);
-}
-__device__ __forceinline__ void tmem_st1(uint32_t taddr, float v) {
-    asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" :: "r"(taddr), "r"(__float_as_uint(v)) : "memory");
-    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-}
-
 // ---- epilogue ---------------------------------------------------------------------------------
 
 __device__ __forceinline__ void two_sum(float a, float b, float& s, float& e) {
     s = __fadd_rn(a, b);
     const float bp = __fsub_rn(s, a);
     e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bp)), __fsub_rn(b, bp));
-}
-
-// x . R[:, c] with a double-float accumulation, rounded once to fp32, computed by the whole
-// warp: rt is row c of R^T (d contiguous floats); lane l takes terms 4l .. 4l+3 (d = 128) or
-// 2l .. 2l+1 (d = 64). The result is returned on every lane.
-template <int D>
-__device__ __forceinline__ float warp_exact_dot(const __nv_bfloat16* __restrict__ x, const float* __restrict__ rt,
-                                                int lane) {
-    constexpr int PER = D / 32;
-    float xs[PER], rs[PER];
-    if constexpr (PER == 4) {
-        const float4 r4 = *reinterpret_cast<const float4*>(rt + 4 * lane);
-        const uint2 xb = *reinterpret_cast<const uint2*>(x + 4 * lane);
-        rs[0] = r4.x; rs[1] = r4.y; rs[2] = r4.z; rs[3] = r4.w;
-        xs[0] = __uint_as_float(xb.x << 16); xs[1] = __uint_as_float(xb.x & 0xFFFF0000u);
-        xs[2] = __uint_as_float(xb.y << 16); xs[3] = __uint_as_float(xb.y & 0xFFFF0000u);
-    } else {
-        const float2 r2 = *reinterpret_cast<const float2*>(rt + 2 * lane);
-        const uint32_t xb = *reinterpret_cast<const uint32_t*>(x + 2 * lane);
-        rs[0] = r2.x; rs[1] = r2.y;
-        xs[0] = __uint_as_float(xb << 16); xs[1] = __uint_as_float(xb & 0xFFFF0000u);
-    }
-    float hi = 0.0f, lo = 0.0f;
-#pragma unroll
-    for (int j = 0; j < PER; ++j) {
-        const float p = __fmul_rn(xs[j], rs[j]);
-        const float pe = __fmaf_rn(xs[j], rs[j], -p);
-        float t, e;
-        two_sum(hi, p, t, e);
-        hi = t;
-        lo = __fadd_rn(lo, __fadd_rn(pe, e));
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        const float h2 = __shfl_xor_sync(0xffffffffu, hi, o);
-        const float l2 = __shfl_xor_sync(0xffffffffu, lo, o);
-        float t, e;
-        two_sum(hi, h2, t, e);
-        hi = t;
-        lo = __fadd_rn(__fadd_rn(lo, l2), e);
-    }
-    return __fadd_rn(hi, lo);
 }
 
 __host__ __device__ constexpr int bit_offset(int kind, int c, int d) {
@@ -281,72 +230,164 @@ struct GroupStats {
     float mn[NG], mx[NG];
 };
 
+template <int NCH>
+struct ChunkStats {
+    float mn[NCH], mx[NCH];
+};
+
 // Rare path for a whole warp-tile: some row has a group whose stored zero or scale could be off
 // by more than one fp16 ulp. Every channel that may hold such a group's min (max) is recomputed
-// exactly by the whole warp and written back into the row's accumulator column; the group stats
-// are redone from the other channels and the exact ones. Pass 2 then reads the corrected row.
+// exactly, and the group's min/max for the stored zero and scale are redone from the other
+// channels and the exact ones. Only 32-channel chunks whose min (max) comes near the cut are
+// reread. Exact dots run over the whole warp (lane l takes terms PER*l ..), up to 4 candidates
+// at a time with their loads issued together. (The codes of these channels are 0 near the min
+// and 3 near the max either way.)
 template <int D, int G>
 __device__ __noinline__ GroupStats<D / G> exact_fixup(uint32_t tacc, const float* __restrict__ t_s, int tok,
-                                                       bool need, float err, GroupStats<D / G> st, int head, int h_kv,
+                                                       bool need, float err, GroupStats<D / G> st,
+                                                       ChunkStats<D / 32> cs, int head, int h_kv,
                                                        const __nv_bfloat16* __restrict__ x_base,
                                                        const float* __restrict__ rt_head, int lane) {
     constexpr int NG = D / G;
     constexpr int NCH = D / 32;
-    bool need_min[NG], need_max[NG];
+    constexpr int PER = D / 32;                     // terms per lane
+    constexpr int B = 4;                            // candidates per round
     float lo_cut[NG], hi_cut[NG];
-    GroupStats<NG> nc;                              // stats over the non-candidate channels
+    GroupStats<NG> nc = st;                         // stats over non-candidates (+ exact candidates)
+    bool need_min[NG], need_max[NG];
 #pragma unroll
     for (int g = 0; g < NG; ++g) {
         const float r0 = st.mx[g] - st.mn[g];
         need_min[g] = need && (fabsf(st.mn[g]) < 4096.0f * err || r0 < 8192.0f * err);
         need_max[g] = need && r0 < 8192.0f * err;
-        lo_cut[g] = st.mn[g] + 2.0f * err;
-        hi_cut[g] = st.mx[g] - 2.0f * err;
-        nc.mn[g] = FLT_MAX;
-        nc.mx[g] = -FLT_MAX;
+        lo_cut[g] = need_min[g] ? st.mn[g] + 2.0f * err : -FLT_MAX;
+        hi_cut[g] = need_max[g] ? st.mx[g] - 2.0f * err : FLT_MAX;
+        if (need_min[g]) nc.mn[g] = FLT_MAX;
+        if (need_max[g]) nc.mx[g] = -FLT_MAX;
     }
     uint32_t cand[NCH];
-#pragma unroll
     for (int ch = 0; ch < NCH; ++ch) {
-        float v[32];
-        tmem_ld32(tacc + 32 * ch, v);
-        tmem_wait_ld();
-        uint32_t cm = 0u;
+        const int g = (32 * ch) / G;
+        float lc = -FLT_MAX, hc = FLT_MAX;
+        bool touched = false;
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-            const int c = 32 * ch + j, g = c / G;
-            const float xh = fminf(fmaxf(v[j], -t_s[c]), t_s[c]);
-            if ((need_min[g] && xh <= lo_cut[g]) || (need_max[g] && xh >= hi_cut[g])) {
-                cm |= 1u << j;
+        for (int k = 0; k < NCH; ++k)
+            if (k == ch) touched = need && (cs.mn[k] <= lo_cut[k * 32 / G] || cs.mx[k] >= hi_cut[k * 32 / G]);
+        uint32_t cm = 0u;
+        if (__any_sync(0xffffffffu, touched)) {
+#pragma unroll
+            for (int gg = 0; gg < NG; ++gg)
+                if (gg == g) { lc = lo_cut[gg]; hc = hi_cut[gg]; }
+            float v[32];
+            tmem_ld32(tacc + 32 * ch, v);
+            tmem_wait_ld();
+            float cmn = FLT_MAX, cmx = -FLT_MAX;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+                const float xh = fminf(fmaxf(v[j], -t_s[32 * ch + j]), t_s[32 * ch + j]);
+                const bool is_c = touched && (xh <= lc || xh >= hc);
+                cm |= (uint32_t)is_c << j;
+                if (!is_c) { cmn = fminf(cmn, xh); cmx = fmaxf(cmx, xh); }
+            }
+            if (touched) {
+#pragma unroll
+                for (int gg = 0; gg < NG; ++gg)
+                    if (gg == g) {
+                        if (need_min[gg]) nc.mn[gg] = fminf(nc.mn[gg], cmn);
+                        if (need_max[gg]) nc.mx[gg] = fmaxf(nc.mx[gg], cmx);
+                    }
+            }
+        } else if (need) {
+            // untouched chunk of a group under repair: its stats count as non-candidates
+#pragma unroll
+            for (int k = 0; k < NCH; ++k)
+                if (k == ch) {
+#pragma unroll
+                    for (int gg = 0; gg < NG; ++gg)
+                        if (gg == g) {
+                            if (need_min[gg]) nc.mn[gg] = fminf(nc.mn[gg], cs.mn[k]);
+                            if (need_max[gg]) nc.mx[gg] = fmaxf(nc.mx[gg], cs.mx[k]);
+                        }
+                }
+        }
+#pragma unroll
+        for (int k = 0; k < NCH; ++k)
+            if (k == ch) cand[k] = cm;
+    }
+    for (;;) {
+        int s_src[B], s_c[B];
+        float rv[B][PER], xv[B][PER];
+#pragma unroll
+        for (int k = 0; k < B; ++k) {
+            bool mine = false;
+#pragma unroll
+            for (int ch = 0; ch < NCH; ++ch) mine |= cand[ch] != 0u;
+            const uint32_t has = __ballot_sync(0xffffffffu, mine);
+            s_src[k] = has ? __ffs(has) - 1 : -1;
+            int myc = 0;
+            if (has && lane == s_src[k]) {
+                bool done = false;
+#pragma unroll
+                for (int ch = 0; ch < NCH; ++ch)
+                    if (!done && cand[ch]) {
+                        myc = 32 * ch + __ffs(cand[ch]) - 1;
+                        cand[ch] &= cand[ch] - 1;
+                        done = true;
+                    }
+            }
+            s_c[k] = __shfl_sync(0xffffffffu, myc, has ? s_src[k] : 0);
+            const int st_tok = __shfl_sync(0xffffffffu, tok, has ? s_src[k] : 0);
+            if (has) {
+                const float* rr = rt_head + (size_t)s_c[k] * D + PER * lane;
+                const __nv_bfloat16* xr = x_base + ((size_t)st_tok * h_kv + head) * D + PER * lane;
+                if constexpr (PER == 4) {
+                    const float4 r4 = *reinterpret_cast<const float4*>(rr);
+                    const uint2 xb = *reinterpret_cast<const uint2*>(xr);
+                    rv[k][0] = r4.x; rv[k][1] = r4.y; rv[k][2] = r4.z; rv[k][3] = r4.w;
+                    xv[k][0] = __uint_as_float(xb.x << 16); xv[k][1] = __uint_as_float(xb.x & 0xFFFF0000u);
+                    xv[k][2] = __uint_as_float(xb.y << 16); xv[k][3] = __uint_as_float(xb.y & 0xFFFF0000u);
+                } else {
+                    const float2 r2 = *reinterpret_cast<const float2*>(rr);
+                    const uint32_t xb = *reinterpret_cast<const uint32_t*>(xr);
+                    rv[k][0] = r2.x; rv[k][1] = r2.y;
+                    xv[k][0] = __uint_as_float(xb << 16); xv[k][1] = __uint_as_float(xb & 0xFFFF0000u);
+                }
             } else {
-                nc.mn[g] = fminf(nc.mn[g], xh);
-                nc.mx[g] = fmaxf(nc.mx[g], xh);
+#pragma unroll
+                for (int j = 0; j < PER; ++j) { rv[k][j] = 0.0f; xv[k][j] = 0.0f; }
             }
         }
-        cand[ch] = cm;
-    }
-    uint32_t need_lanes = __ballot_sync(0xffffffffu, need);
-    while (need_lanes) {
-        const int src = __ffs(need_lanes) - 1;
-        need_lanes &= need_lanes - 1;
-        const int src_tok = __shfl_sync(0xffffffffu, tok, src);
-        const __nv_bfloat16* xr = x_base + ((size_t)src_tok * h_kv + head) * D;
+        if (s_src[0] < 0) break;
 #pragma unroll
-        for (int ch = 0; ch < NCH; ++ch) {
-            uint32_t cm = __shfl_sync(0xffffffffu, cand[ch], src);
-            while (cm) {
-                const int c = 32 * ch + __ffs(cm) - 1;
-                cm &= cm - 1;
-                const float ex = warp_exact_dot<D>(xr, rt_head + (size_t)c * D, lane);
-                const float exc = fminf(fmaxf(ex, -t_s[c]), t_s[c]);
-                float cur = tmem_ld1(tacc + c);     // every lane its own row's column c
-                if (lane == src) {
-                    cur = exc;
+        for (int k = 0; k < B; ++k) {
+            float hi = 0.0f, lo = 0.0f;
 #pragma unroll
-                    for (int g = 0; g < NG; ++g)
-                        if (c / G == g) { nc.mn[g] = fminf(nc.mn[g], exc); nc.mx[g] = fmaxf(nc.mx[g], exc); }
-                }
-                tmem_st1(tacc + c, cur);
+            for (int j = 0; j < PER; ++j) {
+                const float p = __fmul_rn(xv[k][j], rv[k][j]);
+                const float pe = __fmaf_rn(xv[k][j], rv[k][j], -p);
+                float t, e;
+                two_sum(hi, p, t, e);
+                hi = t;
+                lo = __fadd_rn(lo, __fadd_rn(pe, e));
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                const float h2 = __shfl_xor_sync(0xffffffffu, hi, o);
+                const float l2 = __shfl_xor_sync(0xffffffffu, lo, o);
+                float t, e;
+                two_sum(hi, h2, t, e);
+                hi = t;
+                lo = __fadd_rn(__fadd_rn(lo, l2), e);
+            }
+            if (s_src[k] >= 0 && lane == s_src[k]) {
+                const int c = s_c[k];
+                const float exc = fminf(fmaxf(__fadd_rn(hi, lo), -t_s[c]), t_s[c]);
+#pragma unroll
+                for (int g = 0; g < NG; ++g)
+                    if (c / G == g) {
+                        if (need_min[g]) nc.mn[g] = fminf(nc.mn[g], exc);
+                        if (need_max[g]) nc.mx[g] = fmaxf(nc.mx[g], exc);
+                    }
             }
         }
     }
@@ -371,6 +412,7 @@ __device__ __forceinline__ void epilogue_tile(uint32_t tacc, uint32_t acc_empty,
 #pragma unroll
     for (int g = 0; g < NG; ++g) { mn[g] = FLT_MAX; mx[g] = -FLT_MAX; }
     float sq0 = 0.0f, sq1 = 0.0f;
+    float chmn[NCH], chmx[NCH];                     // per-chunk clipped min/max (fixup detection)
     // not unrolled over chunks: the compiler would otherwise keep several chunks live
 #pragma unroll 1
     for (int ch = 0; ch < NCH; ++ch) {
@@ -394,18 +436,29 @@ __device__ __forceinline__ void epilogue_tile(uint32_t tacc, uint32_t acc_empty,
 #pragma unroll
         for (int g = 0; g < NG; ++g)
             if ((32 * ch) / G == g) { mn[g] = fminf(mn[g], cmn); mx[g] = fmaxf(mx[g], cmx); }
+#pragma unroll
+        for (int k = 0; k < NCH; ++k)
+            if (k == ch) { chmn[k] = cmn; chmx[k] = cmx; }
     }
-    const float err = 1.01f * (float)(D / 16) * 18.0f * 0x1p-23f * sqrtf((sq0 + sq1) * 1.002f);
+    const float err = 1.01f * (float)(D / 16) * 9.0f * 0x1p-23f * sqrtf((sq0 + sq1) * 1.002f);
     bool need = false;
 #pragma unroll
     for (int g = 0; g < NG; ++g) need |= ok && (fabsf(mn[g]) < 4096.0f * err || (mx[g] - mn[g]) < 8192.0f * err);
+    // stats for the stored scale/zero; the codes use the tensor-core stats (their shift is far
+    // inside the rounding tolerance, and min/max channels code 0/3 either way)
+    float mn_sz[NG], mx_sz[NG];
+#pragma unroll
+    for (int g = 0; g < NG; ++g) { mn_sz[g] = mn[g]; mx_sz[g] = mx[g]; }
     if (__any_sync(0xffffffffu, need)) {
         GroupStats<NG> st;
 #pragma unroll
         for (int g = 0; g < NG; ++g) { st.mn[g] = mn[g]; st.mx[g] = mx[g]; }
-        st = exact_fixup<D, G>(tacc, t_s, tok, need, err, st, head, h_kv, x_base, rt_head, lane);
+        ChunkStats<NCH> cs;
 #pragma unroll
-        for (int g = 0; g < NG; ++g) { mn[g] = st.mn[g]; mx[g] = st.mx[g]; }
+        for (int k = 0; k < NCH; ++k) { cs.mn[k] = chmn[k]; cs.mx[k] = chmx[k]; }
+        st = exact_fixup<D, G>(tacc, t_s, tok, need, err, st, cs, head, h_kv, x_base, rt_head, lane);
+#pragma unroll
+        for (int g = 0; g < NG; ++g) { mn_sz[g] = st.mn[g]; mx_sz[g] = st.mx[g]; }
     }
 
     // ---- pass 2: codes in fp32, packed in place
@@ -432,7 +485,7 @@ __device__ __forceinline__ void epilogue_tile(uint32_t tacc, uint32_t acc_empty,
         }
         pack_chunk<D, G, KIND>(v, ch, mn, inv, words);
     }
-    if (ok) store_row<D, G>(words, mn, mx, slot, head, h_kv, KIND, int2_pool);
+    if (ok) store_row<D, G>(words, mn_sz, mx_sz, slot, head, h_kv, KIND, int2_pool);
 }
 
 template <int D, int G>
@@ -459,15 +512,15 @@ write_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant
     auto full = [&](int s) { return bar0 + 8 * s; };
     auto empty = [&](int s) { return bar0 + 8 * (kStages + s); };
     auto acc_full = [&](int a) { return bar0 + 8 * (2 * kStages + a); };
-    auto acc_empty = [&](int a) { return bar0 + 8 * (2 * kStages + kGroups + a); };
-    const uint32_t b_full = bar0 + 8 * (2 * kStages + 2 * kGroups);
+    auto acc_empty = [&](int a) { return bar0 + 8 * (2 * kStages + kAccs + a); };
+    const uint32_t b_full = bar0 + 8 * (2 * kStages + 2 * kAccs);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kOffMisc);
     volatile int* fail = reinterpret_cast<volatile int*>(smem + L::kOffMisc + 4);
     const size_t pair = (size_t)kind * h_kv + head;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) { mbar_init(full(s), 1); mbar_init(empty(s), 1); }
-        for (int a = 0; a < kGroups; ++a) { mbar_init(acc_full(a), 1); mbar_init(acc_empty(a), 128); }
+        for (int a = 0; a < kAccs; ++a) { mbar_init(acc_full(a), 1); mbar_init(acc_empty(a), 128); }
         mbar_init(b_full, 1);
         *fail = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -529,8 +582,8 @@ write_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant
             }
             for (int i = 0; ok && i < my_tiles; ++i) {
                 if (*fail) break;
-                const int s = i % kStages, a = i % kGroups;
-                if (!mbar_wait(acc_empty(a), ((i / kGroups) & 1) ^ 1) || !mbar_wait(full(s), (i / kStages) & 1)) {
+                const int s = i % kStages, a = i % kAccs;
+                if (!mbar_wait(acc_empty(a), ((i / kAccs) & 1) ^ 1) || !mbar_wait(full(s), (i / kStages) & 1)) {
                     *fail = 1;
                     record_error(&dbg->kind, &dbg->index, 4, i);
                     break;
@@ -553,10 +606,10 @@ write_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant
                 issued = i + 1;
             }
             // drain: the last commit covers every MMA issued before it
-            if (issued > 0) (void)mbar_wait(acc_full((issued - 1) % kGroups), ((issued - 1) / kGroups) & 1);
+            if (issued > 0) (void)mbar_wait(acc_full((issued - 1) % kAccs), ((issued - 1) / kAccs) & 1);
         }
     } else {
-        // ---- epilogue: warp-group e takes local tiles e, e + kGroups, ... with accumulator e;
+        // ---- epilogue: warp-group e takes local tiles e, e + kGroups, ... (accumulator i % kAccs);
         // thread = token row = TMEM lane 32*(warp%4) + lane
         const int e = (warp - 2) / 4;
         const int q = warp % 4;
@@ -564,10 +617,11 @@ write_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant
         const __nv_bfloat16* x_base = kind == 0 ? k_in : v_in;
         const float* rt_head = (kind == 0 ? r_kt : r_vt) + (size_t)head * D * D;
         for (int i = e; i < my_tiles; i += kGroups) {
+            const int a = i % kAccs;
             const int tok = ((int)blockIdx.x + i * (int)gridDim.x) * kTile + m;
             bool ok = tok < n;
             const int64_t slot = ok ? dst_slots[tok] : -1;        // issued before the wait
-            const bool got = mbar_wait(acc_full(e), (i / kGroups) & 1);
+            const bool got = mbar_wait(acc_full(a), (i / kAccs) & 1);
             const int stop = *fail;
             if (__any_sync(0xffffffffu, !got || stop)) {       // warp-uniform exit
                 if (lane == 0) {
@@ -581,11 +635,11 @@ write_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant
                 if (debug) record_error(&dbg->kind, &dbg->index, 1, slot);
                 ok = false;
             }
-            const uint32_t tacc = tmem + e * D + ((uint32_t)(32 * q) << 16);
+            const uint32_t tacc = tmem + a * D + ((uint32_t)(32 * q) << 16);
             if (kind == 0)
-                epilogue_tile<D, G, 0>(tacc, acc_empty(e), t_s, tok, slot, ok, head, h_kv, x_base, rt_head, int2_pool, lane);
+                epilogue_tile<D, G, 0>(tacc, acc_empty(a), t_s, tok, slot, ok, head, h_kv, x_base, rt_head, int2_pool, lane);
             else
-                epilogue_tile<D, G, 1>(tacc, acc_empty(e), t_s, tok, slot, ok, head, h_kv, x_base, rt_head, int2_pool, lane);
+                epilogue_tile<D, G, 1>(tacc, acc_empty(a), t_s, tok, slot, ok, head, h_kv, x_base, rt_head, int2_pool, lane);
         }
     }
 
