@@ -151,10 +151,12 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t phase) {
 //     in the K layout, so that code(c) * 2^(2p'-24) * qb = code * r_part * 2^-20;
 //   kap = 2^(E + 9): S_part = accumulator * kap * 2^(-11 part);
 //   qsum[g] = sum over group g of q_rot (hi, lo).
+// q_rot here already carries sm_scale * log2(e), so the INT2 logits come out in log2 units.
 template <int D, int G>
 __global__ void __launch_bounds__(4 * D)
 q_prep_kernel(const __nv_bfloat16* __restrict__ q, const float* __restrict__ r_k,
-              __half* __restrict__ qb, float* __restrict__ kap, float* __restrict__ qsum, int h_q, int g) {
+              __half* __restrict__ qb, float* __restrict__ kap, float* __restrict__ qsum, int h_q, int g,
+              float sl2_hi, float sl2_lo) {
     constexpr int NG = D / G;
     constexpr int Q4 = D / 4;                      // terms per thread: four threads per output channel
     __shared__ float qs[D];
@@ -196,6 +198,15 @@ q_prep_kernel(const __nv_bfloat16* __restrict__ q, const float* __restrict__ r_k
     {
         float s2, e2;
         two_sum(h, l, s2, e2);
+        h = s2;
+        l = e2;
+    }
+    // times sm_scale * log2(e) (hi + lo): the INT2 logits come out in log2 units
+    {
+        float p, e, s2, e2;
+        two_prod(h, sl2_hi, p, e);
+        e = __fmaf_rn(h, sl2_lo, __fmaf_rn(l, sl2_hi, e));
+        two_sum(p, e, s2, e2);
         h = s2;
         l = e2;
     }
@@ -363,16 +374,20 @@ __device__ void int2_split(const SplitArgs& a, int split, int kv, int b, uint8_t
     }
     __syncwarp();
     uint32_t valid_mask = 0u;    // bit s: stage s holds a real page
+    // launch arguments used every page, held in registers
+    const uint8_t* const pool_kv = a.int2_pool + (size_t)kv * GE::kBlock;
+    const size_t page_stride = (size_t)a.h_kv * GE::kBlock;
+    const int64_t pool_pages = a.int2_pages;
+    const bool dbg_on = a.debug != 0;
     auto issue = [&](int j) {
         const int s = j % kStages;
         const int32_t phys = __shfl_sync(0xffffffffu, ((j >> 5) & 1) ? ids1 : ids0, j & 31);
-        const bool ok = phys >= 0 && phys < a.int2_pages;
-        if (!ok && a.debug && lane == 0) record_error(&a.dbg->kind, &a.dbg->index, 2, phys);
+        const bool ok = phys >= 0 && phys < pool_pages;
+        if (!ok && dbg_on && lane == 0) record_error(&a.dbg->kind, &a.dbg->index, 2, phys);
         valid_mask = ok ? (valid_mask | (1u << s)) : (valid_mask & ~(1u << s));
         if (lane == 0) {
             if (ok)
-                bulk_load(stage_s + s * GE::kBlock, a.int2_pool + ((size_t)phys * a.h_kv + kv) * GE::kBlock,
-                          GE::kBlock, bar_s + 8 * s);
+                bulk_load(stage_s + s * GE::kBlock, pool_kv + (size_t)phys * page_stride, GE::kBlock, bar_s + 8 * s);
             else
                 mbar_arrive(bar_s + 8 * s);
         }
@@ -418,7 +433,6 @@ __device__ void int2_split(const SplitArgs& a, int split, int kv, int b, uint8_t
         }
     }
     const float pvs = a.pv_scale[kv];
-    const float sl2 = a.scale_log2, sl2_lo = a.scale_log2_lo;
 
 
     bool failed = false;
@@ -500,10 +514,8 @@ __device__ void int2_split(const SplitArgs& a, int split, int kv, int b, uint8_t
                             dl = __fadd_rn(dl, __fadd_rn(low, e4));
                         }
                     }
-                    float p_, e_;
-                    two_prod(dh, sl2, p_, e_);
-                    lh[slot] = p_;
-                    ll[slot] = __fadd_rn(e_, __fmaf_rn(dl, sl2, __fmul_rn(dh, sl2_lo)));
+                    lh[slot] = dh;          // already in log2 units (the query carries the scale)
+                    ll[slot] = dl;
                 }
                 const bool ok0 = v0 && (4 * hb + tig < GQ), ok1 = v1 && (4 * hb + tig < GQ);
                 if (!ok0) { lh[0] = -INFINITY; ll[0] = 0.0f; }
@@ -534,8 +546,9 @@ __device__ void int2_split(const SplitArgs& a, int split, int kv, int b, uint8_t
                 for (int gg = 0; gg < NG; ++gg) {
                     const float2 s0 = __half22float2(vsz[gid * NG + gg]);
                     const float2 s1 = __half22float2(vsz[(gid + 8) * NG + gg]);
-                    const float x0 = ok0 ? fminf(__fmul_rn(__fmul_rn(p0, s0.x), pvs), 65504.0f) : 0.0f;
-                    const float x1 = ok1 ? fminf(__fmul_rn(__fmul_rn(p1, s1.x), pvs), 65504.0f) : 0.0f;
+                    // p <= 1 and s_v <= (2/3) max T_v, so x <= 32752 (1 + tiny): fp16 without a clamp
+                    const float x0 = ok0 ? __fmul_rn(__fmul_rn(p0, s0.x), pvs) : 0.0f;
+                    const float x1 = ok1 ? __fmul_rn(__fmul_rn(p1, s1.x), pvs) : 0.0f;
                     const __half h0 = __float2half_rn(x0), h1 = __float2half_rn(x1);
                     Pv[hb][gg][0] = pack_half2(h0, __float2half_rn(__fmul_rn(__fsub_rn(x0, __half2float(h0)), 2048.0f)));
                     Pv[hb][gg][1] = pack_half2(h1, __float2half_rn(__fmul_rn(__fsub_rn(x1, __half2float(h1)), 2048.0f)));
@@ -1007,12 +1020,14 @@ cudaError_t launch_decode(const Shape& s, const LayerParams& prm, const DecodePl
     float* qsum = kap + nh;
     const __nv_bfloat16* q = static_cast<const __nv_bfloat16*>(a.q);
 
+    const double sl2d = s.sm_scale * 1.4426950408889634073599;     // sm_scale * log2(e)
+    const float sl2_hi = (float)sl2d, sl2_lo = (float)(sl2d - (double)sl2_hi);
     cudaError_t e = cudaSuccess;
     {
         ProfScope ps(prof, OSCAR_KERNEL_QROT, st);
 #define OSCAR_QPREP_CASE(D_, G_) \
         if (s.d == D_ && s.group == G_) \
-            e = launch_pdl(q_prep_kernel<D_, G_>, dim3(a.batch * s.h_q), dim3(4 * D_), 0, st, q, prm.r_k, qb, kap, qsum, s.h_q, g);
+            e = launch_pdl(q_prep_kernel<D_, G_>, dim3(a.batch * s.h_q), dim3(4 * D_), 0, st, q, prm.r_k, qb, kap, qsum, s.h_q, g, sl2_hi, sl2_lo);
         OSCAR_QPREP_CASE(64, 32)
         OSCAR_QPREP_CASE(64, 64)
         OSCAR_QPREP_CASE(128, 32)
@@ -1035,11 +1050,8 @@ cudaError_t launch_decode(const Shape& s, const LayerParams& prm, const DecodePl
     sa.bf16_splits = plan.bf16_splits;
     sa.bf16_pages_per_split = (s.sink + s.recent + kPage - 1) / kPage;
     sa.total_splits = plan.total_splits;
-    {
-        const double sl2 = s.sm_scale * 1.4426950408889634073599;
-        sa.scale_log2 = (float)sl2;
-        sa.scale_log2_lo = (float)(sl2 - (double)sa.scale_log2);
-    }
+    sa.scale_log2 = sl2_hi;
+    sa.scale_log2_lo = sl2_lo;
     sa.debug = s.debug; sa.dbg = dbg;
 
     ProfScope ps_split(prof, OSCAR_KERNEL_SPLIT, st);

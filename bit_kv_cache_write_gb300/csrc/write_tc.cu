@@ -23,7 +23,8 @@
 // off by under 2^-24 M, plus the final truncation), with M bounded
 // by sum_i |x_i R_ic| <= ||x||_2 (R orthogonal). Only the d/16 steps of the
 // leading piece carry a full-size M. When that bound could move the stored zero
-// or scale by more than one fp16 ulp, the candidate min/max channels are
+// or scale by more than one fp16 step (tested on the fp16 roundings of the bound's ends), the
+// candidate min/max channels are
 // recomputed with a double-float dot product over a row of R^T (batches of 8 channels spread over
 // the warp), as on the CUDA-core path. Those exact values set the stored zero and scale.
 //
@@ -225,6 +226,28 @@ __device__ __forceinline__ void group_inv(const float* mn, const float* mx, floa
     }
 }
 
+// fp16 (round to nearest even) of x as an integer that is monotone in x: consecutive fp16 values
+// differ by one.
+__device__ __forceinline__ int f16_ordered(float x) {
+    const int b = (int)__half_as_ushort(__float2half_rn(x));
+    return (b & 0x8000) ? 0x8000 - b : b + 0x8000;
+}
+
+// Whether a value known to lie within +-e of v could round to an fp16 more than one step away
+// from fp16(v).
+__device__ __forceinline__ bool f16_unsure(float v, float e) {
+    const int o = f16_ordered(v);
+    return o - f16_ordered(v - e) > 1 || f16_ordered(v + e) - o > 1;
+}
+
+// The stored zero fp16(mn) and scale fp16((mx - mn) / 3) of a group whose exact min/max lie
+// within +-err of (mn, mx): bit 0 = the zero may be off by more than one fp16 step, bit 1 = the
+// scale may.
+__device__ __forceinline__ int sz_unsure(float mn, float mx, float err) {
+    const float e = err * 1.01f;                 // covers the fp32 rounding of the tests themselves
+    return (f16_unsure(mn, e) ? 1 : 0) | (f16_unsure(__fdiv_rn(__fsub_rn(mx, mn), 3.0f), e * (2.0f / 3.0f)) ? 2 : 0);
+}
+
 template <int NG>
 struct GroupStats {
     float mn[NG], mx[NG];
@@ -257,9 +280,9 @@ __device__ __noinline__ GroupStats<D / G> exact_fixup(uint32_t tacc, const float
     bool need_min[NG], need_max[NG];
 #pragma unroll
     for (int g = 0; g < NG; ++g) {
-        const float r0 = st.mx[g] - st.mn[g];
-        need_min[g] = need && (fabsf(st.mn[g]) < 4096.0f * err || r0 < 8192.0f * err);
-        need_max[g] = need && r0 < 8192.0f * err;
+        const int u = need ? sz_unsure(st.mn[g], st.mx[g], err) : 0;
+        need_min[g] = u != 0;                       // the scale needs both ends
+        need_max[g] = (u & 2) != 0;
         lo_cut[g] = need_min[g] ? st.mn[g] + 2.0f * err : -FLT_MAX;
         hi_cut[g] = need_max[g] ? st.mx[g] - 2.0f * err : FLT_MAX;
         if (need_min[g]) nc.mn[g] = FLT_MAX;
@@ -443,7 +466,7 @@ __device__ __forceinline__ void epilogue_tile(uint32_t tacc, uint32_t acc_empty,
     const float err = 1.01f * (float)(D / 16) * 9.0f * 0x1p-23f * sqrtf((sq0 + sq1) * 1.002f);
     bool need = false;
 #pragma unroll
-    for (int g = 0; g < NG; ++g) need |= ok && (fabsf(mn[g]) < 4096.0f * err || (mx[g] - mn[g]) < 8192.0f * err);
+    for (int g = 0; g < NG; ++g) need |= ok && sz_unsure(mn[g], mx[g], err) != 0;
     // stats for the stored scale/zero; the codes use the tensor-core stats (their shift is far
     // inside the rounding tolerance, and min/max channels code 0/3 either way)
     float mn_sz[NG], mx_sz[NG];
