@@ -28,6 +28,10 @@
 // recomputed with a double-float dot product over a row of R^T (batches of 8 channels spread over
 // the warp), as on the CUDA-core path. Those exact values set the stored zero and scale.
 //
+// Every CTA takes a share of one head's token tiles for K and then the same tiles for V, so the
+// rare exact path (mostly V rows) spreads evenly over the GPU; R_v replaces R_k in shared memory
+// once the K tiles' MMAs are done.
+//
 // Roles: warp 0 loads (TMA), warp 1 allocates tensor memory and issues the MMAs,
 // warps 2..9 run the epilogue as two warp-groups that take alternate tiles, each with its own
 // accumulator (warp w reads TMEM lanes 32*(w%4) .. +31). Every
@@ -65,7 +69,7 @@ struct TcLayout {
     static constexpr int kOffB = 0;
     static constexpr int kOffA = kOffB + kPieces * kPieceBytes;
     static constexpr int kOffT = kOffA + kStages * kTileBytes;
-    static constexpr int kOffBar = kOffT + D * 4;
+    static constexpr int kOffBar = kOffT + 2 * D * 4;          // T_k and T_v of the head
     static constexpr int kBars = 2 * kStages + 2 * kAccs + 1;     // full, empty, acc_full[], acc_empty[], b_full
     static constexpr int kOffMisc = kOffBar + kBars * 8;
     static constexpr int kBytes = kOffMisc + 16;
@@ -258,85 +262,90 @@ struct ChunkStats {
     float mn[NCH], mx[NCH];
 };
 
-// Rare path for a whole warp-tile: some row has a group whose stored zero or scale could be off
-// by more than one fp16 ulp. Every channel that may hold such a group's min (max) is recomputed
-// exactly, and the group's min/max for the stored zero and scale are redone from the other
-// channels and the exact ones. Only 32-channel chunks whose min (max) comes near the cut are
-// reread. Exact dots run over the whole warp (lane l takes terms PER*l ..), up to 4 candidates
-// at a time with their loads issued together. (The codes of these channels are 0 near the min
-// and 3 near the max either way.)
+template <int NG, int NCH>
+struct FixState {
+    uint32_t cand[NCH];                             // candidate channels, bit j of word ch = channel 32ch+j
+    float mn[NG], mx[NG];                           // stats over non-candidates (+ exact candidates)
+    bool need_min[NG], need_max[NG];
+};
+
+// Rare path for a warp-tile, part 1 (needs the accumulator): some row has a group whose stored
+// zero or scale could be off by more than one fp16 step. Marks every channel that may hold such
+// a group's min (max) as a candidate and takes the group stats over the other channels. Only
+// 32-channel chunks whose min (max) comes near the cut are reread.
 template <int D, int G>
-__device__ __noinline__ GroupStats<D / G> exact_fixup(uint32_t tacc, const float* __restrict__ t_s, int tok,
-                                                       bool need, float err, GroupStats<D / G> st,
-                                                       ChunkStats<D / 32> cs, int head, int h_kv,
+__device__ __noinline__ FixState<D / G, D / 32> fixup_detect(uint32_t tacc, const float* __restrict__ t_s,
+                                                              bool need, float err, GroupStats<D / G> st,
+                                                              ChunkStats<D / 32> cs) {
+    constexpr int NG = D / G;
+    constexpr int NCH = D / 32;
+    FixState<NG, NCH> fs;
+    float lo_cut[NG], hi_cut[NG];
+#pragma unroll
+    for (int g = 0; g < NG; ++g) {
+        const int u = need ? sz_unsure(st.mn[g], st.mx[g], err) : 0;
+        fs.need_min[g] = u != 0;                    // the scale needs both ends
+        fs.need_max[g] = (u & 2) != 0;
+        lo_cut[g] = fs.need_min[g] ? st.mn[g] + 2.0f * err : -FLT_MAX;
+        hi_cut[g] = fs.need_max[g] ? st.mx[g] - 2.0f * err : FLT_MAX;
+        fs.mn[g] = fs.need_min[g] ? FLT_MAX : st.mn[g];
+        fs.mx[g] = fs.need_max[g] ? -FLT_MAX : st.mx[g];
+    }
+    for (int ch = 0; ch < NCH; ++ch) {
+        const int g = (32 * ch) / G;
+        float lc = -FLT_MAX, hc = FLT_MAX, cmn0 = 0.0f, cmx0 = 0.0f;
+        bool nmin = false, nmax = false;
+#pragma unroll
+        for (int k = 0; k < NCH; ++k)
+            if (k == ch) { cmn0 = cs.mn[k]; cmx0 = cs.mx[k]; }
+#pragma unroll
+        for (int gg = 0; gg < NG; ++gg)
+            if (gg == g) { lc = lo_cut[gg]; hc = hi_cut[gg]; nmin = fs.need_min[gg]; nmax = fs.need_max[gg]; }
+        const bool touched = cmn0 <= lc || cmx0 >= hc;
+        uint32_t cm = 0u;
+        float cmn = cmn0, cmx = cmx0;
+        if (__any_sync(0xffffffffu, touched)) {
+            float v[32];
+            tmem_ld32(tacc + 32 * ch, v);
+            tmem_wait_ld();
+            if (touched) {
+                cmn = FLT_MAX;
+                cmx = -FLT_MAX;
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    const float xh = fminf(fmaxf(v[j], -t_s[32 * ch + j]), t_s[32 * ch + j]);
+                    const bool is_c = xh <= lc || xh >= hc;
+                    cm |= (uint32_t)is_c << j;
+                    if (!is_c) { cmn = fminf(cmn, xh); cmx = fmaxf(cmx, xh); }
+                }
+            }
+        }
+#pragma unroll
+        for (int gg = 0; gg < NG; ++gg)
+            if (gg == g) {
+                if (nmin) fs.mn[gg] = fminf(fs.mn[gg], cmn);
+                if (nmax) fs.mx[gg] = fmaxf(fs.mx[gg], cmx);
+            }
+#pragma unroll
+        for (int k = 0; k < NCH; ++k)
+            if (k == ch) fs.cand[k] = cm;
+    }
+    return fs;
+}
+
+// Part 2 (after the accumulator is released): the candidates' exact values, each a double-float
+// dot over a row of R^T spread across the warp (lane l takes terms PER*l ..), up to 4 candidates
+// at a time with their loads issued together; returns the repaired stats of this row's groups.
+// (The codes of these channels are 0 near the min and 3 near the max either way.)
+template <int D, int G>
+__device__ __noinline__ GroupStats<D / G> fixup_exact(FixState<D / G, D / 32> fs, const float* __restrict__ t_s,
+                                                       int tok, int head, int h_kv,
                                                        const __nv_bfloat16* __restrict__ x_base,
                                                        const float* __restrict__ rt_head, int lane) {
     constexpr int NG = D / G;
     constexpr int NCH = D / 32;
     constexpr int PER = D / 32;                     // terms per lane
     constexpr int B = 4;                            // candidates per round
-    float lo_cut[NG], hi_cut[NG];
-    GroupStats<NG> nc = st;                         // stats over non-candidates (+ exact candidates)
-    bool need_min[NG], need_max[NG];
-#pragma unroll
-    for (int g = 0; g < NG; ++g) {
-        const int u = need ? sz_unsure(st.mn[g], st.mx[g], err) : 0;
-        need_min[g] = u != 0;                       // the scale needs both ends
-        need_max[g] = (u & 2) != 0;
-        lo_cut[g] = need_min[g] ? st.mn[g] + 2.0f * err : -FLT_MAX;
-        hi_cut[g] = need_max[g] ? st.mx[g] - 2.0f * err : FLT_MAX;
-        if (need_min[g]) nc.mn[g] = FLT_MAX;
-        if (need_max[g]) nc.mx[g] = -FLT_MAX;
-    }
-    uint32_t cand[NCH];
-    for (int ch = 0; ch < NCH; ++ch) {
-        const int g = (32 * ch) / G;
-        float lc = -FLT_MAX, hc = FLT_MAX;
-        bool touched = false;
-#pragma unroll
-        for (int k = 0; k < NCH; ++k)
-            if (k == ch) touched = need && (cs.mn[k] <= lo_cut[k * 32 / G] || cs.mx[k] >= hi_cut[k * 32 / G]);
-        uint32_t cm = 0u;
-        if (__any_sync(0xffffffffu, touched)) {
-#pragma unroll
-            for (int gg = 0; gg < NG; ++gg)
-                if (gg == g) { lc = lo_cut[gg]; hc = hi_cut[gg]; }
-            float v[32];
-            tmem_ld32(tacc + 32 * ch, v);
-            tmem_wait_ld();
-            float cmn = FLT_MAX, cmx = -FLT_MAX;
-#pragma unroll
-            for (int j = 0; j < 32; ++j) {
-                const float xh = fminf(fmaxf(v[j], -t_s[32 * ch + j]), t_s[32 * ch + j]);
-                const bool is_c = touched && (xh <= lc || xh >= hc);
-                cm |= (uint32_t)is_c << j;
-                if (!is_c) { cmn = fminf(cmn, xh); cmx = fmaxf(cmx, xh); }
-            }
-            if (touched) {
-#pragma unroll
-                for (int gg = 0; gg < NG; ++gg)
-                    if (gg == g) {
-                        if (need_min[gg]) nc.mn[gg] = fminf(nc.mn[gg], cmn);
-                        if (need_max[gg]) nc.mx[gg] = fmaxf(nc.mx[gg], cmx);
-                    }
-            }
-        } else if (need) {
-            // untouched chunk of a group under repair: its stats count as non-candidates
-#pragma unroll
-            for (int k = 0; k < NCH; ++k)
-                if (k == ch) {
-#pragma unroll
-                    for (int gg = 0; gg < NG; ++gg)
-                        if (gg == g) {
-                            if (need_min[gg]) nc.mn[gg] = fminf(nc.mn[gg], cs.mn[k]);
-                            if (need_max[gg]) nc.mx[gg] = fmaxf(nc.mx[gg], cs.mx[k]);
-                        }
-                }
-        }
-#pragma unroll
-        for (int k = 0; k < NCH; ++k)
-            if (k == ch) cand[k] = cm;
-    }
     for (;;) {
         int s_src[B], s_c[B];
         float rv[B][PER], xv[B][PER];
@@ -344,7 +353,7 @@ __device__ __noinline__ GroupStats<D / G> exact_fixup(uint32_t tacc, const float
         for (int k = 0; k < B; ++k) {
             bool mine = false;
 #pragma unroll
-            for (int ch = 0; ch < NCH; ++ch) mine |= cand[ch] != 0u;
+            for (int ch = 0; ch < NCH; ++ch) mine |= fs.cand[ch] != 0u;
             const uint32_t has = __ballot_sync(0xffffffffu, mine);
             s_src[k] = has ? __ffs(has) - 1 : -1;
             int myc = 0;
@@ -352,9 +361,9 @@ __device__ __noinline__ GroupStats<D / G> exact_fixup(uint32_t tacc, const float
                 bool done = false;
 #pragma unroll
                 for (int ch = 0; ch < NCH; ++ch)
-                    if (!done && cand[ch]) {
-                        myc = 32 * ch + __ffs(cand[ch]) - 1;
-                        cand[ch] &= cand[ch] - 1;
+                    if (!done && fs.cand[ch]) {
+                        myc = 32 * ch + __ffs(fs.cand[ch]) - 1;
+                        fs.cand[ch] &= fs.cand[ch] - 1;
                         done = true;
                     }
             }
@@ -408,13 +417,16 @@ __device__ __noinline__ GroupStats<D / G> exact_fixup(uint32_t tacc, const float
 #pragma unroll
                 for (int g = 0; g < NG; ++g)
                     if (c / G == g) {
-                        if (need_min[g]) nc.mn[g] = fminf(nc.mn[g], exc);
-                        if (need_max[g]) nc.mx[g] = fmaxf(nc.mx[g], exc);
+                        if (fs.need_min[g]) fs.mn[g] = fminf(fs.mn[g], exc);
+                        if (fs.need_max[g]) fs.mx[g] = fmaxf(fs.mx[g], exc);
                     }
             }
         }
     }
-    return need ? nc : st;
+    GroupStats<NG> out;
+#pragma unroll
+    for (int g = 0; g < NG; ++g) { out.mn[g] = fs.mn[g]; out.mx[g] = fs.mx[g]; }
+    return out;
 }
 
 // Epilogue of one tile for one warp: lane = token row, its fp32 row in TMEM at tacc. Two passes
@@ -472,16 +484,16 @@ __device__ __forceinline__ void epilogue_tile(uint32_t tacc, uint32_t acc_empty,
     float mn_sz[NG], mx_sz[NG];
 #pragma unroll
     for (int g = 0; g < NG; ++g) { mn_sz[g] = mn[g]; mx_sz[g] = mx[g]; }
-    if (__any_sync(0xffffffffu, need)) {
+    const bool any_need = __any_sync(0xffffffffu, need);
+    FixState<NG, NCH> fs;
+    if (any_need) {
         GroupStats<NG> st;
 #pragma unroll
         for (int g = 0; g < NG; ++g) { st.mn[g] = mn[g]; st.mx[g] = mx[g]; }
         ChunkStats<NCH> cs;
 #pragma unroll
         for (int k = 0; k < NCH; ++k) { cs.mn[k] = chmn[k]; cs.mx[k] = chmx[k]; }
-        st = exact_fixup<D, G>(tacc, t_s, tok, need, err, st, cs, head, h_kv, x_base, rt_head, lane);
-#pragma unroll
-        for (int g = 0; g < NG; ++g) { mn_sz[g] = st.mn[g]; mx_sz[g] = st.mx[g]; }
+        fs = fixup_detect<D, G>(tacc, t_s, need, err, st, cs);
     }
 
     // ---- pass 2: codes in fp32, packed in place
@@ -508,6 +520,13 @@ __device__ __forceinline__ void epilogue_tile(uint32_t tacc, uint32_t acc_empty,
         }
         pack_chunk<D, G, KIND>(v, ch, mn, inv, words);
     }
+    if (any_need) {                                 // the accumulator is free again by now
+        const GroupStats<NG> st = fixup_exact<D, G>(fs, t_s, tok, head, h_kv, x_base, rt_head, lane);
+        if (need) {
+#pragma unroll
+            for (int g = 0; g < NG; ++g) { mn_sz[g] = st.mn[g]; mx_sz[g] = st.mx[g]; }
+        }
+    }
     if (ok) store_row<D, G>(words, mn_sz, mx_sz, slot, head, h_kv, KIND, int2_pool);
 }
 
@@ -523,10 +542,14 @@ write_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant
     extern __shared__ uint8_t smem_raw[];
     // 1024-byte aligned base (pointer arithmetic keeps the shared address space visible)
     uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-    const int head = blockIdx.y, kind = blockIdx.z;
+    // every CTA takes its share of this head's token tiles for K, then the same tiles for V
+    // (local tiles 0 .. my_tiles-1 are K, my_tiles .. 2 my_tiles-1 are V)
+    const int head = blockIdx.y;
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const int n_tiles = (n + kTile - 1) / kTile;
     const int my_tiles = (int)blockIdx.x < n_tiles ? (n_tiles - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
+    const int my_total = 2 * my_tiles;
+    auto tile_of = [&](int i) { return (int)blockIdx.x + (i < my_tiles ? i : i - my_tiles) * (int)gridDim.x; };
 
     const uint32_t sb = smem_u32(smem);
     const uint32_t b_s = sb + L::kOffB, a_s = sb + L::kOffA;
@@ -539,7 +562,6 @@ write_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant
     const uint32_t b_full = bar0 + 8 * (2 * kStages + 2 * kAccs);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kOffMisc);
     volatile int* fail = reinterpret_cast<volatile int*>(smem + L::kOffMisc + 4);
-    const size_t pair = (size_t)kind * h_kv + head;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) { mbar_init(full(s), 1); mbar_init(empty(s), 1); }
@@ -548,13 +570,15 @@ write_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant
         *fail = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        // the three pieces of this pair's R: calibration data, loaded before waiting on the
-        // preceding grid
+        // the three pieces of R_k of this head: calibration data, loaded before waiting on the
+        // preceding grid (R_v replaces them after the last K tile)
         mbar_expect_tx(b_full, kPieces * L::kPieceBytes);
         for (int p = 0; p < kPieces; ++p)
-            bulk_load(b_s + p * L::kPieceBytes, r_img + (pair * kPieces + p) * (size_t)(D * D), L::kPieceBytes, b_full);
+            bulk_load(b_s + p * L::kPieceBytes, r_img + ((size_t)head * kPieces + p) * (size_t)(D * D), L::kPieceBytes,
+                      b_full);
     }
-    for (int i = threadIdx.x; i < D; i += kThreads) t_s[i] = t_all[pair * D + i];
+    for (int i = threadIdx.x; i < 2 * D; i += kThreads)
+        t_s[i] = t_all[((size_t)(i / D) * h_kv + head) * D + i % D];
     if (warp == 1) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
                      :: "r"(smem_u32(tmem_slot)), "r"(L::kTmemCols) : "memory");
@@ -572,9 +596,9 @@ write_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant
     if (warp == 0) {
         // ---- TMA producer
         if (lane == 0) {
-            const CUtensorMap* map = kind == 0 ? &map_k : &map_v;
             int issued = 0;
-            for (int i = 0; i < my_tiles; ++i) {
+            for (int i = 0; i < my_total; ++i) {
+                const CUtensorMap* map = i < my_tiles ? &map_k : &map_v;
                 if (*fail) break;
                 const int s = i % kStages;
                 if (!mbar_wait(empty(s), ((i / kStages) & 1) ^ 1)) {
@@ -582,7 +606,7 @@ write_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant
                     record_error(&dbg->kind, &dbg->index, 4, i);
                     break;
                 }
-                const int tile = (int)blockIdx.x + i * (int)gridDim.x;
+                const int tile = tile_of(i);
                 mbar_expect_tx(full(s), L::kTileBytes);
 #pragma unroll
                 for (int h = 0; h < L::kHalves; ++h)
@@ -603,8 +627,26 @@ write_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant
                 *fail = 1;
                 record_error(&dbg->kind, &dbg->index, 4, -1);
             }
-            for (int i = 0; ok && i < my_tiles; ++i) {
+            for (int i = 0; ok && i < my_total; ++i) {
                 if (*fail) break;
+                if (i == my_tiles) {
+                    // switch to R_v: every K-tile MMA must have finished reading the pieces
+                    if (!mbar_wait(acc_full((i - 1) % kAccs), ((i - 1) / kAccs) & 1)) {
+                        *fail = 1;
+                        record_error(&dbg->kind, &dbg->index, 4, i);
+                        break;
+                    }
+                    tc_fence_after();
+                    mbar_expect_tx(b_full, kPieces * L::kPieceBytes);
+                    for (int p = 0; p < kPieces; ++p)
+                        bulk_load(b_s + p * L::kPieceBytes, r_img + (((size_t)h_kv + head) * kPieces + p) * (size_t)(D * D),
+                                  L::kPieceBytes, b_full);
+                    if (!mbar_wait(b_full, 1)) {
+                        *fail = 1;
+                        record_error(&dbg->kind, &dbg->index, 4, i);
+                        break;
+                    }
+                }
                 const int s = i % kStages, a = i % kAccs;
                 if (!mbar_wait(acc_empty(a), ((i / kAccs) & 1) ^ 1) || !mbar_wait(full(s), (i / kStages) & 1)) {
                     *fail = 1;
@@ -637,11 +679,12 @@ write_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant
         const int e = (warp - 2) / 4;
         const int q = warp % 4;
         const int m = 32 * q + lane;
-        const __nv_bfloat16* x_base = kind == 0 ? k_in : v_in;
-        const float* rt_head = (kind == 0 ? r_kt : r_vt) + (size_t)head * D * D;
-        for (int i = e; i < my_tiles; i += kGroups) {
+        for (int i = e; i < my_total; i += kGroups) {
             const int a = i % kAccs;
-            const int tok = ((int)blockIdx.x + i * (int)gridDim.x) * kTile + m;
+            const int kind = i < my_tiles ? 0 : 1;
+            const __nv_bfloat16* x_base = kind == 0 ? k_in : v_in;
+            const float* rt_head = (kind == 0 ? r_kt : r_vt) + (size_t)head * D * D;
+            const int tok = tile_of(i) * kTile + m;
             bool ok = tok < n;
             const int64_t slot = ok ? dst_slots[tok] : -1;        // issued before the wait
             const bool got = mbar_wait(acc_full(a), (i / kAccs) & 1);
@@ -662,7 +705,8 @@ write_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant
             if (kind == 0)
                 epilogue_tile<D, G, 0>(tacc, acc_empty(a), t_s, tok, slot, ok, head, h_kv, x_base, rt_head, int2_pool, lane);
             else
-                epilogue_tile<D, G, 1>(tacc, acc_empty(a), t_s, tok, slot, ok, head, h_kv, x_base, rt_head, int2_pool, lane);
+                epilogue_tile<D, G, 1>(tacc, acc_empty(a), t_s + D, tok, slot, ok, head, h_kv, x_base, rt_head, int2_pool,
+                                       lane);
         }
     }
 
@@ -711,13 +755,12 @@ cudaError_t launch_tc(const Shape& s, const LayerParams& p, int num_sms, const v
     if (attr != cudaSuccess) return attr;
     CUtensorMap mk, mv;
     if (!make_row_map(&mk, k, n, s.h_kv, D) || !make_row_map(&mv, v, n, s.h_kv, D)) return cudaErrorInvalidValue;
-    const int pairs = 2 * s.h_kv;
     const int n_tiles = (n + kTile - 1) / kTile;
-    int gx = num_sms / pairs;
+    int gx = num_sms / s.h_kv;
     gx = gx < 1 ? 1 : (gx > n_tiles ? n_tiles : gx);
     ProfScope ps(prof, OSCAR_KERNEL_WRITE, st);
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(gx, s.h_kv, 2);
+    cfg.gridDim = dim3(gx, s.h_kv, 1);
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = L::kDynamic;
     cfg.stream = st;
