@@ -185,14 +185,25 @@ class GpuWorkload:
         self.ws = torch.empty(self.ctx.decode_workspace_size(1, self.hist), dtype=torch.uint8, device=dev)
         self.out = torch.empty(layers, 1, h_q, d, dtype=torch.float32, device=dev)
         self.q_all = torch.cat(self.qs, 0).view(layers, 1, h_q, d).contiguous()
+        self.side = torch.cuda.Stream(device=dev)
+        self.demoted = [torch.cuda.Event() for _ in range(layers)]
         torch.cuda.synchronize()
 
     def step(self):
+        """Per layer: demote the oldest recent token, then decode. The demotes run on a side stream
+        (they depend on nothing the decodes produce); decode(layer) waits for demote(layer)."""
+        import torch
+        main = torch.cuda.current_stream()
+        self.side.wait_stream(main)
         for layer in range(self.layers):
-            self.ctx.demote_recent(layer, self.bf16_pools[layer], self.src, self.int2_pools[layer], self.dst)
+            with torch.cuda.stream(self.side):
+                self.ctx.demote_recent(layer, self.bf16_pools[layer], self.src, self.int2_pools[layer], self.dst)
+                self.demoted[layer].record(self.side)
+            main.wait_event(self.demoted[layer])
             self.ctx.decode(layer, self.q_all[layer], self.int2_pools[layer], self.tables[layer], self.hist_len,
                             self.hist, self.bf16_pools[layer], self.bf16_tables[layer], self.bf16_len,
                             self.out[layer], self.ws)
+        main.wait_stream(self.side)
 
     launches_per_step_per_layer = 4     # write (demote), q rotation, split, merge
 
@@ -478,7 +489,7 @@ def main():
             "config": {"workload": args.workload, "batch": 1, "context": wl.hist + wl.n_bf16, "int2_history": wl.hist,
                        "bf16_tokens": wl.n_bf16, "layers": layers, "h_q": cfg["h_q"], "h_kv": cfg["h_kv"],
                        "head_dim": cfg["d"], "group": cfg["group"], "page_size": P,
-                       "step": "per layer: demote 1 token + decode; one CUDA graph per step",
+                       "step": "per layer: demote 1 token (side stream) + decode after it; one CUDA graph per step",
                        "l2": "inputs larger than L2: %.2f GB of distinct pages per step" % (step_bytes / 1e9),
                        "parallelism": "replicas" if world > 1 else "single GPU"},
             "hbm_gbs_step": step_bytes * args.steps * world / max_sec / 1e9,

@@ -209,7 +209,8 @@ oscar_status oscar_calibrate_upload(oscar_ctx_t* ctx, int layer, const float* R_
         float tmax = 0.0f;
         for (int c = 0; c < s.d; ++c) tmax = std::max(tmax, T_v[(size_t)h * s.d + c]);
         const double smax = std::max(1e-30, (2.0 / 3.0) * (double)tmax * 1.001);
-        int sigma = (int)std::floor(std::log2(32752.0 / smax));
+        // weights reach 2^kSoftmaxHeadroomLog2 between the decode's lazy max updates
+        int sigma = (int)std::floor(std::log2(32752.0 / smax)) - oscar::kSoftmaxHeadroomLog2;
         sigma = std::min(40, std::max(-40, sigma));
         pvs[h] = std::ldexp(1.0f, sigma);
     }

@@ -50,6 +50,7 @@ namespace {
 constexpr int kWarps = 4;
 constexpr int kStages = 4;
 constexpr long long kWaitCycles = 2000000000LL;   // give up on a page copy after ~1 s
+constexpr float kNoMax = -1e30f;                   // running max before any token
 
 __device__ __forceinline__ float fast_exp2(float x) { return exp2f(x); }
 
@@ -358,7 +359,7 @@ __device__ void int2_split(const SplitArgs& a, int split, int kv, int b, uint8_t
     float m_run[NHB], l_run[NHB], zacc[NHB][NG];
 #pragma unroll
     for (int hb = 0; hb < NHB; ++hb) {
-        m_run[hb] = -INFINITY;
+        m_run[hb] = kNoMax;          // finite: ex2(-inf - kNoMax) = 0 without a guard
         l_run[hb] = 0.0f;
 #pragma unroll
         for (int gg = 0; gg < NG; ++gg) zacc[hb][gg] = 0.0f;
@@ -525,16 +526,13 @@ __device__ void int2_split(const SplitArgs& a, int split, int kv, int b, uint8_t
                 mp = fmaxf(mp, __shfl_xor_sync(0xffffffffu, mp, 4));
                 mp = fmaxf(mp, __shfl_xor_sync(0xffffffffu, mp, 8));
                 mp = fmaxf(mp, __shfl_xor_sync(0xffffffffu, mp, 16));
-                const float mn = fmaxf(m_run[hb], mp);
-                float p0 = 0.0f, p1 = 0.0f, alpha = 1.0f;
-                if (mn != -INFINITY) {
-                    alpha = ex2(m_run[hb] - mn);
-                    p0 = ex2(__fadd_rn(__fsub_rn(lh[0], mn), ll[0]));
-                    p1 = ex2(__fadd_rn(__fsub_rn(lh[1], mn), ll[1]));
+                // lazy reference: raised only when a logit passes it by more than 2^kSoftmaxHeadroomLog2,
+                // so p <= 2^8 and the O rescale is rare
+                if (__any_sync(0xffffffffu, mp > m_run[hb] + (float)kSoftmaxHeadroomLog2)) {
+                    const float mn = fmaxf(m_run[hb], mp);
+                    const float alpha = ex2(m_run[hb] - mn);
                     m_run[hb] = mn;
-                }
-                l_run[hb] = __fmaf_rn(l_run[hb], alpha, p0 + p1);
-                if (__any_sync(0xffffffffu, alpha != 1.0f)) {
+                    l_run[hb] *= alpha;
 #pragma unroll
                     for (int mm = 0; mm < NK; ++mm)
 #pragma unroll
@@ -542,11 +540,15 @@ __device__ void int2_split(const SplitArgs& a, int split, int kv, int b, uint8_t
 #pragma unroll
                     for (int gg = 0; gg < NG; ++gg) zacc[hb][gg] *= alpha;
                 }
+                const float p0 = ex2(__fadd_rn(__fsub_rn(lh[0], m_run[hb]), ll[0]));
+                const float p1 = ex2(__fadd_rn(__fsub_rn(lh[1], m_run[hb]), ll[1]));
+                l_run[hb] = __fadd_rn(l_run[hb], __fadd_rn(p0, p1));
 #pragma unroll
                 for (int gg = 0; gg < NG; ++gg) {
                     const float2 s0 = __half22float2(vsz[gid * NG + gg]);
                     const float2 s1 = __half22float2(vsz[(gid + 8) * NG + gg]);
-                    // p <= 1 and s_v <= (2/3) max T_v, so x <= 32752 (1 + tiny): fp16 without a clamp
+                    // p <= 2^8 and s_v <= (2/3) max T_v, and 2^sigma leaves that headroom, so
+                    // x <= 32752 (1 + tiny): fp16 without a clamp
                     const float x0 = ok0 ? __fmul_rn(__fmul_rn(p0, s0.x), pvs) : 0.0f;
                     const float x1 = ok1 ? __fmul_rn(__fmul_rn(p1, s1.x), pvs) : 0.0f;
                     const __half h0 = __float2half_rn(x0), h1 = __float2half_rn(x1);
@@ -651,7 +653,7 @@ __device__ void int2_split(const SplitArgs& a, int split, int kv, int b, uint8_t
         float mm_ = -INFINITY;
 #pragma unroll
         for (int w2 = 0; w2 < kWarps; ++w2) mm_ = fmaxf(mm_, ml_s[w2][h][0]);
-        const float f = m_run[hb] == -INFINITY ? 0.0f : fast_exp2(m_run[hb] - mm_);
+        const float f = m_run[hb] <= kNoMax ? 0.0f : fast_exp2(m_run[hb] - mm_);
         if (f == 0.0f) continue;
 #pragma unroll
         for (int mm = 0; mm < NK; ++mm) {

@@ -12,6 +12,9 @@ namespace oscar {
 constexpr int kPage = 16;
 constexpr int kMaxBf16 = 512;     // sink + recent upper bound
 constexpr float kLog2e = 1.4426950408889634f;
+// The INT2 decode raises its running softmax max only when a logit passes it by more than
+// 2^kSoftmaxHeadroomLog2 (log2 units), so weights stay at or below 2^8 between rescales.
+constexpr int kSoftmaxHeadroomLog2 = 8;
 
 // Per-layer device parameters. All pointers index into one allocation.
 struct LayerParams {
@@ -20,7 +23,7 @@ struct LayerParams {
     const float* r_vt;     // [H_kv][d][d], r_vt[h][i][c] = r_v[h][c][i]
     const float* t_k;      // [H_kv][d]
     const float* t_v;      // [H_kv][d]
-    const float* pv_scale; // [H_kv] 2^sigma with (2/3) max T_v * 2^sigma <= 32752: keeps p * s_v * 2^sigma in fp16
+    const float* pv_scale; // [H_kv] 2^sigma with 2^8 (2/3) max T_v 2^sigma <= 32752: keeps p s_v 2^sigma in fp16
     const uint16_t* r_img; // [K,V][H_kv][3][d*d] bf16 pieces of R as tensor-core operand images
     const float* r_kt;     // [H_kv][d][d], r_kt[h][c][i] = r_k[h][i][c] (exact recompute of the bulk write)
 };
