@@ -179,6 +179,23 @@ __host__ __device__ constexpr uint32_t pack_bias(int kind, int w, int d) {
     return b;
 }
 
+// The packed bit offset of channel 32 ch + j is off(j) + off(32 ch) for both layouts and head
+// sizes, with no carry out of a 32-bit word and a word shift of at most one. So one 32-channel
+// chunk body, with compile-time offsets, serves every chunk.
+__host__ __device__ constexpr bool chunk_additive(int kind, int d) {
+    for (int ch = 0; ch < d / 32; ++ch) {
+        const int delta = bit_offset(kind, 32 * ch, d);
+        if (delta / 32 > 1) return false;
+        for (int j = 0; j < 32; ++j) {
+            const int b = bit_offset(kind, j, d);
+            if (bit_offset(kind, 32 * ch + j, d) != b + delta || b % 32 + delta % 32 >= 32) return false;
+        }
+    }
+    return true;
+}
+static_assert(chunk_additive(0, 64) && chunk_additive(0, 128) && chunk_additive(1, 64) && chunk_additive(1, 128),
+              "packed layout not chunk-additive");
+
 template <int KIND, int D, int W = 0>
 __device__ __forceinline__ void init_words(uint32_t* words) {
     if constexpr (W < D / 16) {
@@ -496,12 +513,12 @@ __device__ __forceinline__ void epilogue_tile(uint32_t tacc, uint32_t acc_empty,
         fs = fixup_detect<D, G>(tacc, t_s, need, err, st, cs);
     }
 
-    // ---- pass 2: codes in fp32, packed in place
+    // ---- pass 2: codes in fp32, packed in place (one chunk body; offsets = off(j) + off(32 ch))
     float inv[NG];
     group_inv<D, G>(mn, mx, inv);
     uint32_t words[D / 16];
     init_words<KIND, D>(words);
-#pragma unroll
+#pragma unroll 1
     for (int ch = 0; ch < NCH; ++ch) {
         float v[32];
         tmem_ld32(tacc + 32 * ch, v);
@@ -510,15 +527,36 @@ __device__ __forceinline__ void epilogue_tile(uint32_t tacc, uint32_t acc_empty,
             tc_fence_before();
             mbar_arrive(acc_empty);
         }
+        float gmn = mn[0], ginv = inv[0];
+#pragma unroll
+        for (int g = 1; g < NG; ++g)
+            if ((32 * ch) / G == g) { gmn = mn[g]; ginv = inv[g]; }
+        uint32_t cw[D / 16];
+#pragma unroll
+        for (int w = 0; w < D / 16; ++w) cw[w] = 0u;
 #pragma unroll
         for (int j = 0; j < 32; j += 4) {
             const float4 t = *reinterpret_cast<const float4*>(t_s + 32 * ch + j);
-            v[j] = fminf(fmaxf(v[j], -t.x), t.x);
-            v[j + 1] = fminf(fmaxf(v[j + 1], -t.y), t.y);
-            v[j + 2] = fminf(fmaxf(v[j + 2], -t.z), t.z);
-            v[j + 3] = fminf(fmaxf(v[j + 3], -t.w), t.w);
+            const float tt[4] = {t.x, t.y, t.z, t.w};
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const float xh = fminf(fmaxf(v[j + k], -tt[k]), tt[k]);
+                // u in [0, 3 + tiny]: adding 1.5 * 2^23 rounds it half-to-even onto the integer grid
+                const float u = __fmul_rn(__fsub_rn(xh, gmn), ginv);
+                const uint32_t bits = __float_as_uint(__fadd_rn(u, 12582912.0f));
+                const int off = bit_offset(KIND, j + k, D);
+                cw[off >> 5] += bits << (off & 31);
+            }
         }
-        pack_chunk<D, G, KIND>(v, ch, mn, inv, words);
+        const int delta = bit_offset(KIND, 32 * ch, D);
+        const int bs = delta & 31;
+        if (delta >> 5) {
+#pragma unroll
+            for (int w = D / 16 - 1; w >= 1; --w) words[w] += cw[w - 1] << bs;
+        } else {
+#pragma unroll
+            for (int w = 0; w < D / 16; ++w) words[w] += cw[w] << bs;
+        }
     }
     if (any_need) {                                 // the accumulator is free again by now
         const GroupStats<NG> st = fixup_exact<D, G>(fs, t_s, tok, head, h_kv, x_base, rt_head, lane);
