@@ -69,7 +69,8 @@ struct TcLayout {
     static constexpr int kOffB = 0;
     static constexpr int kOffA = kOffB + kPieces * kPieceBytes;
     static constexpr int kOffT = kOffA + kStages * kTileBytes;
-    static constexpr int kOffBar = kOffT + 2 * D * 4;          // T_k and T_v of the head
+    // T_k, T_v of the head, then per 32-channel chunk min T_k (at 2D) and min T_v (at 3D)
+    static constexpr int kOffBar = kOffT + 4 * D * 4;
     static constexpr int kBars = 2 * kStages + 2 * kAccs + 1;     // full, empty, acc_full[], acc_empty[], b_full
     static constexpr int kOffMisc = kOffBar + kBars * 8;
     static constexpr int kBytes = kOffMisc + 16;
@@ -89,10 +90,12 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
 __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" :: "r"(bar), "r"(bytes) : "memory");
 }
+// try_wait with a suspend-time hint: the warp sleeps (up to ~0.1 ms) instead of spinning on the
+// issue slots that the other warps of the SM need.
 __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t phase) {
     uint32_t ok;
-    asm volatile("{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
-                 : "=r"(ok) : "r"(bar), "r"(phase) : "memory");
+    asm volatile("{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3; selp.u32 %0, 1, 0, p; }"
+                 : "=r"(ok) : "r"(bar), "r"(phase), "r"(100000u) : "memory");
     return ok != 0;
 }
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t phase) {
@@ -471,7 +474,9 @@ __device__ __forceinline__ void epilogue_tile(uint32_t tacc, uint32_t acc_empty,
         float v[32];
         tmem_ld32(tacc + 32 * ch, v);
         tmem_wait_ld();
-        float cmn = FLT_MAX, cmx = -FLT_MAX;
+        // min_c clip(x_c) = min(min_c max(x_c, -t_c), min_c t_c) and max_c clip(x_c) =
+        // max(max_c min(x_c, t_c), -min_c t_c): one op per element and side instead of a clip
+        float cmn = t_s[2 * D + ch], cmx = -t_s[2 * D + ch];        // min t over the chunk
 #pragma unroll
         for (int j = 0; j < 32; j += 4) {
             const float4 t = *reinterpret_cast<const float4*>(t_s + 32 * ch + j);
@@ -479,10 +484,8 @@ __device__ __forceinline__ void epilogue_tile(uint32_t tacc, uint32_t acc_empty,
             sq1 = fmaf(v[j + 1], v[j + 1], sq1);
             sq0 = fmaf(v[j + 2], v[j + 2], sq0);
             sq1 = fmaf(v[j + 3], v[j + 3], sq1);
-            const float a0 = fminf(fmaxf(v[j], -t.x), t.x), a1 = fminf(fmaxf(v[j + 1], -t.y), t.y);
-            const float a2 = fminf(fmaxf(v[j + 2], -t.z), t.z), a3 = fminf(fmaxf(v[j + 3], -t.w), t.w);
-            cmn = fminf(fminf(cmn, a0), fminf(fminf(a1, a2), a3));
-            cmx = fmaxf(fmaxf(cmx, a0), fmaxf(fmaxf(a1, a2), a3));
+            cmn = fminf(fminf(cmn, fmaxf(v[j], -t.x)), fminf(fmaxf(v[j + 1], -t.y), fminf(fmaxf(v[j + 2], -t.z), fmaxf(v[j + 3], -t.w))));
+            cmx = fmaxf(fmaxf(cmx, fminf(v[j], t.x)), fmaxf(fminf(v[j + 1], t.y), fmaxf(fminf(v[j + 2], t.z), fminf(v[j + 3], t.w))));
         }
         // a 32-channel chunk lies inside one group (G >= 32)
 #pragma unroll
@@ -617,6 +620,13 @@ write_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant
     }
     for (int i = threadIdx.x; i < 2 * D; i += kThreads)
         t_s[i] = t_all[((size_t)(i / D) * h_kv + head) * D + i % D];
+    if (threadIdx.x < 2 * (D / 32)) {
+        const int kd = threadIdx.x / (D / 32), ch = threadIdx.x % (D / 32);
+        const float* t = t_all + ((size_t)kd * h_kv + head) * D + 32 * ch;
+        float m = t[0];
+        for (int j = 1; j < 32; ++j) m = fminf(m, t[j]);
+        t_s[(2 + kd) * D + ch] = m;
+    }
     if (warp == 1) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
                      :: "r"(smem_u32(tmem_slot)), "r"(L::kTmemCols) : "memory");
