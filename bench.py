@@ -121,19 +121,25 @@ def workload_cfg(name):
     return dict(synth.WORKLOADS[name])
 
 
-def algorithmic_bytes(cfg, hist, n_bf16, batch=1):
-    """Decode bytes per layer: packed INT2 codes + fp16 scale/zero + BF16 sink/recent (q, out, tables excluded)."""
-    d, g, h = cfg["d"], cfg["group"], cfg["h_kv"]
-    return batch * (hist * h * 2 * (d // 4 + 4 * (d // g)) + n_bf16 * h * 2 * d * 2)
-
-
 def demote_bytes(cfg, n):
     d, g, h = cfg["d"], cfg["group"], cfg["h_kv"]
     return n * h * 2 * (d * 2 + d // 4 + 4 * (d // g))
 
 
+def token_bytes(cfg, int2_tokens, bf16_tokens):
+    """Decode bytes: packed INT2 codes + fp16 scale/zero per INT2 token, BF16 K/V per BF16 token."""
+    d, g, h = cfg["d"], cfg["group"], cfg["h_kv"]
+    return int2_tokens * h * 2 * (d // 4 + 4 * (d // g)) + bf16_tokens * h * 2 * d * 2
+
+
 class GpuWorkload:
-    """Device-resident caches for every layer, written through the library's own write path."""
+    """Device-resident caches for every layer, written through the library's own write path.
+
+    ``batch`` sequences, each a BF16 sink (64 tokens) + INT2 history + BF16 recent window (256).
+    Mixed-length workloads draw lengths log-uniform and share a prefix: the INT2 pages of the first
+    ``shared_prefix`` tokens and the sink pages are the same physical pages in every table. Every
+    sequence owns one spare INT2 page, outside its history, that receives the per-step demote.
+    Physical INT2 pages are a seeded permutation (non-contiguous tables)."""
 
     def __init__(self, cfg, layers, dev, seed_offset=0):
         import numpy as np
@@ -143,65 +149,107 @@ class GpuWorkload:
 
         self.cfg, self.layers, self.dev = cfg, layers, dev
         d, h_kv, h_q, group = cfg["d"], cfg["h_kv"], cfg["h_q"], cfg["group"]
-        self.hist = cfg["hist"]
-        self.n_bf16 = synth.SINK + synth.RECENT
+        B = cfg.get("batch", 1)
+        sink, recent = synth.SINK, synth.RECENT
+        self.batch, self.n_bf16 = B, sink + recent
+        if "len_lo" in cfg:
+            prefix = cfg["shared_prefix"]
+            _, lengths = synth.mixed_lengths(cfg["seed"], B, cfg["len_lo"], cfg["len_hi"], prefix + self.n_bf16)
+            hist = (lengths - self.n_bf16).astype(np.int64)
+            shared_hist = prefix - sink                      # INT2 tokens of the shared prefix
+        else:
+            hist = np.full(B, cfg["hist"], np.int64)
+            shared_hist = 0
+        assert shared_hist % P == 0
+        self.hist, self.max_hist, self.shared_hist = hist, int(hist.max()), shared_hist
+        shared_pages = shared_hist // P
+        pages = [synth.pages_for(int(x)) for x in hist]
+        unique = [p_ - shared_pages for p_ in pages]
+        total = shared_pages + sum(unique) + B
+        max_pages = max(pages)
         self.ctx = O.Oscar(n_layers=layers, n_q_heads=h_q, n_kv_heads=h_kv, head_dim=d, group=group)
-        self.hist_pages = synth.pages_for(self.hist)
-        self.pool_pages = self.hist_pages + 1                 # + one spare page for the demoted token
-        self.bf16_pages = self.n_bf16 // P
         pb = self.ctx.int2_page_bytes()
+        bf_pages = 4 + (recent // P) * B                     # shared sink pages + recent pages per sequence
         gen = torch.Generator(device=dev)
-        self.int2_pools, self.bf16_pools, self.tables, self.bf16_tables, self.qs = [], [], [], [], []
+        self.int2_pools, self.bf16_pools, self.tables, self.qs = [], [], [], []
         chunk = 16384
         for layer in range(layers):
             li = synth.LayerInputs(cfg, layer + seed_offset)
             q_cal, k_cal, v_cal = li.calibration()
             rk, rv, tk, tv = calibration.calibrate_layer(q_cal, k_cal, v_cal, d ** -0.5, cfg["clip_ratio"])
             self.ctx.calibrate_upload(layer, rk, rv, tk, tv)
-            perm = synth.page_permutation(li.seed, "int2", self.hist_pages)
-            table = torch.from_numpy(np.append(perm, self.hist_pages).astype(np.int32)).to(dev).view(1, -1)
-            pool = torch.zeros(self.pool_pages * pb, dtype=torch.uint8, device=dev)
+            perm = synth.page_permutation(li.seed, "int2", total).astype(np.int64)
+            table = np.zeros((B, max_pages), np.int32)
+            spare = np.zeros(B, np.int64)
+            o = shared_pages
+            for i in range(B):
+                table[i, :shared_pages] = perm[:shared_pages]
+                table[i, shared_pages:pages[i]] = perm[o:o + unique[i]]
+                o += unique[i]
+            spare[:] = perm[o:o + B]
+            table_d = torch.from_numpy(table).to(dev)
+            pool = torch.zeros(total * pb, dtype=torch.uint8, device=dev)
             gen.manual_seed(li.seed)
             km = torch.from_numpy(li.k_prof.mult).to(dev)
             vm = torch.from_numpy(li.v_prof.mult).to(dev)
-            for t0 in range(0, self.hist, chunk):
-                n = min(chunk, self.hist - t0)
-                k = (torch.randn(n, h_kv, d, generator=gen, device=dev) * km).to(torch.bfloat16)
-                v = (torch.randn(n, h_kv, d, generator=gen, device=dev) * vm).to(torch.bfloat16)
-                t = torch.arange(t0, t0 + n, device=dev)
-                slots = table[0, t // P].to(torch.int64) * P + t % P
-                self.ctx.write_tokens(layer, k, v, slots, pool)
-            bf = torch.randn(self.bf16_pages, h_kv, 2, P, d, generator=gen, device=dev)
+            # token ranges written: the shared prefix once (through sequence 0's table), then each
+            # sequence's own history
+            ranges = [(0, 0, shared_hist)] + [(i, shared_hist, int(hist[i])) for i in range(B)]
+            for i, t_lo, t_hi in ranges:
+                for t0 in range(t_lo, t_hi, chunk):
+                    n = min(chunk, t_hi - t0)
+                    k = (torch.randn(n, h_kv, d, generator=gen, device=dev) * km).to(torch.bfloat16)
+                    v = (torch.randn(n, h_kv, d, generator=gen, device=dev) * vm).to(torch.bfloat16)
+                    t = torch.arange(t0, t0 + n, device=dev)
+                    slots = table_d[i, t // P].to(torch.int64) * P + t % P
+                    self.ctx.write_tokens(layer, k, v, slots, pool)
+            bf = torch.randn(bf_pages, h_kv, 2, P, d, generator=gen, device=dev)
             bf = bf * torch.stack([km, vm], dim=1)[None, :, :, None, :]
             self.bf16_pools.append(bf.to(torch.bfloat16).contiguous())
-            self.bf16_tables.append(torch.arange(self.bf16_pages, dtype=torch.int32, device=dev).view(1, -1))
             self.int2_pools.append(pool)
-            self.tables.append(table)
-            self.qs.append(torch.randn(1, h_q, d, generator=gen, device=dev).to(torch.bfloat16))
-        self.hist_len = torch.tensor([self.hist], dtype=torch.int32, device=dev)
-        self.bf16_len = torch.tensor([self.n_bf16], dtype=torch.int32, device=dev)
-        self.src = torch.tensor([synth.SINK * 1], dtype=torch.int64, device=dev)          # oldest recent token
-        self.dst = torch.tensor([self.hist_pages * P], dtype=torch.int64, device=dev)     # spare INT2 slot
-        self.ws = torch.empty(self.ctx.decode_workspace_size(1, self.hist), dtype=torch.uint8, device=dev)
-        self.out = torch.empty(layers, 1, h_q, d, dtype=torch.float32, device=dev)
-        self.q_all = torch.cat(self.qs, 0).view(layers, 1, h_q, d).contiguous()
+            self.tables.append(table_d)
+            self.qs.append(torch.randn(B, h_q, d, generator=gen, device=dev).to(torch.bfloat16))
+        bt = np.zeros((B, self.n_bf16 // P), np.int32)
+        for i in range(B):
+            bt[i, :4] = np.arange(4)
+            bt[i, 4:] = 4 + (recent // P) * i + np.arange(recent // P)
+        self.bf16_table = torch.from_numpy(bt).to(dev)
+        self.hist_len = torch.from_numpy(hist.astype(np.int32)).to(dev)
+        self.bf16_len = torch.full((B,), self.n_bf16, dtype=torch.int32, device=dev)
+        # demote: each sequence's oldest recent token (row 0 of its first recent page) -> row 0 of
+        # its spare INT2 page (same spare page ids in every layer's pool: the permutation per layer
+        # differs, so the spare ids are taken per layer below)
+        self.src = torch.from_numpy((bt[:, 4].astype(np.int64)) * P).to(dev)
+        self.dsts = []
+        for layer in range(layers):
+            li = synth.LayerInputs(cfg, layer + seed_offset)
+            perm = synth.page_permutation(li.seed, "int2", total).astype(np.int64)
+            self.dsts.append(torch.from_numpy(perm[total - B:] * P).to(dev))
+        self.ws = torch.empty(self.ctx.decode_workspace_size(B, self.max_hist), dtype=torch.uint8, device=dev)
+        self.out = torch.empty(layers, B, h_q, d, dtype=torch.float32, device=dev)
+        self.q_all = torch.stack(self.qs, 0).contiguous()
         self.side = torch.cuda.Stream(device=dev)
         self.demoted = [torch.cuda.Event() for _ in range(layers)]
+        # bytes and tokens of one decode of one layer
+        self.tokens_per_layer = int(hist.sum()) + B * self.n_bf16
+        self.logical_bytes = token_bytes(cfg, int(hist.sum()), B * self.n_bf16)
+        self.unique_bytes = token_bytes(cfg, shared_hist + int((hist - shared_hist).sum()), sink + B * recent)
         torch.cuda.synchronize()
 
     def step(self):
-        """Per layer: demote the oldest recent token, then decode. The demotes run on a side stream
-        (they depend on nothing the decodes produce); decode(layer) waits for demote(layer)."""
+        """Per layer: demote the oldest recent token of every sequence, then decode. The demotes run
+        on a side stream (they depend on nothing the decodes produce); decode(layer) waits for
+        demote(layer)."""
         import torch
         main = torch.cuda.current_stream()
         self.side.wait_stream(main)
         for layer in range(self.layers):
             with torch.cuda.stream(self.side):
-                self.ctx.demote_recent(layer, self.bf16_pools[layer], self.src, self.int2_pools[layer], self.dst)
+                self.ctx.demote_recent(layer, self.bf16_pools[layer], self.src, self.int2_pools[layer], self.dsts[layer])
                 self.demoted[layer].record(self.side)
             main.wait_event(self.demoted[layer])
             self.ctx.decode(layer, self.q_all[layer], self.int2_pools[layer], self.tables[layer], self.hist_len,
-                            self.hist, self.bf16_pools[layer], self.bf16_tables[layer], self.bf16_len,
+                            self.max_hist, self.bf16_pools[layer], self.bf16_table, self.bf16_len,
                             self.out[layer], self.ws)
         main.wait_stream(self.side)
 
@@ -353,7 +401,7 @@ def run_reference(args, cfg, world, rank):
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": args.workload, "batch": 1, "context": cfg["hist"] + 320,
+            "config": {"workload": args.workload, "batch": 1, "context": cfg.get("hist", sample_hist) + 320,
                        "note": "each step is a bounded sample of the workload"},
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle", "sample": sample},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -426,10 +474,10 @@ def main():
         barrier()
     sec = start.elapsed_time(stop) / 1e3
     max_sec = max_over_ranks(sec, dev)
-    tokens_per_step = layers * (wl.hist + wl.n_bf16)
+    tokens_per_step = layers * wl.tokens_per_layer
     value = whole_job_rate(tokens_per_step * args.steps, world, max_sec)
     ms_per_step = 1e3 * max_sec / args.steps
-    step_bytes = layers * (algorithmic_bytes(cfg, wl.hist, wl.n_bf16) + demote_bytes(cfg, 1))
+    step_bytes = layers * (wl.unique_bytes + demote_bytes(cfg, wl.batch))
 
     # ---- per-kernel durations (same launches, eager, events around each kernel on its stream)
     wl.ctx.profile_enable(True)
@@ -442,7 +490,8 @@ def main():
                       ("split", O.OSCAR_KERNEL_SPLIT), ("merge", O.OSCAR_KERNEL_MERGE)):
         ms, n = wl.ctx.profile_read(kid)
         kt[name] = {"launches": n, "avg_us": 1e3 * ms / max(n, 1)}
-    split_bytes = algorithmic_bytes(cfg, wl.hist, wl.n_bf16)
+    # roofline on unique bytes (a page shared by several tables counts once: conservative)
+    split_bytes = wl.unique_bytes
     achieved = split_bytes / (kt["split"]["avg_us"] * 1e-6) / 1e9
     peak, peak_kind = measured_peak()
 
@@ -486,10 +535,15 @@ def main():
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-            "config": {"workload": args.workload, "batch": 1, "context": wl.hist + wl.n_bf16, "int2_history": wl.hist,
+            "config": {"workload": args.workload, "batch": wl.batch,
+                       "context": int(wl.hist[0]) + wl.n_bf16 if wl.batch == 1 else "per sequence, see int2_history",
+                       "int2_history": int(wl.hist[0]) if wl.batch == 1 else
+                       {"min": int(wl.hist.min()), "max": int(wl.hist.max()), "sum": int(wl.hist.sum())},
+                       "shared_prefix_int2_tokens": wl.shared_hist,
                        "bf16_tokens": wl.n_bf16, "layers": layers, "h_q": cfg["h_q"], "h_kv": cfg["h_kv"],
                        "head_dim": cfg["d"], "group": cfg["group"], "page_size": P,
-                       "step": "per layer: demote 1 token (side stream) + decode after it; one CUDA graph per step",
+                       "step": "per layer: demote 1 token per sequence (side stream) + decode after it; "
+                               "one CUDA graph per step",
                        "l2": "inputs larger than L2: %.2f GB of distinct pages per step" % (step_bytes / 1e9),
                        "parallelism": "replicas" if world > 1 else "single GPU"},
             "hbm_gbs_step": step_bytes * args.steps * world / max_sec / 1e9,
@@ -497,7 +551,8 @@ def main():
             "roofline": {"bound": "hbm", "kernel": "split (INT2 history + BF16 segment)", "achieved": achieved,
                          "peak": peak, "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / peak,
                          "traffic": kernel_traffic("split", args.workload),
-                         "algorithmic_bytes_per_launch": split_bytes},
+                         "algorithmic_bytes_per_launch": split_bytes,
+                         "logical_bytes_per_launch": wl.logical_bytes},
             "kernels": kt,
             "clocks": clocks.summary(),
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": q_host.numel() * 2,

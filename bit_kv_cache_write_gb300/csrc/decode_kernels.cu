@@ -51,6 +51,7 @@ constexpr int kWarps = 4;
 constexpr int kStages = 4;
 constexpr long long kWaitCycles = 2000000000LL;   // give up on a page copy after ~1 s
 constexpr float kNoMax = -1e30f;                   // running max before any token
+constexpr int kMaxPagesPerSplit = 128;             // longest INT2 split when the grid has many waves
 
 __device__ __forceinline__ float fast_exp2(float x) { return exp2f(x); }
 
@@ -994,10 +995,14 @@ DecodePlan plan_decode(const Shape& s, int num_sms, int batch, int max_hist) {
     DecodePlan p{};
     const int max_pages = (max_hist + kPage - 1) / kPage;
     const int units = batch * s.h_kv;
-    // one wave: units * (INT2 splits + 1 BF16 split) resident CTAs
+    // one wave of units * (INT2 splits + 1 BF16 split) resident CTAs when that keeps splits short
+    // (few units: bs1 decode); otherwise at most kMaxPagesPerSplit pages per split, in as many
+    // waves as that takes (many units or long sequences)
     const int slots = split_ctas_per_sm(s) * num_sms;
     int splits = units > 0 ? slots / units - 1 : 1;
     if (splits < 1) splits = 1;
+    const int by_len = (max_pages + kMaxPagesPerSplit - 1) / kMaxPagesPerSplit;
+    if (splits < by_len) splits = by_len;
     if (max_pages > 0 && splits > max_pages) splits = max_pages;
     if (max_pages == 0) splits = 1;
     p.pages_per_split = max_pages > 0 ? (max_pages + splits - 1) / splits : 1;
