@@ -52,6 +52,9 @@ constexpr int kStages = 4;
 constexpr long long kWaitCycles = 2000000000LL;   // give up on a page copy after ~1 s
 constexpr float kNoMax = -1e30f;                   // running max before any token
 constexpr int kMaxPagesPerSplit = 128;             // longest INT2 split when the grid has many waves
+// last-CTA merge only for short merges (one CTA walks GQ * splits partial rows): large batches;
+// bs1 decodes with ~80 splits keep the wider merge kernel
+constexpr size_t kFuseWeights = 128;
 
 __device__ __forceinline__ float fast_exp2(float x) { return exp2f(x); }
 
@@ -158,7 +161,7 @@ template <int D, int G>
 __global__ void __launch_bounds__(4 * D)
 q_prep_kernel(const __nv_bfloat16* __restrict__ q, const float* __restrict__ r_k,
               __half* __restrict__ qb, float* __restrict__ kap, float* __restrict__ qsum, int h_q, int g,
-              float sl2_hi, float sl2_lo) {
+              float sl2_hi, float sl2_lo, int* __restrict__ counters) {
     constexpr int NG = D / G;
     constexpr int Q4 = D / 4;                      // terms per thread: four threads per output channel
     __shared__ float qs[D];
@@ -170,6 +173,8 @@ q_prep_kernel(const __nv_bfloat16* __restrict__ q, const float* __restrict__ r_k
     const int c = threadIdx.x % D, quarter = threadIdx.x / D;
     pdl_wait();
     pdl_trigger();
+    // the split kernel's ticket counter of this (sequence, KV head) starts at zero
+    if (threadIdx.x == 0 && (bh % h_q) % g == 0) counters[(bh / h_q) * (h_q / g) + kv] = 0;
     if (threadIdx.x < D) qs[c] = __bfloat162float(q[(size_t)bh * D + c]);
     __syncthreads();
     const float* r = r_k + (size_t)kv * D * D + (size_t)quarter * Q4 * D + c;
@@ -272,6 +277,11 @@ struct SplitArgs {
     int h_kv, int2_splits, pages_per_split, bf16_splits, bf16_pages_per_split, total_splits;
     float scale_log2, scale_log2_lo;   // sm_scale * log2(e) as hi + lo
     int debug; DebugWord* dbg;
+    // last-CTA merge: the CTA that finishes a (sequence, KV head) last reduces its partials
+    int fuse_merge;
+    int* counters;                // [B][H_kv] tickets, zeroed by q_prep
+    const float* r_vt;            // [H_kv][D][D]
+    float* out;                   // [B][H_q][D]
 };
 
 template <int D, int G, int GQ>
@@ -808,6 +818,69 @@ __device__ void bf16_split(const SplitArgs& a, int split, int kv, int b, float* 
     }
 }
 
+// Online-softmax merge of one (sequence, KV head)'s splits, run by the CTA that finishes last:
+// per query head, weights 2^(m_s - M) over the split partials, the INT2 splits' sum un-rotated by
+// R_v^T, plus the BF16 split, over L. w_s holds GQ * total_splits floats.
+template <int D, int GQ>
+__device__ __noinline__ void merge_group(const SplitArgs& a, int kv, int b, float* acc_s, float* w_s) {
+    __shared__ float l_s[GQ];
+    const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
+    const int h_q = a.h_kv * GQ, T = a.total_splits;
+    const float* part0 = a.partials + (size_t)(b * h_q + kv * GQ) * T * (D + 2);
+    for (int h = warp; h < GQ; h += kWarps) {
+        const float* part = part0 + (size_t)h * T * (D + 2);
+        float m = -INFINITY;
+        for (int sp = lane; sp < T; sp += 32) m = fmaxf(m, part[(size_t)sp * (D + 2)]);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+        float l = 0.0f;
+        for (int sp = lane; sp < T; sp += 32) {
+            const float ms = part[(size_t)sp * (D + 2)];
+            const float w = (m == -INFINITY || ms == -INFINITY) ? 0.0f : fast_exp2(ms - m);
+            w_s[h * T + sp] = w;
+            l = fmaf(part[(size_t)sp * (D + 2) + 1], w, l);
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
+        if (lane == 0) l_s[h] = l;
+    }
+    __syncthreads();
+    const int c = tid;
+    float ab[GQ];
+#pragma unroll
+    for (int h = 0; h < GQ; ++h) {
+        float ai = 0.0f;
+        ab[h] = 0.0f;
+        if (c < D) {
+            const float* part = part0 + (size_t)h * T * (D + 2) + 2 + c;
+#pragma unroll 8
+            for (int sp = 0; sp < T; ++sp) {
+                const float v = part[(size_t)sp * (D + 2)] * w_s[h * T + sp];
+                if (sp < a.int2_splits) ai += v; else ab[h] += v;
+            }
+            acc_s[h * D + c] = ai;
+        }
+    }
+    __syncthreads();
+    if (c < D) {
+        float o[GQ];
+#pragma unroll
+        for (int h = 0; h < GQ; ++h) o[h] = 0.0f;
+        const float* rt = a.r_vt + (size_t)kv * D * D + c;
+#pragma unroll 4
+        for (int i = 0; i < D; ++i) {
+            const float r = __ldg(rt + (size_t)i * D);
+#pragma unroll
+            for (int h = 0; h < GQ; ++h) o[h] = fmaf(acc_s[h * D + i], r, o[h]);
+        }
+#pragma unroll
+        for (int h = 0; h < GQ; ++h) {
+            const float L = l_s[h];
+            a.out[((size_t)b * h_q + kv * GQ + h) * D + c] = L > 0.0f ? (o[h] + ab[h]) / L : 0.0f;
+        }
+    }
+}
+
 template <int D, int G, int GQ>
 __global__ void __launch_bounds__(kWarps * 32, GQ == 8 ? 2 : 4)
 split_kernel(SplitArgs a) {
@@ -843,6 +916,20 @@ split_kernel(SplitArgs a) {
         float* dst = a.partials + (((size_t)b * h_q + kv * GQ + h) * a.total_splits + split) * (D + 2);
         for (int c = threadIdx.x; c < D; c += blockDim.x) dst[2 + c] = acc_s[h * D + c];
         if (threadIdx.x == 0) { dst[0] = mm; dst[1] = ll; }
+    }
+    if (a.fuse_merge) {
+        // the last CTA of this (sequence, KV head) to finish merges all of its splits
+        __shared__ int ticket_s;
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            __threadfence();
+            ticket_s = atomicAdd(a.counters + (size_t)b * a.h_kv + kv, 1);
+        }
+        __syncthreads();
+        if (ticket_s == a.total_splits - 1) {
+            __threadfence();
+            merge_group<D, GQ>(a, kv, b, acc_s, reinterpret_cast<float*>(dyn_smem));
+        }
     }
 }
 
@@ -1012,7 +1099,10 @@ DecodePlan plan_decode(const Shape& s, int num_sms, int batch, int max_hist) {
     p.ws_partials = align256((size_t)batch * s.h_q * p.total_splits * (s.d + 2) * sizeof(float));
     p.ws_qrot = align256((size_t)batch * s.h_q * (3 * s.d * sizeof(__half) + sizeof(float) +
                                                  2 * (s.d / s.group) * sizeof(float)) + 256);
-    p.ws_total = p.ws_partials + p.ws_qrot;
+    p.ws_counters = align256((size_t)batch * s.h_kv * sizeof(int));
+    p.ws_total = p.ws_partials + p.ws_qrot + p.ws_counters;
+    // the last-CTA merge keeps its weights in the page-stage shared memory (at least 12 KB)
+    p.fuse_merge = (size_t)(s.h_q / s.h_kv) * p.total_splits <= kFuseWeights;
     return p;
 }
 
@@ -1025,6 +1115,7 @@ cudaError_t launch_decode(const Shape& s, const LayerParams& prm, const DecodePl
     __half* qb = reinterpret_cast<__half*>(qbase);
     float* kap = reinterpret_cast<float*>(qbase + align256(nh * 3 * s.d * sizeof(__half)));
     float* qsum = kap + nh;
+    int* counters = reinterpret_cast<int*>(static_cast<char*>(a.ws) + plan.ws_partials + plan.ws_qrot);
     const __nv_bfloat16* q = static_cast<const __nv_bfloat16*>(a.q);
 
     const double sl2d = s.sm_scale * 1.4426950408889634073599;     // sm_scale * log2(e)
@@ -1034,7 +1125,7 @@ cudaError_t launch_decode(const Shape& s, const LayerParams& prm, const DecodePl
         ProfScope ps(prof, OSCAR_KERNEL_QROT, st);
 #define OSCAR_QPREP_CASE(D_, G_) \
         if (s.d == D_ && s.group == G_) \
-            e = launch_pdl(q_prep_kernel<D_, G_>, dim3(a.batch * s.h_q), dim3(4 * D_), 0, st, q, prm.r_k, qb, kap, qsum, s.h_q, g, sl2_hi, sl2_lo);
+            e = launch_pdl(q_prep_kernel<D_, G_>, dim3(a.batch * s.h_q), dim3(4 * D_), 0, st, q, prm.r_k, qb, kap, qsum, s.h_q, g, sl2_hi, sl2_lo, counters);
         OSCAR_QPREP_CASE(64, 32)
         OSCAR_QPREP_CASE(64, 64)
         OSCAR_QPREP_CASE(128, 32)
@@ -1060,6 +1151,10 @@ cudaError_t launch_decode(const Shape& s, const LayerParams& prm, const DecodePl
     sa.scale_log2 = sl2_hi;
     sa.scale_log2_lo = sl2_lo;
     sa.debug = s.debug; sa.dbg = dbg;
+    sa.fuse_merge = plan.fuse_merge ? 1 : 0;
+    sa.counters = counters;
+    sa.r_vt = prm.r_vt;
+    sa.out = a.out;
 
     ProfScope ps_split(prof, OSCAR_KERNEL_SPLIT, st);
 #define OSCAR_SPLIT_CASE(D_, G_) \
@@ -1073,6 +1168,7 @@ cudaError_t launch_decode(const Shape& s, const LayerParams& prm, const DecodePl
 #undef OSCAR_SPLIT_CASE
     ps_split.stop();
     if (e != cudaSuccess) return e;
+    if (plan.fuse_merge) return cudaSuccess;           // merged by the last CTA of each unit
 
     ProfScope ps_merge(prof, OSCAR_KERNEL_MERGE, st);
     const size_t msmem = (size_t)plan.total_splits * sizeof(float);

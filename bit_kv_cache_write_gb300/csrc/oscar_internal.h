@@ -124,6 +124,8 @@ struct DecodePlan {
     int total_splits;
     size_t ws_partials;     // bytes of split partials
     size_t ws_qrot;         // bytes of rotated queries
+    size_t ws_counters;     // bytes of per-(sequence, KV head) tickets of the last-CTA merge
+    bool fuse_merge;        // the split kernel merges (else the merge kernel runs)
     size_t ws_total;
 };
 
