@@ -882,7 +882,7 @@ __device__ __noinline__ void merge_group(const SplitArgs& a, int kv, int b, floa
 }
 
 template <int D, int G, int GQ>
-__global__ void __launch_bounds__(kWarps * 32, GQ == 8 ? 2 : 4)
+__global__ void __launch_bounds__(kWarps * 32, GQ == 8 ? 3 : 4)
 split_kernel(SplitArgs a) {
     extern __shared__ __align__(128) uint8_t dyn_smem[];
     __shared__ __align__(8) uint64_t bars[kWarps * kStages];
