@@ -224,18 +224,30 @@ __device__ __forceinline__ void pack_chunk(const float (&v)[32], int ch, const f
 }
 
 template <int D, int G>
-__device__ __forceinline__ void store_row(const uint32_t* words, const float* mn, const float* mx, int64_t slot,
-                                          int head, int h_kv, int kind, uint8_t* __restrict__ int2_pool) {
+__device__ __forceinline__ uint8_t* row_segment(int64_t slot, int head, int h_kv, int kind, uint8_t* __restrict__ int2_pool) {
     using GE = Geo<D, G>;
-    constexpr int NG = D / G;
     const int64_t pg = slot / kPage;
-    uint8_t* seg = int2_pool + ((size_t)pg * h_kv + head) * GE::kBlock + (size_t)kind * GE::kSeg;
-    const int row = (int)(slot % kPage);
-    uint32_t* dst = reinterpret_cast<uint32_t*>(seg + row * GE::kCodeRow);
+    return int2_pool + ((size_t)pg * h_kv + head) * GE::kBlock + (size_t)kind * GE::kSeg;
+}
+
+template <int D, int G>
+__device__ __forceinline__ void store_codes(const uint32_t* words, int64_t slot, int head, int h_kv, int kind,
+                                            uint8_t* __restrict__ int2_pool) {
+    using GE = Geo<D, G>;
+    uint32_t* dst = reinterpret_cast<uint32_t*>(row_segment<D, G>(slot, head, h_kv, kind, int2_pool) +
+                                                (int)(slot % kPage) * GE::kCodeRow);
 #pragma unroll
     for (int w = 0; w < D / 16; w += 4)
         *reinterpret_cast<uint4*>(dst + w) = make_uint4(words[w], words[w + 1], words[w + 2], words[w + 3]);
-    __half2* szd = reinterpret_cast<__half2*>(seg + GE::kCodeBytes) + row * NG;
+}
+
+template <int D, int G>
+__device__ __forceinline__ void store_sz(const float* mn, const float* mx, int64_t slot, int head, int h_kv, int kind,
+                                         uint8_t* __restrict__ int2_pool) {
+    using GE = Geo<D, G>;
+    constexpr int NG = D / G;
+    __half2* szd = reinterpret_cast<__half2*>(row_segment<D, G>(slot, head, h_kv, kind, int2_pool) + GE::kCodeBytes) +
+                   (int)(slot % kPage) * NG;
 #pragma unroll
     for (int g = 0; g < NG; ++g)
         szd[g] = __halves2half2(__float2half_rn(__fdiv_rn(__fsub_rn(mx[g], mn[g]), 3.0f)), __float2half_rn(mn[g]));
@@ -369,15 +381,23 @@ __device__ __noinline__ GroupStats<D / G> fixup_exact(FixState<D / G, D / 32> fs
     for (;;) {
         int s_src[B], s_c[B];
         float rv[B][PER], xv[B][PER];
+        bool left = true;                           // warp-uniform: some lane still has candidates
 #pragma unroll
         for (int k = 0; k < B; ++k) {
+            s_src[k] = -1;
+            s_c[k] = 0;
+            if (!left) continue;
             bool mine = false;
 #pragma unroll
             for (int ch = 0; ch < NCH; ++ch) mine |= fs.cand[ch] != 0u;
             const uint32_t has = __ballot_sync(0xffffffffu, mine);
-            s_src[k] = has ? __ffs(has) - 1 : -1;
+            if (!has) {
+                left = false;
+                continue;
+            }
+            s_src[k] = __ffs(has) - 1;
             int myc = 0;
-            if (has && lane == s_src[k]) {
+            if (lane == s_src[k]) {
                 bool done = false;
 #pragma unroll
                 for (int ch = 0; ch < NCH; ++ch)
@@ -387,31 +407,27 @@ __device__ __noinline__ GroupStats<D / G> fixup_exact(FixState<D / G, D / 32> fs
                         done = true;
                     }
             }
-            s_c[k] = __shfl_sync(0xffffffffu, myc, has ? s_src[k] : 0);
-            const int st_tok = __shfl_sync(0xffffffffu, tok, has ? s_src[k] : 0);
-            if (has) {
-                const float* rr = rt_head + (size_t)s_c[k] * D + PER * lane;
-                const __nv_bfloat16* xr = x_base + ((size_t)st_tok * h_kv + head) * D + PER * lane;
-                if constexpr (PER == 4) {
-                    const float4 r4 = *reinterpret_cast<const float4*>(rr);
-                    const uint2 xb = *reinterpret_cast<const uint2*>(xr);
-                    rv[k][0] = r4.x; rv[k][1] = r4.y; rv[k][2] = r4.z; rv[k][3] = r4.w;
-                    xv[k][0] = __uint_as_float(xb.x << 16); xv[k][1] = __uint_as_float(xb.x & 0xFFFF0000u);
-                    xv[k][2] = __uint_as_float(xb.y << 16); xv[k][3] = __uint_as_float(xb.y & 0xFFFF0000u);
-                } else {
-                    const float2 r2 = *reinterpret_cast<const float2*>(rr);
-                    const uint32_t xb = *reinterpret_cast<const uint32_t*>(xr);
-                    rv[k][0] = r2.x; rv[k][1] = r2.y;
-                    xv[k][0] = __uint_as_float(xb << 16); xv[k][1] = __uint_as_float(xb & 0xFFFF0000u);
-                }
+            s_c[k] = __shfl_sync(0xffffffffu, myc, s_src[k]);
+            const int st_tok = __shfl_sync(0xffffffffu, tok, s_src[k]);
+            const float* rr = rt_head + (size_t)s_c[k] * D + PER * lane;
+            const __nv_bfloat16* xr = x_base + ((size_t)st_tok * h_kv + head) * D + PER * lane;
+            if constexpr (PER == 4) {
+                const float4 r4 = *reinterpret_cast<const float4*>(rr);
+                const uint2 xb = *reinterpret_cast<const uint2*>(xr);
+                rv[k][0] = r4.x; rv[k][1] = r4.y; rv[k][2] = r4.z; rv[k][3] = r4.w;
+                xv[k][0] = __uint_as_float(xb.x << 16); xv[k][1] = __uint_as_float(xb.x & 0xFFFF0000u);
+                xv[k][2] = __uint_as_float(xb.y << 16); xv[k][3] = __uint_as_float(xb.y & 0xFFFF0000u);
             } else {
-#pragma unroll
-                for (int j = 0; j < PER; ++j) { rv[k][j] = 0.0f; xv[k][j] = 0.0f; }
+                const float2 r2 = *reinterpret_cast<const float2*>(rr);
+                const uint32_t xb = *reinterpret_cast<const uint32_t*>(xr);
+                rv[k][0] = r2.x; rv[k][1] = r2.y;
+                xv[k][0] = __uint_as_float(xb << 16); xv[k][1] = __uint_as_float(xb & 0xFFFF0000u);
             }
         }
         if (s_src[0] < 0) break;
 #pragma unroll
         for (int k = 0; k < B; ++k) {
+            if (s_src[k] < 0) break;                // slots fill in order: the rest are empty
             float hi = 0.0f, lo = 0.0f;
 #pragma unroll
             for (int j = 0; j < PER; ++j) {
@@ -505,16 +521,6 @@ __device__ __forceinline__ void epilogue_tile(uint32_t tacc, uint32_t acc_empty,
 #pragma unroll
     for (int g = 0; g < NG; ++g) { mn_sz[g] = mn[g]; mx_sz[g] = mx[g]; }
     const bool any_need = __any_sync(0xffffffffu, need);
-    FixState<NG, NCH> fs;
-    if (any_need) {
-        GroupStats<NG> st;
-#pragma unroll
-        for (int g = 0; g < NG; ++g) { st.mn[g] = mn[g]; st.mx[g] = mx[g]; }
-        ChunkStats<NCH> cs;
-#pragma unroll
-        for (int k = 0; k < NCH; ++k) { cs.mn[k] = chmn[k]; cs.mx[k] = chmx[k]; }
-        fs = fixup_detect<D, G>(tacc, t_s, need, err, st, cs);
-    }
 
     // ---- pass 2: codes in fp32, packed in place (one chunk body; offsets = off(j) + off(32 ch))
     float inv[NG];
@@ -526,7 +532,7 @@ __device__ __forceinline__ void epilogue_tile(uint32_t tacc, uint32_t acc_empty,
         float v[32];
         tmem_ld32(tacc + 32 * ch, v);
         tmem_wait_ld();
-        if (ch == NCH - 1) {
+        if (ch == NCH - 1 && !any_need) {          // else held until the candidates are marked
             tc_fence_before();
             mbar_arrive(acc_empty);
         }
@@ -561,14 +567,26 @@ __device__ __forceinline__ void epilogue_tile(uint32_t tacc, uint32_t acc_empty,
             for (int w = 0; w < D / 16; ++w) words[w] += cw[w] << bs;
         }
     }
-    if (any_need) {                                 // the accumulator is free again by now
-        const GroupStats<NG> st = fixup_exact<D, G>(fs, t_s, tok, head, h_kv, x_base, rt_head, lane);
+    // the codes are final (they use the tensor-core stats): store them now, so that only a few
+    // registers stay live through the rare path below
+    if (ok) store_codes<D, G>(words, slot, head, h_kv, KIND, int2_pool);
+    if (any_need) {
+        GroupStats<NG> st;
+#pragma unroll
+        for (int g = 0; g < NG; ++g) { st.mn[g] = mn[g]; st.mx[g] = mx[g]; }
+        ChunkStats<NCH> cs;
+#pragma unroll
+        for (int k = 0; k < NCH; ++k) { cs.mn[k] = chmn[k]; cs.mx[k] = chmx[k]; }
+        const FixState<NG, NCH> fs = fixup_detect<D, G>(tacc, t_s, need, err, st, cs);
+        tc_fence_before();
+        mbar_arrive(acc_empty);
+        const GroupStats<NG> ex = fixup_exact<D, G>(fs, t_s, tok, head, h_kv, x_base, rt_head, lane);
         if (need) {
 #pragma unroll
-            for (int g = 0; g < NG; ++g) { mn_sz[g] = st.mn[g]; mx_sz[g] = st.mx[g]; }
+            for (int g = 0; g < NG; ++g) { mn_sz[g] = ex.mn[g]; mx_sz[g] = ex.mx[g]; }
         }
     }
-    if (ok) store_row<D, G>(words, mn_sz, mx_sz, slot, head, h_kv, KIND, int2_pool);
+    if (ok) store_sz<D, G>(mn_sz, mx_sz, slot, head, h_kv, KIND, int2_pool);
 }
 
 template <int D, int G>
