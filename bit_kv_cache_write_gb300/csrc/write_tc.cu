@@ -306,7 +306,7 @@ struct FixState {
 // a group's min (max) as a candidate and takes the group stats over the other channels. Only
 // 32-channel chunks whose min (max) comes near the cut are reread.
 template <int D, int G>
-__device__ __noinline__ FixState<D / G, D / 32> fixup_detect(uint32_t tacc, const float* __restrict__ t_s,
+__device__ __forceinline__ FixState<D / G, D / 32> fixup_detect(uint32_t tacc, const float* __restrict__ t_s,
                                                               bool need, float err, GroupStats<D / G> st,
                                                               ChunkStats<D / 32> cs) {
     constexpr int NG = D / G;
@@ -370,7 +370,7 @@ __device__ __noinline__ FixState<D / G, D / 32> fixup_detect(uint32_t tacc, cons
 // at a time with their loads issued together; returns the repaired stats of this row's groups.
 // (The codes of these channels are 0 near the min and 3 near the max either way.)
 template <int D, int G>
-__device__ __noinline__ GroupStats<D / G> fixup_exact(FixState<D / G, D / 32> fs, const float* __restrict__ t_s,
+__device__ __forceinline__ GroupStats<D / G> fixup_exact(FixState<D / G, D / 32> fs, const float* __restrict__ t_s,
                                                        int tok, int head, int h_kv,
                                                        const __nv_bfloat16* __restrict__ x_base,
                                                        const float* __restrict__ rt_head, int lane) {
@@ -469,6 +469,19 @@ __device__ __noinline__ GroupStats<D / G> fixup_exact(FixState<D / G, D / 32> fs
 // over 32-column chunks (clip + group stats, then codes) keep few values live. Rows past n or with
 // a bad slot (ok false) take part in the warp-wide steps but store nothing. Arrives on acc_empty
 // once the accumulator has been read for the last time.
+// The rare path as one out-of-line call (the fast path keeps its registers): marks the candidates
+// while the accumulator is still held, releases it, then recomputes the candidates exactly.
+template <int D, int G>
+__device__ __noinline__ GroupStats<D / G> fixup(uint32_t tacc, uint32_t acc_empty, const float* __restrict__ t_s,
+                                                 bool need, float err, GroupStats<D / G> st, ChunkStats<D / 32> cs,
+                                                 int tok, int head, int h_kv, const __nv_bfloat16* __restrict__ x_base,
+                                                 const float* __restrict__ rt_head, int lane) {
+    const FixState<D / G, D / 32> fs = fixup_detect<D, G>(tacc, t_s, need, err, st, cs);
+    tc_fence_before();
+    mbar_arrive(acc_empty);
+    return fixup_exact<D, G>(fs, t_s, tok, head, h_kv, x_base, rt_head, lane);
+}
+
 template <int D, int G, int KIND>
 __device__ __forceinline__ void epilogue_tile(uint32_t tacc, uint32_t acc_empty, const float* __restrict__ t_s,
                                               int tok, int64_t slot, bool ok, int head, int h_kv,
@@ -577,10 +590,8 @@ __device__ __forceinline__ void epilogue_tile(uint32_t tacc, uint32_t acc_empty,
         ChunkStats<NCH> cs;
 #pragma unroll
         for (int k = 0; k < NCH; ++k) { cs.mn[k] = chmn[k]; cs.mx[k] = chmx[k]; }
-        const FixState<NG, NCH> fs = fixup_detect<D, G>(tacc, t_s, need, err, st, cs);
-        tc_fence_before();
-        mbar_arrive(acc_empty);
-        const GroupStats<NG> ex = fixup_exact<D, G>(fs, t_s, tok, head, h_kv, x_base, rt_head, lane);
+        const GroupStats<NG> ex = fixup<D, G>(tacc, acc_empty, t_s, need, err, st, cs, tok, head, h_kv, x_base,
+                                              rt_head, lane);
         if (need) {
 #pragma unroll
             for (int g = 0; g < NG; ++g) { mn_sz[g] = ex.mn[g]; mx_sz[g] = ex.mx[g]; }
