@@ -55,7 +55,7 @@ namespace {
 constexpr int kTile = 128;                     // tokens per tile (UMMA M)
 constexpr int kPieces = kRotationPieces;       // bf16 pieces of R
 constexpr int kStages = 3;                     // X tile buffers
-constexpr int kGroups = 4;                     // epilogue warp-groups
+constexpr int kGroups = 3;                     // epilogue warp-groups
 constexpr int kAccs = 4;                       // fp32 accumulators in TMEM (kAccs / kGroups per group)
 constexpr int kEpiWarps = 4 * kGroups;
 constexpr int kThreads = 32 * (2 + kEpiWarps);
@@ -601,7 +601,7 @@ __device__ __forceinline__ void epilogue_tile(uint32_t tacc, uint32_t acc_empty,
 }
 
 template <int D, int G>
-__global__ void __maxnreg__(96)
+__global__ void __maxnreg__(128)
 write_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_v,
                 const uint16_t* __restrict__ r_img, const float* __restrict__ r_kt, const float* __restrict__ r_vt,
                 const float* __restrict__ t_all,
