@@ -66,6 +66,43 @@ def test_write_tokens_parity(cuda, name, over, n):
     print("tolerated boundary flips:", flips)
 
 
+@pytest.mark.parametrize("name,n", [("qwen3_8b_bs1_100k", 40), ("qwen3_8b_bs1_100k", 640), ("tiny", 600)])
+def test_write_degenerate_and_saturated_groups(cuda, name, n):
+    """The degenerate group (max = min: scale 0, every code 0) and heavy clipping, on both kernels
+    (n < 512 runs on CUDA cores, n >= 512 on tensor cores). Thresholds are 0.5 everywhere. Rows come
+    in three kinds: zeros (every group is 0); 10 * (1 @ R^T), whose rotation is about 10 in every
+    channel, so the clipped row is 0.5 everywhere; and ordinary rows, most of whose channels clip
+    to +-0.5."""
+    cfg = cases.workload(name)
+    li, (rk, rv, _, _) = cases.calibration(cfg)
+    d, h_kv = cfg["d"], cfg["h_kv"]
+    tk = np.full((h_kv, d), 0.5, np.float32)
+    tv = np.full((h_kv, d), 0.5, np.float32)
+    geo = layout.Int2Geometry(d, cfg["group"], h_kv)
+    n_pages = synth.pages_for(n) + 3
+    slots = synth.rng_for(li.seed, "degenerate").permutation(n_pages * P)[:n].astype(np.int64)
+    k, v = li.kv("degenerate", n)
+    k, v = np.array(k, np.float32), np.array(v, np.float32)
+    ones = np.ones(d)
+    for h in range(h_kv):
+        k[0::3, h] = 0.0
+        v[0::3, h] = 0.0
+        k[1::3, h] = 10.0 * (ones @ rk[h].astype(np.float64).T)
+        v[1::3, h] = 10.0 * (ones @ rv[h].astype(np.float64).T)
+    ref = np.zeros(n_pages * geo.page_bytes, np.uint8)
+    info = cache.write_tokens(ref, geo, k, v, slots, rk, rv, tk, tv)
+    for kind in ("k", "v"):                          # the oracle really sees degenerate groups
+        for h in range(h_kv):
+            assert np.all(info[kind][h]["codes"][0::3] == 0) and np.all(info[kind][h]["codes"][1::3] == 0)
+
+    ctx = make_ctx(cfg)
+    ctx.calibrate_upload(0, rk, rv, tk, tv)
+    pool = torch.zeros(n_pages * geo.page_bytes, dtype=torch.uint8, device=cuda)
+    ctx.write_tokens(0, bf16(k, cuda), bf16(v, cuda), torch.from_numpy(slots).to(cuda), pool)
+    torch.cuda.synchronize()
+    cases.compare_int2(pool.cpu().numpy(), ref, geo, slots, info)
+
+
 @pytest.mark.parametrize("name,n", [("qwen3_8b_bs1_100k", 2000), ("tiny", 700)])
 def test_tensor_core_and_cuda_core_writes_agree(cuda, monkeypatch, name, n):
     """Both write kernels against the oracle, and against each other (codes may differ only by
