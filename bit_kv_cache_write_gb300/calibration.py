@@ -42,8 +42,22 @@ def rotation_from_target(target):
     return r
 
 
-def calibrate_layer(q_cal, k_cal, v_cal, sm_scale, clip_ratio=0.9):
-    """q_cal [n, H_q, d], k_cal/v_cal [m, H_kv, d] -> fp32 (R_k, R_v, T_k, T_v)."""
+def hadamard_rotation(d):
+    """R = H P with no covariance basis: the data-oblivious rotation that the v2
+    abstract contrasts with OSCAR ("Hadamard-only" / "QuaRot-style" INT2), kept
+    for the ablation."""
+    r = np.empty((d, d))
+    r[:, _bitrev_columns(d)] = _hadamard(d)
+    return r
+
+
+def calibrate_layer(q_cal, k_cal, v_cal, sm_scale, clip_ratio=0.9, kind="oscar"):
+    """q_cal [n, H_q, d], k_cal/v_cal [m, H_kv, d] -> fp32 (R_k, R_v, T_k, T_v).
+
+    kind "oscar": R = U H P from the attention-aware targets; kind "hadamard":
+    R = H P for K and V (the ablation), with thresholds by the same rule."""
+    if kind not in ("oscar", "hadamard"):
+        raise ValueError("unknown rotation kind %r" % (kind,))
     n, h_q, d = q_cal.shape
     h_kv = k_cal.shape[1]
     g = h_q // h_kv
@@ -60,8 +74,11 @@ def calibrate_layer(q_cal, k_cal, v_cal, sm_scale, clip_ratio=0.9):
         s = np.exp(logits)
         s /= s.sum(axis=1, keepdims=True)
         sv = s @ vh
-        rk = rotation_from_target(qg.T @ qg)
-        rv = rotation_from_target(sv.T @ sv)
+        if kind == "oscar":
+            rk = rotation_from_target(qg.T @ qg)
+            rv = rotation_from_target(sv.T @ sv)
+        else:
+            rk = rv = hadamard_rotation(d)
         r_k[h], r_v[h] = rk, rv
         t_k[h] = clip_ratio * np.abs(kh @ rk).max(axis=0)
         t_v[h] = clip_ratio * np.abs(vh @ rv).max(axis=0)

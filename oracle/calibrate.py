@@ -16,22 +16,31 @@ import numpy as np
 from . import rotation
 
 
-def calibrate_head(q_rows, k_rows, v_rows, sm_scale, clip_ratio, hadamard_block=None):
+def calibrate_head(q_rows, k_rows, v_rows, sm_scale, clip_ratio, hadamard_block=None, kind="oscar"):
     """Return (R_k, R_v, T_k, T_v) for one KV head, all fp64.
 
     q_rows [n_q, d]: the head group's calibration queries stacked as rows.
     k_rows, v_rows [n_kv, d]: calibration keys and values of this KV head.
+    kind: "oscar" (R = U H P from the attention-aware targets) or "hadamard"
+    (the data-oblivious ablation R = H P; thresholds by the same rule).
     """
-    c_k = rotation.key_covariance(q_rows)
-    c_v = rotation.value_covariance(q_rows, k_rows, v_rows, sm_scale)
-    r_k = rotation.oscar_rotation(c_k, hadamard_block)
-    r_v = rotation.oscar_rotation(c_v, hadamard_block)
+    if kind == "oscar":
+        c_k = rotation.key_covariance(q_rows)
+        c_v = rotation.value_covariance(q_rows, k_rows, v_rows, sm_scale)
+        r_k = rotation.oscar_rotation(c_k, hadamard_block)
+        r_v = rotation.oscar_rotation(c_v, hadamard_block)
+    elif kind == "hadamard":
+        d = np.asarray(k_rows).shape[1]
+        r_k = rotation.hadamard_only_rotation(d, hadamard_block)
+        r_v = r_k.copy()
+    else:
+        raise ValueError("unknown rotation kind %r" % (kind,))
     t_k = rotation.clip_thresholds(k_rows, r_k, clip_ratio)
     t_v = rotation.clip_thresholds(v_rows, r_v, clip_ratio)
     return r_k, r_v, t_k, t_v
 
 
-def calibrate_layer(q_cal, k_cal, v_cal, sm_scale, clip_ratio, hadamard_block=None):
+def calibrate_layer(q_cal, k_cal, v_cal, sm_scale, clip_ratio, hadamard_block=None, kind="oscar"):
     """Calibrate all KV heads of a layer.
 
     q_cal [n, H_q, d]; k_cal, v_cal [m, H_kv, d]. Returns fp64 arrays
@@ -47,5 +56,5 @@ def calibrate_layer(q_cal, k_cal, v_cal, sm_scale, clip_ratio, hadamard_block=No
     for h in range(h_kv):
         q_rows = np.asarray(q_cal[:, h * g:(h + 1) * g, :], dtype=np.float64).reshape(-1, d)
         rk[h], rv[h], tk[h], tv[h] = calibrate_head(
-            q_rows, k_cal[:, h, :], v_cal[:, h, :], sm_scale, clip_ratio, hadamard_block)
+            q_rows, k_cal[:, h, :], v_cal[:, h, :], sm_scale, clip_ratio, hadamard_block, kind)
     return rk, rv, tk, tv

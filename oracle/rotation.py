@@ -121,6 +121,19 @@ def oscar_rotation(target, hadamard_block=None):
     return u @ normalized_hadamard(d, hadamard_block) @ bit_reversal_matrix(d)
 
 
+def hadamard_only_rotation(d, hadamard_block=None):
+    """R = H @ P: the data-oblivious rotation that the pages set OSCAR against.
+
+    The v2 abstract (arXiv 2605.17757v2) contrasts OSCAR with data-oblivious
+    Hadamard rotations ("Hadamard-only INT2", "QuaRot-style INT2"), and the
+    QbitAI article (section "OSCAR aligns the rotation with attention") says a
+    plain Hadamard spreads outliers without knowing which directions attention
+    uses. The ablation keeps everything else of OSCAR (bit-reversal, clipping,
+    grouping) and drops U, i.e. U = I.
+    """
+    return normalized_hadamard(d, hadamard_block) @ bit_reversal_matrix(d)
+
+
 def clip_thresholds(x_rows, r, ratio):
     """Per-channel clip threshold: ratio * max_rows |(x @ R)_c|."""
     xr = np.asarray(x_rows, dtype=np.float64) @ np.asarray(r, dtype=np.float64)

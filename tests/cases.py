@@ -20,11 +20,14 @@ def workload(name, **over):
 
 
 def calibration(cfg, layer=0):
-    """Oracle calibration of one layer, rounded to the fp32 values both sides consume."""
+    """Oracle calibration of one layer, rounded to the fp32 values both sides consume.
+
+    cfg["rotation"] (default "oscar") may select the Hadamard-only ablation ("hadamard")."""
     li = synth.LayerInputs(cfg, layer)
     q_cal, k_cal, v_cal = li.calibration()
     sm = cfg["d"] ** -0.5
-    rk, rv, tk, tv = calibrate.calibrate_layer(q_cal, k_cal, v_cal, sm, cfg["clip_ratio"])
+    rk, rv, tk, tv = calibrate.calibrate_layer(q_cal, k_cal, v_cal, sm, cfg["clip_ratio"],
+                                               kind=cfg.get("rotation", "oscar"))
     f32 = [np.asarray(a, np.float32) for a in (rk, rv, tk, tv)]
     return li, f32
 

@@ -45,6 +45,7 @@ DECODE_CASES = [
     ("qwen3_32b_mixed16", {}, [1700, 2100, 1640], [320, 320, 320], 50, 4),
     ("qwen3_8b_bs1_100k", dict(h_q=8, h_kv=8), [1200], [320], 0, 0),
     ("qwen3_8b_bs1_100k", dict(h_q=16, h_kv=8), [640], [200], 0, 0),
+    ("qwen3_8b_bs1_100k", dict(rotation="hadamard"), [2500], [320], 0, 0),      # Hadamard-only ablation
 ]
 
 

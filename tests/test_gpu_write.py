@@ -42,6 +42,8 @@ WRITE_CASES = [
     ("qwen3_8b_bs1_100k", dict(group=32), 333),
     ("qwen3_8b_bs1_100k", dict(group=64, h_kv=2, h_q=4), 5),
     ("tiny", {}, 1),
+    ("qwen3_8b_bs1_100k", dict(rotation="hadamard"), 777),      # Hadamard-only ablation, tensor cores
+    ("qwen3_8b_bs1_100k", dict(rotation="hadamard"), 40),       # and CUDA cores
 ]
 
 
