@@ -1086,7 +1086,12 @@ DecodePlan plan_decode(const Shape& s, int num_sms, int batch, int max_hist) {
     // (few units: bs1 decode); otherwise at most kMaxPagesPerSplit pages per split, in as many
     // waves as that takes (many units or long sequences)
     const int slots = split_ctas_per_sm(s) * num_sms;
-    int splits = units > 0 ? slots / units - 1 : 1;
+    // BF16 splits: two when the grid is one wave of few units (bs1), so that the BF16 segment's CTA
+    // (about 1.7x an INT2 split's bytes at 100k) is not the last to finish
+    const int bf16_pages = (s.sink + s.recent + kPage - 1) / kPage;
+    p.bf16_splits = (units > 0 && slots / units >= 16 && bf16_pages >= 2) ? 2 : 1;
+    p.bf16_pages_per_split = (bf16_pages + p.bf16_splits - 1) / p.bf16_splits;
+    int splits = units > 0 ? slots / units - p.bf16_splits : 1;
     if (splits < 1) splits = 1;
     const int by_len = (max_pages + kMaxPagesPerSplit - 1) / kMaxPagesPerSplit;
     if (splits < by_len) splits = by_len;
@@ -1094,7 +1099,6 @@ DecodePlan plan_decode(const Shape& s, int num_sms, int batch, int max_hist) {
     if (max_pages == 0) splits = 1;
     p.pages_per_split = max_pages > 0 ? (max_pages + splits - 1) / splits : 1;
     p.int2_splits = max_pages > 0 ? (max_pages + p.pages_per_split - 1) / p.pages_per_split : 1;
-    p.bf16_splits = 1;
     p.total_splits = p.int2_splits + p.bf16_splits;
     p.ws_partials = align256((size_t)batch * s.h_q * p.total_splits * (s.d + 2) * sizeof(float));
     p.ws_qrot = align256((size_t)batch * s.h_q * (3 * s.d * sizeof(__half) + sizeof(float) +
@@ -1146,7 +1150,7 @@ cudaError_t launch_decode(const Shape& s, const LayerParams& prm, const DecodePl
     sa.partials = partials;
     sa.h_kv = s.h_kv; sa.int2_splits = plan.int2_splits; sa.pages_per_split = plan.pages_per_split;
     sa.bf16_splits = plan.bf16_splits;
-    sa.bf16_pages_per_split = (s.sink + s.recent + kPage - 1) / kPage;
+    sa.bf16_pages_per_split = plan.bf16_pages_per_split;
     sa.total_splits = plan.total_splits;
     sa.scale_log2 = sl2_hi;
     sa.scale_log2_lo = sl2_lo;

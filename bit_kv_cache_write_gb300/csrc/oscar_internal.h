@@ -120,7 +120,8 @@ void build_rotation_images(const float* r, int h_kv, int d, uint16_t* out);
 struct DecodePlan {
     int int2_splits;        // splits over the INT2 history
     int pages_per_split;    // INT2 pages per split
-    int bf16_splits;        // splits over the BF16 segment (0 if the segment is empty by config)
+    int bf16_splits;        // splits over the BF16 segment
+    int bf16_pages_per_split;  // BF16 pages per BF16 split
     int total_splits;
     size_t ws_partials;     // bytes of split partials
     size_t ws_qrot;         // bytes of rotated queries
