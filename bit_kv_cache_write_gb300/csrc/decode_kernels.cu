@@ -171,16 +171,18 @@ q_prep_kernel(const __nv_bfloat16* __restrict__ q, const float* __restrict__ r_k
     const int bh = blockIdx.x;
     const int kv = (bh % h_q) / g;
     const int c = threadIdx.x % D, quarter = threadIdx.x / D;
+    // R_k terms of this thread: constant calibration data, so they load before the wait for the
+    // previous kernel (all in flight at once)
+    const float* r = r_k + (size_t)kv * D * D + (size_t)quarter * Q4 * D + c;
+    float rv[Q4];
+#pragma unroll
+    for (int i = 0; i < Q4; ++i) rv[i] = __ldg(r + (size_t)i * D);
     pdl_wait();
     pdl_trigger();
     // the split kernel's ticket counter of this (sequence, KV head) starts at zero
     if (threadIdx.x == 0 && (bh % h_q) % g == 0) counters[(bh / h_q) * (h_q / g) + kv] = 0;
     if (threadIdx.x < D) qs[c] = __bfloat162float(q[(size_t)bh * D + c]);
     __syncthreads();
-    const float* r = r_k + (size_t)kv * D * D + (size_t)quarter * Q4 * D + c;
-    float rv[Q4];
-#pragma unroll
-    for (int i = 0; i < Q4; ++i) rv[i] = __ldg(r + (size_t)i * D);       // all loads in flight at once
     float hi = 0.0f, lo = 0.0f;
 #pragma unroll
     for (int i = 0; i < Q4; ++i) {
