@@ -11,11 +11,11 @@
 // three bf16 pieces, R ~= R1 + R2 + R3 (24 significant bits): bf16 x bf16
 // products are exact in fp32, so the rotation keeps fp32-level accuracy. One
 // thread issues tcgen05.mma into an fp32 accumulator in tensor memory, small
-// pieces first. Two accumulators alternate between two epilogue warp-groups, so
-// the MMAs of tile i+1 overlap the epilogue of tile i. Each epilogue thread owns one token row (one TMEM lane).
-// It clips the row, takes the group min/max, decides the codes in fp32 exactly
-// as the CUDA-core kernel does, and stores the packed row and its scale/zero
-// into the paged cache.
+// pieces first. Four accumulators rotate over three epilogue warp-groups, so the
+// MMAs of the next tiles overlap the epilogues of the current ones. Each epilogue thread owns one
+// token row (one TMEM lane). It clips the row, takes the group min/max, decides the codes in fp32
+// exactly as the CUDA-core kernel does, stores the packed codes, and then the scale/zero (after the
+// rare exact path below, which can change only those).
 //
 // Error bound of the tensor-core rotation. Within one MMA step the products are
 // aligned to the largest term and truncated about 24 bits below it, and the sum
@@ -25,16 +25,18 @@
 // leading piece carry a full-size M. When that bound could move the stored zero
 // or scale by more than one fp16 step (tested on the fp16 roundings of the bound's ends), the
 // candidate min/max channels are
-// recomputed with a double-float dot product over a row of R^T (batches of 8 channels spread over
-// the warp), as on the CUDA-core path. Those exact values set the stored zero and scale.
+// recomputed with a double-float dot product over a row of R^T (up to 4 candidates per round, each
+// spread over the warp), as on the CUDA-core path. Those exact values set the stored zero and scale.
 //
 // Every CTA takes a share of one head's token tiles for K and then the same tiles for V, so the
 // rare exact path (mostly V rows) spreads evenly over the GPU; R_v replaces R_k in shared memory
 // once the K tiles' MMAs are done.
 //
 // Roles: warp 0 loads (TMA), warp 1 allocates tensor memory and issues the MMAs,
-// warps 2..9 run the epilogue as two warp-groups that take alternate tiles, each with its own
-// accumulator (warp w reads TMEM lanes 32*(w%4) .. +31). Every
+// warps 2..13 run the epilogue as three warp-groups that take tiles in turn, tile i in accumulator
+// i % 4 (warp w reads TMEM lanes 32*(w%4) .. +31). 14 warps at 128 registers fit one SM without
+// spills; 18 warps would cap every thread at 96, because one of the four schedulers of an SM
+// would carry five warps from its 16K registers. Every
 // mbarrier wait is bounded. A role that gives up sets a shared flag and records
 // kind 4 in the error word. The others then stop, and the copies and MMAs still
 // in flight are drained (bounded) before tensor memory is freed.
