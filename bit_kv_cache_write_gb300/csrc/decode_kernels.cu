@@ -15,11 +15,15 @@
 //        copies, four stages per warp. They compute q_rot . codes and
 //        p . codes with mma.sync m16n8k16 on the packed codes, and keep an
 //        online softmax.
-//      - BF16 splits handle sink + recent on CUDA cores.
+//      - BF16 splits handle sink + recent on CUDA cores: the last split of each
+//        (sequence, KV head), or the last two when one wave serves few units.
 //      - Each split writes a partial (m, l, acc[d]) per query head of the
 //        group, with m in log2 units.
 //   3. merge: combines the splits of each query head, un-rotates the INT2
-//      accumulator by R_v^T and normalises.
+//      accumulator by R_v^T and normalises. When that merge is short
+//      (g x splits <= 128, i.e. large batches) the CTA of the split kernel that
+//      finishes a (sequence, KV head) last does it instead, and there are two
+//      launches per layer.
 //
 // Exactness of the INT2 logits. With codes c in {0..3}, scale s and zero z per
 // group:
