@@ -160,7 +160,35 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
     for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const float* v) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+        "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};"
+        :: "r"(taddr),
+           "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])), "r"(__float_as_uint(v[3])),
+           "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])), "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])),
+           "r"(__float_as_uint(v[8])), "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
+           "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])), "r"(__float_as_uint(v[15])),
+           "r"(__float_as_uint(v[16])), "r"(__float_as_uint(v[17])), "r"(__float_as_uint(v[18])), "r"(__float_as_uint(v[19])),
+           "r"(__float_as_uint(v[20])), "r"(__float_as_uint(v[21])), "r"(__float_as_uint(v[22])), "r"(__float_as_uint(v[23])),
+           "r"(__float_as_uint(v[24])), "r"(__float_as_uint(v[25])), "r"(__float_as_uint(v[26])), "r"(__float_as_uint(v[27])),
+           "r"(__float_as_uint(v[28])), "r"(__float_as_uint(v[29])), "r"(__float_as_uint(v[30])), "r"(__float_as_uint(v[31]))
+        : "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 // ---- epilogue ---------------------------------------------------------------------------------
+
+// Three-input fp32 min / max (one instruction each on sm_100 and later; finite inputs here).
+__device__ __forceinline__ float fmin3(float a, float b, float c) {
+    float r;
+    asm("min.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+    float r;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
 
 __device__ __forceinline__ void two_sum(float a, float b, float& s, float& e) {
     s = __fadd_rn(a, b);
@@ -505,9 +533,9 @@ __device__ __forceinline__ void epilogue_tile(uint32_t tacc, uint32_t acc_empty,
         float v[32];
         tmem_ld32(tacc + 32 * ch, v);
         tmem_wait_ld();
-        // min_c clip(x_c) = min(min_c max(x_c, -t_c), min_c t_c) and max_c clip(x_c) =
-        // max(max_c min(x_c, t_c), -min_c t_c): one op per element and side instead of a clip
-        float cmn = t_s[2 * D + ch], cmx = -t_s[2 * D + ch];        // min t over the chunk
+        // the clipped row goes back into the accumulator, so pass 2 (and the rare path) read it
+        // clipped; ||x|| is taken before the clip
+        float cmn = FLT_MAX, cmx = -FLT_MAX;
 #pragma unroll
         for (int j = 0; j < 32; j += 4) {
             const float4 t = *reinterpret_cast<const float4*>(t_s + 32 * ch + j);
@@ -515,9 +543,16 @@ __device__ __forceinline__ void epilogue_tile(uint32_t tacc, uint32_t acc_empty,
             sq1 = fmaf(v[j + 1], v[j + 1], sq1);
             sq0 = fmaf(v[j + 2], v[j + 2], sq0);
             sq1 = fmaf(v[j + 3], v[j + 3], sq1);
-            cmn = fminf(fminf(cmn, fmaxf(v[j], -t.x)), fminf(fmaxf(v[j + 1], -t.y), fminf(fmaxf(v[j + 2], -t.z), fmaxf(v[j + 3], -t.w))));
-            cmx = fmaxf(fmaxf(cmx, fminf(v[j], t.x)), fmaxf(fminf(v[j + 1], t.y), fmaxf(fminf(v[j + 2], t.z), fminf(v[j + 3], t.w))));
+            v[j] = fminf(fmaxf(v[j], -t.x), t.x);
+            v[j + 1] = fminf(fmaxf(v[j + 1], -t.y), t.y);
+            v[j + 2] = fminf(fmaxf(v[j + 2], -t.z), t.z);
+            v[j + 3] = fminf(fmaxf(v[j + 3], -t.w), t.w);
+            cmn = fmin3(cmn, v[j], v[j + 1]);
+            cmn = fmin3(cmn, v[j + 2], v[j + 3]);
+            cmx = fmax3(cmx, v[j], v[j + 1]);
+            cmx = fmax3(cmx, v[j + 2], v[j + 3]);
         }
+        tmem_st32(tacc + 32 * ch, v);
         // a 32-channel chunk lies inside one group (G >= 32)
 #pragma unroll
         for (int g = 0; g < NG; ++g)
@@ -526,6 +561,7 @@ __device__ __forceinline__ void epilogue_tile(uint32_t tacc, uint32_t acc_empty,
         for (int k = 0; k < NCH; ++k)
             if (k == ch) { chmn[k] = cmn; chmx[k] = cmx; }
     }
+    tmem_wait_st();                                 // pass 2 reads back what pass 1 stored
     const float err = 1.01f * (float)(D / 16) * 9.0f * 0x1p-23f * sqrtf((sq0 + sq1) * 1.002f);
     bool need = false;
 #pragma unroll
@@ -560,11 +596,9 @@ __device__ __forceinline__ void epilogue_tile(uint32_t tacc, uint32_t acc_empty,
         for (int w = 0; w < D / 16; ++w) cw[w] = 0u;
 #pragma unroll
         for (int j = 0; j < 32; j += 4) {
-            const float4 t = *reinterpret_cast<const float4*>(t_s + 32 * ch + j);
-            const float tt[4] = {t.x, t.y, t.z, t.w};
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
-                const float xh = fminf(fmaxf(v[j + k], -tt[k]), tt[k]);
+                const float xh = v[j + k];                // clipped in pass 1
                 // u in [0, 3 + tiny]: adding 1.5 * 2^23 rounds it half-to-even onto the integer grid
                 const float u = __fmul_rn(__fsub_rn(xh, gmn), ginv);
                 const uint32_t bits = __float_as_uint(__fadd_rn(u, 12582912.0f));
