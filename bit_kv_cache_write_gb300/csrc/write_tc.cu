@@ -178,6 +178,34 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float* v) {
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 // ---- epilogue ---------------------------------------------------------------------------------
 
+// Packed fp32 pairs (sm_100 and later): each half of sub/mul/add/fma.f32x2 rounds to nearest
+// exactly as the scalar instruction does.
+__device__ __forceinline__ uint64_t f32x2(float lo, float hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ uint64_t sub_f32x2(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ uint64_t mul_f32x2(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ uint64_t add_f32x2(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ uint64_t fma_f32x2(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+    return r;
+}
+
 // Three-input fp32 min / max (one instruction each on sm_100 and later; finite inputs here).
 __device__ __forceinline__ float fmin3(float a, float b, float c) {
     float r;
@@ -525,7 +553,7 @@ __device__ __forceinline__ void epilogue_tile(uint32_t tacc, uint32_t acc_empty,
     float mn[NG], mx[NG];
 #pragma unroll
     for (int g = 0; g < NG; ++g) { mn[g] = FLT_MAX; mx[g] = -FLT_MAX; }
-    float sq0 = 0.0f, sq1 = 0.0f;
+    uint64_t sq2 = 0ull;                            // packed (sum over even, sum over odd channels)
     float chmn[NCH], chmx[NCH];                     // per-chunk clipped min/max (fixup detection)
     // not unrolled over chunks: the compiler would otherwise keep several chunks live
 #pragma unroll 1
@@ -539,10 +567,9 @@ __device__ __forceinline__ void epilogue_tile(uint32_t tacc, uint32_t acc_empty,
 #pragma unroll
         for (int j = 0; j < 32; j += 4) {
             const float4 t = *reinterpret_cast<const float4*>(t_s + 32 * ch + j);
-            sq0 = fmaf(v[j], v[j], sq0);
-            sq1 = fmaf(v[j + 1], v[j + 1], sq1);
-            sq0 = fmaf(v[j + 2], v[j + 2], sq0);
-            sq1 = fmaf(v[j + 3], v[j + 3], sq1);
+            const uint64_t a2 = f32x2(v[j], v[j + 1]), b2 = f32x2(v[j + 2], v[j + 3]);
+            sq2 = fma_f32x2(a2, a2, sq2);                 // even channels in the low half, odd in the high
+            sq2 = fma_f32x2(b2, b2, sq2);
             v[j] = fminf(fmaxf(v[j], -t.x), t.x);
             v[j + 1] = fminf(fmaxf(v[j + 1], -t.y), t.y);
             v[j + 2] = fminf(fmaxf(v[j + 2], -t.z), t.z);
@@ -562,6 +589,7 @@ __device__ __forceinline__ void epilogue_tile(uint32_t tacc, uint32_t acc_empty,
             if (k == ch) { chmn[k] = cmn; chmx[k] = cmx; }
     }
     tmem_wait_st();                                 // pass 2 reads back what pass 1 stored
+    const float sq0 = __uint_as_float((uint32_t)sq2), sq1 = __uint_as_float((uint32_t)(sq2 >> 32));
     const float err = 1.01f * (float)(D / 16) * 9.0f * 0x1p-23f * sqrtf((sq0 + sq1) * 1.002f);
     bool need = false;
 #pragma unroll
@@ -594,17 +622,17 @@ __device__ __forceinline__ void epilogue_tile(uint32_t tacc, uint32_t acc_empty,
         uint32_t cw[D / 16];
 #pragma unroll
         for (int w = 0; w < D / 16; ++w) cw[w] = 0u;
+        // u = (x_hat - mn) * inv, then + 1.5 * 2^23, two channels per packed fp32 instruction (each
+        // half rounds exactly as the scalar op would). u is in [0, 3 + tiny], so adding 1.5 * 2^23
+        // rounds it half-to-even onto the integer grid. x_hat was clipped in pass 1.
+        const uint64_t mn2 = f32x2(gmn, gmn), inv2 = f32x2(ginv, ginv), mag2 = f32x2(12582912.0f, 12582912.0f);
 #pragma unroll
-        for (int j = 0; j < 32; j += 4) {
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const float xh = v[j + k];                // clipped in pass 1
-                // u in [0, 3 + tiny]: adding 1.5 * 2^23 rounds it half-to-even onto the integer grid
-                const float u = __fmul_rn(__fsub_rn(xh, gmn), ginv);
-                const uint32_t bits = __float_as_uint(__fadd_rn(u, 12582912.0f));
-                const int off = bit_offset(KIND, j + k, D);
-                cw[off >> 5] += bits << (off & 31);
-            }
+        for (int j = 0; j < 32; j += 2) {
+            const uint64_t b2 = add_f32x2(mul_f32x2(sub_f32x2(f32x2(v[j], v[j + 1]), mn2), inv2), mag2);
+            const uint32_t bits0 = (uint32_t)b2, bits1 = (uint32_t)(b2 >> 32);
+            const int off0 = bit_offset(KIND, j, D), off1 = bit_offset(KIND, j + 1, D);
+            cw[off0 >> 5] += bits0 << (off0 & 31);
+            cw[off1 >> 5] += bits1 << (off1 & 31);
         }
         const int delta = bit_offset(KIND, 32 * ch, D);
         const int bs = delta & 31;
