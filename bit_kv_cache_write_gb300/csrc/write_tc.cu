@@ -71,8 +71,8 @@ struct TcLayout {
     static constexpr int kOffB = 0;
     static constexpr int kOffA = kOffB + kPieces * kPieceBytes;
     static constexpr int kOffT = kOffA + kStages * kTileBytes;
-    // T_k, T_v of the head, then per 32-channel chunk min T_k (at 2D) and min T_v (at 3D)
-    static constexpr int kOffBar = kOffT + 4 * D * 4;
+    // T_k, T_v of the head
+    static constexpr int kOffBar = kOffT + 2 * D * 4;
     static constexpr int kBars = 2 * kStages + 2 * kAccs + 1;     // full, empty, acc_full[], acc_empty[], b_full
     static constexpr int kOffMisc = kOffBar + kBars * 8;
     static constexpr int kBytes = kOffMisc + 16;
@@ -403,7 +403,7 @@ __device__ __forceinline__ FixState<D / G, D / 32> fixup_detect(uint32_t tacc, c
                 cmx = -FLT_MAX;
 #pragma unroll
                 for (int j = 0; j < 32; ++j) {
-                    const float xh = fminf(fmaxf(v[j], -t_s[32 * ch + j]), t_s[32 * ch + j]);
+                    const float xh = v[j];                 // clipped in pass 1
                     const bool is_c = xh <= lc || xh >= hc;
                     cm |= (uint32_t)is_c << j;
                     if (!is_c) { cmn = fminf(cmn, xh); cmx = fmaxf(cmx, xh); }
@@ -713,13 +713,6 @@ write_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant
     }
     for (int i = threadIdx.x; i < 2 * D; i += kThreads)
         t_s[i] = t_all[((size_t)(i / D) * h_kv + head) * D + i % D];
-    if (threadIdx.x < 2 * (D / 32)) {
-        const int kd = threadIdx.x / (D / 32), ch = threadIdx.x % (D / 32);
-        const float* t = t_all + ((size_t)kd * h_kv + head) * D + 32 * ch;
-        float m = t[0];
-        for (int j = 1; j < 32; ++j) m = fminf(m, t[j]);
-        t_s[(2 + kd) * D + ch] = m;
-    }
     if (warp == 1) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
                      :: "r"(smem_u32(tmem_slot)), "r"(L::kTmemCols) : "memory");
