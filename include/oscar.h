@@ -127,9 +127,14 @@ typedef struct {
 typedef struct oscar_ctx oscar_ctx_t;
 
 /* Create a context on the current CUDA device.
- * Validates cfg, then allocates the per-layer calibration buffers
- * (n_layers * (3 * H_kv * d * d + 2 * H_kv * d + H_kv) * 4 bytes: R_k, R_v, R_v^T,
- * T_k, T_v and one P.V exponent per KV head) and the error word. On failure *out is NULL.
+ * Validates cfg, then allocates the per-layer calibration buffers and the
+ * error word. Per layer:
+ *   (3 * H_kv * d * d + 2 * H_kv * d + H_kv) * 4 bytes: R_k, R_v, R_v^T, T_k, T_v
+ *     and one P.V exponent per KV head;
+ *   H_kv * d * d * 4 bytes: R_k^T (the exact path of the tensor-core write);
+ *   2 * 3 * H_kv * d * d * 2 bytes: R_k and R_v as three bf16 pieces each, in
+ *     the shared-memory image the tensor-core write loads.
+ * (3.7 MB per layer at H_kv = 8, d = 128.) On failure *out is NULL.
  * Blocking: returns after the allocations complete. */
 OSCAR_API oscar_status oscar_create(const oscar_config_t* cfg, oscar_ctx_t** out);
 
