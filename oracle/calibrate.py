@@ -5,7 +5,7 @@ attention": a few calibration samples give, per layer and per head, the key
 target Q^T Q and the value target V^T S^T S V; from them the offline stage makes
 a fixed rotation and clipping thresholds that inference reuses unchanged.
 
-Readings (the design doc lists them): the key target of a KV head stacks the
+Readings taken where the pages are silent: the key target of a KV head stacks the
 calibration queries of all query heads of its group as rows; S is the row-wise
 softmax of sm_scale * Q K^T over the calibration keys (no mask); thresholds are
 ``clip_ratio`` times the per-channel calibration maximum of |x @ R|.

@@ -4,7 +4,7 @@ Source: QbitAI article on OSCAR, serving-pipeline part: four 2-bit values are
 packed into one byte; the cache stays compatible with paged KV serving and the
 radix prefix cache (v1/v2 abstracts: "paged KV-cache layouts", "prefix
 caching"). The pages fix nothing else about the layout, so the layout below is
-this library's own definition (stated in include/oscar.h and the design doc) and the
+this library's own definition (stated in include/oscar.h) and the
 oracle writes it out independently of the CUDA code.
 
 INT2 pool: bytes [num_pages][H_kv][2 (K, V)][segment], page size P.

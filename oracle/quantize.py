@@ -5,8 +5,7 @@ is rotated, clipped, quantized and packed into the INT2 history; 2-bit INT has
 four levels; the INT2 decode kernel dequantizes with a scale and a zero point.
 The v1/v2 abstracts fix the rotation and clipping thresholds offline.
 
-Definition used here (the pages give no formula; these readings are listed in
-DESIGN.md):
+Definition used here (the pages give no formula; these are readings of them):
 
   x_rot = x @ R                           exact (fp64), then rounded to fp32
   x_hat = min(max(x_rot, -T), T)          per channel threshold T

@@ -10,7 +10,7 @@ balances the INT2 groups. The v2 abstract (arXiv 2605.17757v2) calls these
 "attention-aware covariance targets" and "second-moment structures", and the
 title's "spectral" is read as: U is the eigenbasis of that target.
 
-Readings taken where the pages are silent (all listed in the design doc):
+Readings taken where the pages are silent:
 * rotation acts on row vectors, x_rot = x @ R;
 * U holds eigenvectors as columns, sorted by descending eigenvalue, each column
   signed so its largest-magnitude entry is positive (ties: lowest index);
