@@ -282,6 +282,7 @@ oscar_status oscar_decode(oscar_ctx_t* ctx, int layer, const void* q,
     if (st != OSCAR_OK) return st;
     if (batch < 0 || max_hist < 0) return fail(OSCAR_ERR_INVALID_ARG, "batch %d / max_hist %d negative", batch, max_hist);
     if (batch == 0) return OSCAR_OK;
+    if (batch > 65535) return fail(OSCAR_ERR_UNSUPPORTED, "batch %d above 65535 (one grid dimension per sequence)", batch);
     if (!q || !out || !hist_len || !bf16_len) return fail(OSCAR_ERR_INVALID_ARG, "device pointer is NULL");
     if (max_hist > 0 && (!int2_pool || !int2_tables || int2_table_stride <= 0 || int2_pool_pages <= 0))
         return fail(OSCAR_ERR_INVALID_ARG, "INT2 pool/tables missing while max_hist = %d", max_hist);

@@ -204,7 +204,8 @@ OSCAR_API size_t oscar_decode_workspace_size(const oscar_ctx_t* ctx, int batch, 
  *   workspace:    DEVICE, >= oscar_decode_workspace_size(ctx, batch, max_hist)
  *                 bytes, 256-byte aligned. It holds split partials and is
  *                 scratch between calls.
- * Asynchronous on `stream`. batch == 0 is a no-op. */
+ * Asynchronous on `stream`. batch == 0 is a no-op; batch > 65535 returns
+ * OSCAR_ERR_UNSUPPORTED. */
 OSCAR_API oscar_status oscar_decode(oscar_ctx_t* ctx, int layer, const void* q,
                           const void* int2_pool, int64_t int2_pool_pages,
                           const int32_t* int2_tables, int int2_table_stride,

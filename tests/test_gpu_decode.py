@@ -105,6 +105,20 @@ def test_debug_bounds_records_bad_page(cuda):
     assert np.all(np.isfinite(got))
 
 
+def test_batch_above_the_grid_limit_is_rejected(cuda):
+    cfg = cases.workload("tiny")
+    ctx = O.Oscar(n_layers=1, n_q_heads=cfg["h_q"], n_kv_heads=cfg["h_kv"], head_dim=cfg["d"], group=cfg["group"])
+    li, (rk, rv, tk, tv) = cases.calibration(cfg)
+    ctx.calibrate_upload(0, rk, rv, tk, tv)
+    B = 65536
+    z = lambda *s, dt=torch.int32: torch.zeros(*s, dtype=dt, device=cuda)
+    with pytest.raises(O.OscarError) as e:
+        ctx.decode(0, z(B, 4, 64, dt=torch.bfloat16), z(4096, dt=torch.uint8), z(B, 4), z(B), 64,
+                   z(2 * 2 * 2 * 16 * 64, dt=torch.bfloat16), z(B, 20), z(B), z(B, 4, 64, dt=torch.float32),
+                   z(1024, dt=torch.uint8))
+    assert e.value.status == -2
+
+
 def test_workspace_too_small_is_rejected(cuda):
     cfg = cases.workload("tiny")
     ctx = O.Oscar(n_layers=1, n_q_heads=cfg["h_q"], n_kv_heads=cfg["h_kv"], head_dim=cfg["d"], group=cfg["group"])
