@@ -83,3 +83,35 @@ def calibrate_layer(q_cal, k_cal, v_cal, sm_scale, clip_ratio=0.9, kind="oscar")
         t_k[h] = clip_ratio * np.abs(kh @ rk).max(axis=0)
         t_v[h] = clip_ratio * np.abs(vh @ rv).max(axis=0)
     return r_k, r_v, t_k, t_v
+
+
+def calibrate_layer_gpu(q_cal, k_cal, v_cal, sm_scale, clip_ratio=0.9, device="cuda"):
+    """calibrate_layer with the two covariance targets accumulated on the GPU (fp64,
+    ``oscar_calibration_targets``); the eigendecomposition, R = U H P and the thresholds stay on the
+    host. Inputs are host arrays [n, H_q, d] and [m, H_kv, d]; returns fp32 (R_k, R_v, T_k, T_v)."""
+    import torch
+    from . import oscar
+
+    q = torch.as_tensor(np.ascontiguousarray(q_cal, np.float32), device=device)
+    k = torch.as_tensor(np.ascontiguousarray(k_cal, np.float32), device=device)
+    v = torch.as_tensor(np.ascontiguousarray(v_cal, np.float32), device=device)
+    n, h_q, d = q.shape
+    h_kv = k.shape[1]
+    tk = torch.empty(h_kv, d, d, dtype=torch.float64, device=device)
+    tv = torch.empty_like(tk)
+    ws = torch.empty(oscar.oscar_calibration_workspace_size(n, h_q, h_kv, d), dtype=torch.uint8, device=device)
+    oscar.oscar_calibration_targets(q, k, v, sm_scale, tk, tv, ws)
+    tk, tv = tk.cpu().numpy(), tv.cpu().numpy()
+    kh_all = np.asarray(k_cal, np.float64)
+    vh_all = np.asarray(v_cal, np.float64)
+    r_k = np.empty((h_kv, d, d), np.float32)
+    r_v = np.empty((h_kv, d, d), np.float32)
+    t_k = np.empty((h_kv, d), np.float32)
+    t_v = np.empty((h_kv, d), np.float32)
+    for h in range(h_kv):
+        rk = rotation_from_target(tk[h])
+        rv = rotation_from_target(tv[h])
+        r_k[h], r_v[h] = rk, rv
+        t_k[h] = clip_ratio * np.abs(kh_all[:, h] @ rk).max(axis=0)
+        t_v[h] = clip_ratio * np.abs(vh_all[:, h] @ rv).max(axis=0)
+    return r_k, r_v, t_k, t_v

@@ -310,6 +310,41 @@ oscar_status oscar_decode(oscar_ctx_t* ctx, int layer, const void* q,
     return e == cudaSuccess ? OSCAR_OK : cuda_fail(e, "decode launch");
 }
 
+namespace {
+bool calibration_shape_ok(int n, int h_q, int h_kv, int d) {
+    return n >= 1 && h_kv >= 1 && h_q >= h_kv && h_q % h_kv == 0 && (d == 64 || d == 128);
+}
+}  // namespace
+
+size_t oscar_calibration_workspace_size(int n, int n_q_heads, int n_kv_heads, int head_dim) {
+    if (!calibration_shape_ok(n, n_q_heads, n_kv_heads, head_dim)) return 0;
+    return oscar::calibration_workspace_bytes(n, n_q_heads, n_kv_heads, head_dim);
+}
+
+oscar_status oscar_calibration_targets(const float* q_cal, const float* k_cal, const float* v_cal, int n, int m,
+                                       int n_q_heads, int n_kv_heads, int head_dim, double sm_scale,
+                                       double* target_k, double* target_v, void* workspace, size_t workspace_bytes,
+                                       void* stream) {
+    if (!q_cal || !k_cal || !v_cal || !target_k || !target_v)
+        return fail(OSCAR_ERR_INVALID_ARG, "device pointer is NULL");
+    if (n < 1 || m < 1 || n_kv_heads < 1 || n_q_heads < n_kv_heads || n_q_heads % n_kv_heads ||
+        !(sm_scale > 0.0) || !std::isfinite(sm_scale))
+        return fail(OSCAR_ERR_INVALID_ARG, "n %d, m %d, heads %d/%d or sm_scale %g invalid", n, m, n_q_heads,
+                    n_kv_heads, sm_scale);
+    if ((head_dim != 64 && head_dim != 128) || m > oscar::kCalibMaxKeys)
+        return fail(OSCAR_ERR_UNSUPPORTED, "head_dim %d or m %d (at most %d keys) unsupported", head_dim, m,
+                    oscar::kCalibMaxKeys);
+    const size_t need = oscar::calibration_workspace_bytes(n, n_q_heads, n_kv_heads, head_dim);
+    if (!workspace || workspace_bytes < need)
+        return fail(OSCAR_ERR_WORKSPACE, "workspace %zu bytes, need %zu", workspace_bytes, need);
+    if (reinterpret_cast<uintptr_t>(workspace) % 256)
+        return fail(OSCAR_ERR_INVALID_ARG, "workspace is not 256-byte aligned");
+    cudaError_t e = oscar::launch_calibration_targets(q_cal, k_cal, v_cal, n, m, n_q_heads, n_kv_heads, head_dim,
+                                                      sm_scale, target_k, target_v, static_cast<double*>(workspace),
+                                                      static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? OSCAR_OK : cuda_fail(e, "calibration launch");
+}
+
 size_t oscar_int2_page_bytes(const oscar_ctx_t* ctx) {
     if (!ctx) return 0;
     const oscar::Shape& s = ctx->shape;

@@ -103,6 +103,14 @@ cudaError_t launch_write(const Shape& s, const LayerParams& p, int num_sms,
 
 cudaError_t launch_transpose(const float* src, float* dst, int h, int d, cudaStream_t st);
 
+// Offline calibration targets (calib_kernels.cu): Q^T Q and (S V)^T (S V) per KV head, fp64.
+constexpr int kCalibMaxKeys = 8192;                                     // m: calibration keys per head
+constexpr size_t kCalibMaxSmem = (size_t)(kCalibMaxKeys + 128) * sizeof(double);
+size_t calibration_workspace_bytes(int n, int h_q, int h_kv, int d);
+cudaError_t launch_calibration_targets(const float* q, const float* k, const float* v, int n, int m, int h_q, int h_kv,
+                                       int d, double sm_scale, double* target_k, double* target_v, double* sv_rows,
+                                       cudaStream_t st);
+
 // ---- tensor-core bulk write (write_tc.cu)
 constexpr int kTcMinTokens = 512;     // below this the CUDA-core kernel is used
 constexpr int kRotationPieces = 3;    // bf16 pieces of R in the operand images

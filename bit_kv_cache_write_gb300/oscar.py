@@ -52,6 +52,9 @@ _SIGS = {
     "oscar_debug_error": (_i, [_vp, ctypes.POINTER(_i), ctypes.POINTER(ctypes.c_longlong)]),
     "oscar_decode_static_workspace": (_i, [_vp, _i, _vp, _vp, _i64, _vp, _i, _vp, _i, _vp, _i64, _vp, _i, _vp,
                                            _vp, _i, _vp]),
+    "oscar_calibration_workspace_size": (_sz, [_i, _i, _i, _i]),
+    "oscar_calibration_targets": (_i, [_vp, _vp, _vp, _i, _i, _i, _i, _i, ctypes.c_double, _vp, _vp, _vp, _sz,
+                                       _vp]),
     "oscar_profile_enable": (_i, [_vp, _i]),
     "oscar_profile_read": (_i, [_vp, _i, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_longlong)]),
 }
@@ -183,6 +186,23 @@ def oscar_decode(ctx, layer, q, int2_pool, int2_tables, hist_len, max_hist, bf16
         _dptr(bf16_len, torch.int32, "bf16_len"),
         _dptr(out, torch.float32, "out"), _dptr(workspace, None, "workspace"),
         workspace.numel() * workspace.element_size(), batch, _stream(stream)), "oscar_decode")
+
+
+def oscar_calibration_workspace_size(n, n_q_heads, n_kv_heads, head_dim):
+    return lib().oscar_calibration_workspace_size(n, n_q_heads, n_kv_heads, head_dim)
+
+
+def oscar_calibration_targets(q_cal, k_cal, v_cal, sm_scale, target_k, target_v, workspace, stream=None):
+    """q_cal fp32 [n][H_q][d], k_cal/v_cal fp32 [m][H_kv][d] -> target_k/target_v fp64 [H_kv][d][d] (device)."""
+    import torch
+    n, h_q, d = q_cal.shape
+    m, h_kv = k_cal.shape[0], k_cal.shape[1]
+    _check(lib().oscar_calibration_targets(
+        _dptr(q_cal, torch.float32, "q_cal"), _dptr(k_cal, torch.float32, "k_cal"),
+        _dptr(v_cal, torch.float32, "v_cal"), n, m, h_q, h_kv, d, float(sm_scale),
+        _dptr(target_k, torch.float64, "target_k"), _dptr(target_v, torch.float64, "target_v"),
+        _dptr(workspace, None, "workspace"), workspace.numel() * workspace.element_size(), _stream(stream)),
+        "oscar_calibration_targets")
 
 
 def oscar_decode_static_workspace(ctx, layer, q, int2_pool, int2_tables, hist_len, max_hist, bf16_pool,

@@ -243,6 +243,29 @@ OSCAR_API oscar_status oscar_decode_static_workspace(oscar_ctx_t* ctx, int layer
                                                      const int32_t* bf16_len, float* out, int batch, void* stream);
 
 /* Bytes of one INT2 page (all heads, K and V) and of one BF16 page. */
+/* Offline calibration targets on the GPU ([QBIT] section "OSCAR aligns the
+ * rotation with attention": per layer and per head, the key target Q^T Q and
+ * the score-weighted value target V^T S^T S V, estimated from a few
+ * calibration samples). The host then takes their eigenvectors U and forms
+ * R = U H P and the clip thresholds. This call needs no context.
+ *   q_cal:    DEVICE fp32 [n][H_q][d] calibration queries.
+ *   k_cal, v_cal: DEVICE fp32 [m][H_kv][d] calibration keys and values.
+ *   target_k, target_v: DEVICE fp64 [H_kv][d][d], written. For KV head h, the
+ *             key target stacks the queries of its H_q/H_kv query heads as
+ *             rows (n * H_q/H_kv rows). S is the row-wise softmax of
+ *             sm_scale * Q K^T over the m keys of head h, with no mask, and
+ *             the value target is (S V)^T (S V).
+ *   workspace: DEVICE, >= oscar_calibration_workspace_size(n, H_q, H_kv, d)
+ *             bytes, 256-byte aligned (the rows of S V, fp64).
+ * Supported: d in {64, 128}; H_q a multiple of H_kv; n >= 1; 1 <= m <= 8192.
+ * Other sizes return OSCAR_ERR_UNSUPPORTED or OSCAR_ERR_INVALID_ARG before
+ * anything is launched. Asynchronous on `stream`. All arithmetic is fp64. */
+OSCAR_API size_t oscar_calibration_workspace_size(int n, int n_q_heads, int n_kv_heads, int head_dim);
+OSCAR_API oscar_status oscar_calibration_targets(const float* q_cal, const float* k_cal, const float* v_cal,
+                                                 int n, int m, int n_q_heads, int n_kv_heads, int head_dim,
+                                                 double sm_scale, double* target_k, double* target_v,
+                                                 void* workspace, size_t workspace_bytes, void* stream);
+
 OSCAR_API size_t oscar_int2_page_bytes(const oscar_ctx_t* ctx);
 OSCAR_API size_t oscar_bf16_page_bytes(const oscar_ctx_t* ctx);
 
