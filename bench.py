@@ -169,15 +169,29 @@ class GpuWorkload:
         max_pages = max(pages)
         self.ctx = O.Oscar(n_layers=layers, n_q_heads=h_q, n_kv_heads=h_kv, head_dim=d, group=group)
         pb = self.ctx.int2_page_bytes()
-        bf_pages = 4 + (recent // P) * B                     # shared sink pages + recent pages per sequence
+        # the sink pages belong to the shared prefix when there is one; otherwise every sequence owns its sink
+        self.shared_sink = shared_hist > 0
+        sink_pages = sink // P
+        bf_pages = (sink_pages if self.shared_sink else sink_pages * B) + (recent // P) * B
         gen = torch.Generator(device=dev)
         self.int2_pools, self.bf16_pools, self.tables, self.qs = [], [], [], []
+        self.calib = []                                      # fp32 (R_k, R_v) per layer, as uploaded
+        laplace = cfg["dist"] == "laplace"
+
+        def rows(n):
+            if not laplace:
+                return torch.randn(n, h_kv, d, generator=gen, device=dev)
+            # Laplace(0, 1) by inversion of a uniform draw: -sign(u) log(1 - 2|u|), u in (-1/2, 1/2)
+            u = torch.rand(n, h_kv, d, generator=gen, device=dev) - 0.5
+            return -torch.sign(u) * torch.log1p(-2.0 * u.abs().clamp(max=0.5 - 2.0 ** -25))
+
         chunk = 16384
         for layer in range(layers):
             li = synth.LayerInputs(cfg, layer + seed_offset)
             q_cal, k_cal, v_cal = li.calibration()
             rk, rv, tk, tv = calibration.calibrate_layer(q_cal, k_cal, v_cal, d ** -0.5, cfg["clip_ratio"])
             self.ctx.calibrate_upload(layer, rk, rv, tk, tv)
+            self.calib.append((np.asarray(rk, np.float32), np.asarray(rv, np.float32)))
             perm = synth.page_permutation(li.seed, "int2", total).astype(np.int64)
             table = np.zeros((B, max_pages), np.int32)
             spare = np.zeros(B, np.int64)
@@ -198,28 +212,32 @@ class GpuWorkload:
             for i, t_lo, t_hi in ranges:
                 for t0 in range(t_lo, t_hi, chunk):
                     n = min(chunk, t_hi - t0)
-                    k = (torch.randn(n, h_kv, d, generator=gen, device=dev) * km).to(torch.bfloat16)
-                    v = (torch.randn(n, h_kv, d, generator=gen, device=dev) * vm).to(torch.bfloat16)
+                    k = (rows(n) * km).to(torch.bfloat16)
+                    v = (rows(n) * vm).to(torch.bfloat16)
                     t = torch.arange(t0, t0 + n, device=dev)
                     slots = table_d[i, t // P].to(torch.int64) * P + t % P
                     self.ctx.write_tokens(layer, k, v, slots, pool)
-            bf = torch.randn(bf_pages, h_kv, 2, P, d, generator=gen, device=dev)
+            bf = torch.stack([rows(bf_pages * P).view(bf_pages, P, h_kv, d).transpose(1, 2) for _ in range(2)], 2)
             bf = bf * torch.stack([km, vm], dim=1)[None, :, :, None, :]
             self.bf16_pools.append(bf.to(torch.bfloat16).contiguous())
             self.int2_pools.append(pool)
             self.tables.append(table_d)
             self.qs.append(torch.randn(B, h_q, d, generator=gen, device=dev).to(torch.bfloat16))
         bt = np.zeros((B, self.n_bf16 // P), np.int32)
+        per_seq = (recent // P) + (0 if self.shared_sink else sink_pages)
+        first_own = sink_pages if self.shared_sink else 0
         for i in range(B):
-            bt[i, :4] = np.arange(4)
-            bt[i, 4:] = 4 + (recent // P) * i + np.arange(recent // P)
+            if self.shared_sink:
+                bt[i, :sink_pages] = np.arange(sink_pages)
+            bt[i, first_own:] = first_own + per_seq * i + np.arange(per_seq)
+        self.bf16_table_np = bt
         self.bf16_table = torch.from_numpy(bt).to(dev)
         self.hist_len = torch.from_numpy(hist.astype(np.int32)).to(dev)
         self.bf16_len = torch.full((B,), self.n_bf16, dtype=torch.int32, device=dev)
         # demote: each sequence's oldest recent token (row 0 of its first recent page) -> row 0 of
         # its spare INT2 page (same spare page ids in every layer's pool: the permutation per layer
         # differs, so the spare ids are taken per layer below)
-        self.src = torch.from_numpy((bt[:, 4].astype(np.int64)) * P).to(dev)
+        self.src = torch.from_numpy((bt[:, sink_pages].astype(np.int64)) * P).to(dev)
         self.dsts = []
         for layer in range(layers):
             li = synth.LayerInputs(cfg, layer + seed_offset)
@@ -233,7 +251,8 @@ class GpuWorkload:
         # bytes and tokens of one decode of one layer
         self.tokens_per_layer = int(hist.sum()) + B * self.n_bf16
         self.logical_bytes = token_bytes(cfg, int(hist.sum()), B * self.n_bf16)
-        self.unique_bytes = token_bytes(cfg, shared_hist + int((hist - shared_hist).sum()), sink + B * recent)
+        self.unique_bytes = token_bytes(cfg, shared_hist + int((hist - shared_hist).sum()),
+                                        (sink if self.shared_sink else sink * B) + B * recent)
         torch.cuda.synchronize()
 
     def step(self):
@@ -253,7 +272,6 @@ class GpuWorkload:
                             self.out[layer], self.ws)
         main.wait_stream(self.side)
 
-    launches_per_step_per_layer = 4     # write (demote), q rotation, split, merge
 
 
 def write_bytes(cfg, n):
@@ -411,6 +429,87 @@ def run_reference(args, cfg, world, rank):
 
 # --------------------------------------------------------------------------- main
 
+def measure_decode(cfg, layers, dev, steps, warmup, local, seed_offset=0):
+    """Build a workload's caches, capture one step in a CUDA graph and time K replays (max over ranks).
+
+    Returns (workload, graph, metrics). The metrics hold the step time, per-kernel CUDA-event averages
+    from an eager pass of the same launches, and the split kernel's achieved GB/s on unique bytes."""
+    import torch
+    from bit_kv_cache_write_gb300 import oscar as O
+    wl = GpuWorkload(cfg, layers, dev, seed_offset=seed_offset)
+    stream = torch.cuda.current_stream()
+
+    # ---- capture one step in a CUDA graph (the library launches on the capturing stream)
+    wl.step()
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        wl.step()
+    for _ in range(warmup):
+        graph.replay()
+    torch.cuda.synchronize()
+
+    # ---- timed region: K graph replays; every step reads more distinct pages than L2 holds
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clocks:
+        barrier()
+        torch.cuda.synchronize()
+        start.record(stream)
+        for _ in range(steps):
+            graph.replay()
+        stop.record(stream)
+        torch.cuda.synchronize()
+        barrier()
+    sec = start.elapsed_time(stop) / 1e3
+    max_sec = max_over_ranks(sec, dev)
+
+    # ---- per-kernel durations (same launches, eager, events around each kernel on its stream)
+    wl.ctx.profile_enable(True)
+    for _ in range(steps):
+        wl.step()
+    torch.cuda.synchronize()
+    wl.ctx.profile_enable(False)
+    kt = {}
+    for name, kid in (("write", O.OSCAR_KERNEL_WRITE), ("q_rotate", O.OSCAR_KERNEL_QROT),
+                      ("split", O.OSCAR_KERNEL_SPLIT), ("merge", O.OSCAR_KERNEL_MERGE)):
+        ms, n = wl.ctx.profile_read(kid)
+        kt[name] = {"launches": n, "avg_us": 1e3 * ms / max(n, 1)}
+    # roofline on unique bytes (a page shared by several tables counts once: conservative)
+    split_bytes = wl.unique_bytes
+    achieved = split_bytes / (kt["split"]["avg_us"] * 1e-6) / 1e9
+    launches = sum(v["launches"] for v in kt.values()) // max(steps, 1)
+    return wl, graph, {"max_sec": max_sec, "kernels": kt, "clocks": clocks.summary(), "achieved": achieved,
+                       "split_bytes": split_bytes, "launches_per_step": launches}
+
+
+def workload_line(name, layers, dev, steps, warmup, local):
+    """Throughput of one more decode workload at a reduced layer count (its per-layer pages exceed L2)."""
+    import torch
+    cfg = workload_cfg(name)
+    wl, graph, m = measure_decode(cfg, layers, dev, steps, warmup, local)
+    peak, peak_kind = measured_peak()
+    us_layer = 1e6 * m["max_sec"] / steps / layers
+    split_us = m["kernels"]["split"]["avg_us"]
+    res = {"layers": layers, "batch": wl.batch, "h_q": cfg["h_q"], "h_kv": cfg["h_kv"], "group": cfg["group"],
+           "int2_history": {"min": int(wl.hist.min()), "max": int(wl.hist.max()), "sum": int(wl.hist.sum())},
+           "shared_prefix_int2_tokens": wl.shared_hist,
+           "us_per_layer": us_layer, "kv_tokens_per_s": wl.tokens_per_layer / (us_layer * 1e-6),
+           "kernels": m["kernels"],
+           "split_roofline": {"bound": "hbm", "achieved": m["achieved"], "peak": peak, "peak_kind": peak_kind,
+                              "unit": "GB/s", "frac": m["achieved"] / peak,
+                              "algorithmic_bytes_per_launch": wl.unique_bytes,
+                              "logical_bytes_per_launch": wl.logical_bytes,
+                              "logical_gbs": wl.logical_bytes / (split_us * 1e-6) / 1e9,
+                              "traffic": kernel_traffic("split", name)},
+           "step_gbs": (wl.unique_bytes + demote_bytes(cfg, wl.batch)) / (us_layer * 1e-6) / 1e9,
+           "clocks": m["clocks"],
+           "l2": "inputs larger than L2: %.2f GB of distinct pages per step" % (layers * wl.unique_bytes / 1e9)}
+    del graph, wl
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return res
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -423,6 +522,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-write", action="store_true", help="skip the bulk-write / demote measurement")
     ap.add_argument("--only-write", action="store_true", help="print only the bulk-write / demote measurement")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="skip the batch-64 and mixed-batch decode workloads (measured at N = 1 only)")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
 
@@ -448,51 +549,14 @@ def main():
         return 0
 
     layers = args.layers or cfg["layers"]
-    wl = GpuWorkload(cfg, layers, dev, seed_offset=1000 * rank)
+    wl, graph, m = measure_decode(cfg, layers, dev, args.steps, args.warmup, local, seed_offset=1000 * rank)
     stream = torch.cuda.current_stream()
-
-    # ---- capture one step in a CUDA graph (the library launches on the capturing stream)
-    wl.step()
-    torch.cuda.synchronize()
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph):
-        wl.step()
-    for _ in range(args.warmup):
-        graph.replay()
-    torch.cuda.synchronize()
-
-    # ---- timed region: K graph replays; inputs (2.1 GB of pages over the layers) exceed L2
-    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with ClockSampler(local) as clocks:
-        barrier()
-        torch.cuda.synchronize()
-        start.record(stream)
-        for _ in range(args.steps):
-            graph.replay()
-        stop.record(stream)
-        torch.cuda.synchronize()
-        barrier()
-    sec = start.elapsed_time(stop) / 1e3
-    max_sec = max_over_ranks(sec, dev)
+    max_sec = m["max_sec"]
     tokens_per_step = layers * wl.tokens_per_layer
     value = whole_job_rate(tokens_per_step * args.steps, world, max_sec)
     ms_per_step = 1e3 * max_sec / args.steps
     step_bytes = layers * (wl.unique_bytes + demote_bytes(cfg, wl.batch))
-
-    # ---- per-kernel durations (same launches, eager, events around each kernel on its stream)
-    wl.ctx.profile_enable(True)
-    for _ in range(args.steps):
-        wl.step()
-    torch.cuda.synchronize()
-    wl.ctx.profile_enable(False)
-    kt = {}
-    for name, kid in (("write", O.OSCAR_KERNEL_WRITE), ("q_rotate", O.OSCAR_KERNEL_QROT),
-                      ("split", O.OSCAR_KERNEL_SPLIT), ("merge", O.OSCAR_KERNEL_MERGE)):
-        ms, n = wl.ctx.profile_read(kid)
-        kt[name] = {"launches": n, "avg_us": 1e3 * ms / max(n, 1)}
-    # roofline on unique bytes (a page shared by several tables counts once: conservative)
-    split_bytes = wl.unique_bytes
-    achieved = split_bytes / (kt["split"]["avg_us"] * 1e-6) / 1e9
+    kt, clocks, achieved, split_bytes = m["kernels"], m["clocks"], m["achieved"], m["split_bytes"]
     peak, peak_kind = measured_peak()
 
     # ---- end to end through the public API with host buffers: q in (pinned H2D), outputs out (D2H)
@@ -530,6 +594,13 @@ def main():
 
     write = bench_write(dev, max(args.steps, 5), args.warmup) if rank == 0 and not args.no_write else None
 
+    # ---- the batched and mixed-length decode workloads (N = 1), at layer counts whose pages exceed L2
+    workloads = None
+    if world == 1 and not args.no_workloads:
+        workloads = {"qwen3_4b_b64_32k": workload_line("qwen3_4b_b64_32k", 2, dev, args.steps, args.warmup, local),
+                     "qwen3_32b_mixed16": workload_line("qwen3_32b_mixed16", 4, dev, args.steps, args.warmup,
+                                                        local)}
+
     if rank == 0:
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -554,12 +625,13 @@ def main():
                          "algorithmic_bytes_per_launch": split_bytes,
                          "logical_bytes_per_launch": wl.logical_bytes},
             "kernels": kt,
-            "clocks": clocks.summary(),
+            "clocks": clocks,
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": q_host.numel() * 2,
                     "d2h_bytes_per_step": out_host.numel() * 4},
-            "gpu_launches": args.steps * layers * GpuWorkload.launches_per_step_per_layer,
+            "gpu_launches": args.steps * m["launches_per_step"],
             "cpu_baseline": cpu_baseline,
             "write": write,
+            "workloads": workloads,
         }
         print(json.dumps(line))
     if world > 1:

@@ -41,13 +41,24 @@ size_t layer_floats(const oscar::Shape& s) {
     return 3 * (size_t)s.h_kv * s.d * s.d + 2 * (size_t)s.h_kv * s.d + (size_t)s.h_kv;
 }
 
+// The context's buffers live on the device that was current at oscar_create; launches go to the
+// current device, so the two must agree.
+oscar_status check_device(const oscar_ctx_t* ctx) {
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev != ctx->device)
+        return fail(OSCAR_ERR_INVALID_ARG, "current device %d is not the context's device %d", dev, ctx->device);
+    return OSCAR_OK;
+}
+
 oscar_status check_ctx_layer(const oscar_ctx_t* ctx, int layer) {
     if (!ctx) return fail(OSCAR_ERR_INVALID_ARG, "ctx is NULL");
     if (layer < 0 || layer >= ctx->cfg.n_layers)
         return fail(OSCAR_ERR_INVALID_ARG, "layer %d outside [0, %d)", layer, ctx->cfg.n_layers);
     if (!ctx->calibrated[layer])
         return fail(OSCAR_ERR_NOT_CALIBRATED, "layer %d has no uploaded calibration", layer);
-    return OSCAR_OK;
+    return check_device(ctx);
 }
 
 }  // namespace
@@ -182,6 +193,7 @@ oscar_status oscar_calibrate_upload(oscar_ctx_t* ctx, int layer, const float* R_
     if (layer < 0 || layer >= ctx->cfg.n_layers)
         return fail(OSCAR_ERR_INVALID_ARG, "layer %d outside [0, %d)", layer, ctx->cfg.n_layers);
     if (!R_k || !R_v || !T_k || !T_v) return fail(OSCAR_ERR_INVALID_ARG, "calibration pointer is NULL");
+    if (oscar_status dst = check_device(ctx); dst != OSCAR_OK) return dst;
     const oscar::Shape& s = ctx->shape;
     const size_t hdd = (size_t)s.h_kv * s.d * s.d, hd = (size_t)s.h_kv * s.d;
     for (size_t i = 0; i < hdd; ++i)
@@ -265,7 +277,7 @@ oscar_status oscar_demote_recent(oscar_ctx_t* ctx, int layer, const void* bf16_p
 }
 
 size_t oscar_decode_workspace_size(const oscar_ctx_t* ctx, int batch, int max_hist) {
-    if (!ctx || batch < 0 || max_hist < 0) return 0;
+    if (!ctx || batch < 0 || batch > oscar::kMaxBatch || max_hist < 0) return 0;
     return oscar::plan_decode(ctx->shape, ctx->num_sms, batch, max_hist).ws_total;
 }
 
@@ -282,7 +294,8 @@ oscar_status oscar_decode(oscar_ctx_t* ctx, int layer, const void* q,
     if (st != OSCAR_OK) return st;
     if (batch < 0 || max_hist < 0) return fail(OSCAR_ERR_INVALID_ARG, "batch %d / max_hist %d negative", batch, max_hist);
     if (batch == 0) return OSCAR_OK;
-    if (batch > 65535) return fail(OSCAR_ERR_UNSUPPORTED, "batch %d above 65535 (one grid dimension per sequence)", batch);
+    if (batch > oscar::kMaxBatch)
+        return fail(OSCAR_ERR_UNSUPPORTED, "batch %d above %d (one grid dimension per sequence)", batch, oscar::kMaxBatch);
     if (!q || !out || !hist_len || !bf16_len) return fail(OSCAR_ERR_INVALID_ARG, "device pointer is NULL");
     if (max_hist > 0 && (!int2_pool || !int2_tables || int2_table_stride <= 0 || int2_pool_pages <= 0))
         return fail(OSCAR_ERR_INVALID_ARG, "INT2 pool/tables missing while max_hist = %d", max_hist);

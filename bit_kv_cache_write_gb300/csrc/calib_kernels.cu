@@ -142,8 +142,7 @@ cudaError_t launch_calibration_targets(const float* q, const float* k, const flo
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     const size_t smem = (size_t)(m + d) * sizeof(double);
-    static cudaError_t attr =
-        cudaFuncSetAttribute(sv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kCalibMaxSmem);
+    const cudaError_t attr = smem_opt_in<sv_kernel>(kCalibMaxSmem);
     if (attr != cudaSuccess) return attr;
     sv_kernel<<<dim3(rows, h_kv), d, smem, st>>>(q, k, v, rows, m, g, h_q, h_kv, d, sm_scale, sv_rows);
     e = cudaGetLastError();

@@ -1011,7 +1011,7 @@ template <int D, int G, int GQ>
 cudaError_t launch_split(const SplitArgs& a, int batch, cudaStream_t st) {
     auto kern = split_kernel<D, G, GQ>;
     const size_t smem = SplitSmem<D, G, GQ>::kDynamic;
-    static cudaError_t attr = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    const cudaError_t attr = smem_opt_in<split_kernel<D, G, GQ>>(smem);
     if (attr != cudaSuccess) return attr;
     dim3 grid(a.total_splits, a.h_kv, batch);
     return launch_pdl(kern, grid, dim3(kWarps * 32), smem, st, a);
@@ -1047,21 +1047,26 @@ cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t sme
     return cudaLaunchKernelEx(&cfg, kern, args...);
 }
 
-// Resident split CTAs per SM for the shape (queried once per instantiation).
+// Resident split CTAs per SM for the shape on the current device (queried once per device).
 template <int D, int G, int GQ>
 int split_occupancy() {
-    static int occ = [] {
-        int n = 0;
-        auto kern = split_kernel<D, G, GQ>;
-        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SplitSmem<D, G, GQ>::kDynamic);
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, kWarps * 32, SplitSmem<D, G, GQ>::kDynamic) !=
+    static std::atomic<int> occ[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) dev = 64;
+    if (dev < 64) {
+        const int cached = occ[dev].load(std::memory_order_acquire);
+        if (cached > 0) return cached;
+    }
+    int n = 0;
+    auto kern = split_kernel<D, G, GQ>;
+    if (smem_opt_in<split_kernel<D, G, GQ>>(SplitSmem<D, G, GQ>::kDynamic) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, kWarps * 32, SplitSmem<D, G, GQ>::kDynamic) !=
             cudaSuccess || n < 1) {
-            cudaGetLastError();
-            n = 1;
-        }
-        return n;
-    }();
-    return occ;
+        cudaGetLastError();
+        n = 1;
+    }
+    if (dev < 64) occ[dev].store(n, std::memory_order_release);
+    return n;
 }
 
 template <int D, int G>
@@ -1087,7 +1092,8 @@ int split_ctas_per_sm(const Shape& s) {
 DecodePlan plan_decode(const Shape& s, int num_sms, int batch, int max_hist) {
     DecodePlan p{};
     const int max_pages = (max_hist + kPage - 1) / kPage;
-    const int units = batch * s.h_kv;
+    const long long units_ll = (long long)batch * s.h_kv;     // batch <= 65535 is checked by every caller
+    const int units = units_ll > (1 << 30) ? (1 << 30) : (int)units_ll;
     // one wave of units * (INT2 splits + 1 BF16 split) resident CTAs when that keeps splits short
     // (few units: bs1 decode); otherwise at most kMaxPagesPerSplit pages per split, in as many
     // waves as that takes (many units or long sequences)

@@ -53,15 +53,24 @@ extern "C" oscar_status oscar_decode_static_workspace(
     const void* bf16_pool, int64_t bf16_pool_pages, const int32_t* bf16_tables, int bf16_table_stride,
     const int32_t* bf16_len, float* out, int batch, void* stream) {
     if (!ctx) return oscar::record_failure(OSCAR_ERR_INVALID_ARG, "ctx is NULL");
+    if (batch < 0 || max_hist < 0)
+        return oscar::record_failure(OSCAR_ERR_INVALID_ARG, "batch %d / max_hist %d negative", batch, max_hist);
+    if (batch > oscar::kMaxBatch)
+        return oscar::record_failure(OSCAR_ERR_UNSUPPORTED, "batch %d above %d (one grid dimension per sequence)",
+                                     batch, oscar::kMaxBatch);
+    // the array's address is the one of the context's device, which must be the current device
+    int device = 0;
+    cudaError_t e = cudaGetDevice(&device);
+    if (e != cudaSuccess) return oscar::record_failure(OSCAR_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+    if (device != ctx->device)
+        return oscar::record_failure(OSCAR_ERR_INVALID_ARG, "current device %d is not the context's device %d",
+                                     device, ctx->device);
     const size_t need = oscar_decode_workspace_size(ctx, batch, max_hist);
     if (need > kStaticWorkspaceBytes)
         return oscar::record_failure(OSCAR_ERR_WORKSPACE,
                                      "batch %d with max_hist %d needs %zu workspace bytes; the static workspace "
                                      "holds %zu: use oscar_decode with a caller workspace",
                                      batch, max_hist, need, kStaticWorkspaceBytes);
-    int device = 0;
-    cudaError_t e = cudaGetDevice(&device);
-    if (e != cudaSuccess) return oscar::record_failure(OSCAR_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
     void* ws = nullptr;
     oscar_status st = static_workspace(device, &ws);
     if (st != OSCAR_OK) return st;

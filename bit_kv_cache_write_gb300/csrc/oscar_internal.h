@@ -2,6 +2,7 @@
 #pragma once
 
 #include <cuda_runtime.h>
+#include <atomic>
 #include <cstdint>
 #include <vector>
 
@@ -11,10 +12,27 @@ namespace oscar {
 
 constexpr int kPage = 16;
 constexpr int kMaxBf16 = 512;     // sink + recent upper bound
+constexpr int kMaxBatch = 65535;  // sequences per decode call (one grid dimension per sequence)
 constexpr float kLog2e = 1.4426950408889634f;
 // The INT2 decode raises its running softmax max only when a logit passes it by more than
 // 2^kSoftmaxHeadroomLog2 (log2 units), so weights stay at or below 2^8 between rescales.
 constexpr int kSoftmaxHeadroomLog2 = 8;
+
+// Opts kernel Kern into `bytes` of dynamic shared memory on the current device. The CUDA
+// runtime applies the attribute per device, so it is set once for each device that launches
+// the kernel (devices 0..63; a higher ordinal sets it on every call).
+template <auto Kern>
+cudaError_t smem_opt_in(size_t bytes) {
+    static std::atomic<unsigned long long> done{0};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const unsigned long long bit = (dev >= 0 && dev < 64) ? (1ull << dev) : 0ull;
+    if (bit && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
+    e = cudaFuncSetAttribute(Kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+    if (e == cudaSuccess && bit) done.fetch_or(bit, std::memory_order_acq_rel);
+    return e;
+}
 
 // Per-layer device parameters. All pointers index into one allocation.
 struct LayerParams {

@@ -315,9 +315,9 @@ cudaError_t launch_write_tok(const Shape& s, const LayerParams& p, int num_sms,
                              cudaStream_t st) {
     const size_t smem = (size_t)(D * D + kWarps * kTok * D) * sizeof(float);
     auto kern = write_kernel<D, G, kTok>;
-    // Opt in to the large dynamic shared memory once per process (outside any stream capture:
-    // the first call of a shape happens before a caller can capture it).
-    static cudaError_t attr = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    // Opt in to the large dynamic shared memory once per device (outside any stream capture: the
+    // first call of a shape on a device happens before a caller can capture it).
+    const cudaError_t attr = smem_opt_in<write_kernel<D, G, kTok>>(smem);
     if (attr != cudaSuccess) return attr;
     // K and V rotations/thresholds sit back to back: r_k then r_v, t_k then t_v.
     const int pairs = s.h_kv * 2;

@@ -885,7 +885,7 @@ cudaError_t launch_tc(const Shape& s, const LayerParams& p, int num_sms, const v
                       Profiler* prof, cudaStream_t st) {
     using L = TcLayout<D>;
     auto kern = write_tc_kernel<D, G>;
-    static cudaError_t attr = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L::kDynamic);
+    const cudaError_t attr = smem_opt_in<write_tc_kernel<D, G>>(L::kDynamic);
     if (attr != cudaSuccess) return attr;
     CUtensorMap mk, mv;
     if (!make_row_map(&mk, k, n, s.h_kv, D) || !make_row_map(&mv, v, n, s.h_kv, D)) return cudaErrorInvalidValue;

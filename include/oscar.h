@@ -73,6 +73,9 @@
  * - `stream` is a cudaStream_t passed as void*; NULL is the legacy default
  *   stream. Every launch call is asynchronous on that stream. Except where
  *   stated, no call synchronizes.
+ * - A context belongs to the device that was current at oscar_create. Every
+ *   call that takes a context must be made with that device current; on any
+ *   other device it returns OSCAR_ERR_INVALID_ARG before launching anything.
  * - Host-side validation runs before any launch. A failing call has launched
  *   nothing and returns a negative oscar_status. A launch failure returns
  *   OSCAR_ERR_CUDA. oscar_last_error() gives a one-line message for the
@@ -183,7 +186,8 @@ OSCAR_API oscar_status oscar_demote_recent(oscar_ctx_t* ctx, int layer,
                                  const int64_t* dst_slots, int n, void* stream);
 
 /* Bytes of device workspace oscar_decode needs for `batch` sequences whose
- * INT2 history holds at most max_hist tokens. Returns 0 on bad arguments. */
+ * INT2 history holds at most max_hist tokens. Returns 0 on bad arguments
+ * (NULL ctx, negative sizes, batch above 65535). */
 OSCAR_API size_t oscar_decode_workspace_size(const oscar_ctx_t* ctx, int batch, int max_hist);
 
 /* Paged decode attention for one layer ([QBIT] serving pipeline, decode: INT2
