@@ -38,7 +38,7 @@ bool fault(const char* what) {
 bool pow2_in(int v, int lo, int hi) { return v >= lo && v <= hi && (v & (v - 1)) == 0; }
 
 size_t layer_floats(const oscar::Shape& s) {
-    return 3 * (size_t)s.h_kv * s.d * s.d + 2 * (size_t)s.h_kv * s.d + (size_t)s.h_kv;
+    return 3 * (size_t)s.h_kv * s.d * s.d + 2 * (size_t)s.h_kv * s.d + 2 * (size_t)s.h_kv;
 }
 
 // The context's buffers live on the device that was current at oscar_create; launches go to the
@@ -84,6 +84,7 @@ LayerParams layer_params(const oscar_ctx* ctx, int layer) {
     p.t_k = base + 3 * hdd;
     p.t_v = base + 3 * hdd + hd;
     p.pv_scale = base + 3 * hdd + 2 * hd;
+    p.rk_colmax = base + 3 * hdd + 2 * hd + s.h_kv;
     p.r_img = ctx->r_img + layer * ctx->r_img_elems;
     p.r_kt = ctx->r_kt + layer * hdd;
     return p;
@@ -226,8 +227,23 @@ oscar_status oscar_calibrate_upload(oscar_ctx_t* ctx, int layer, const float* R_
         sigma = std::min(40, std::max(-40, sigma));
         pvs[h] = std::ldexp(1.0f, sigma);
     }
+    // Per KV head, an upper bound of the largest column norm of R_k: |(q R_k)_c| <= |q| * max_c |R_k[:, c]|
+    // bounds every rotated query channel, which fixes the query digits' common exponent without a
+    // cross-channel maximum.
+    for (int h = 0; h < s.h_kv; ++h) {
+        double cmax = 0.0;
+        for (int c = 0; c < s.d; ++c) {
+            double n2 = 0.0;
+            for (int i = 0; i < s.d; ++i) {
+                const double r = R_k[((size_t)h * s.d + i) * s.d + c];
+                n2 += r * r;
+            }
+            cmax = std::max(cmax, std::sqrt(n2));
+        }
+        pvs.push_back((float)(cmax * (1.0 + 1e-6)) + 1e-30f);
+    }
     if (e == cudaSuccess)
-        e = cudaMemcpyAsync(const_cast<float*>(p.pv_scale), pvs.data(), s.h_kv * sizeof(float),
+        e = cudaMemcpyAsync(const_cast<float*>(p.pv_scale), pvs.data(), 2 * s.h_kv * sizeof(float),
                             cudaMemcpyHostToDevice, st);
     // bf16 pieces of R_k and R_v as tensor-core operand images for the bulk write
     std::vector<uint16_t> img(ctx->r_img_elems);

@@ -6,10 +6,13 @@
 // combines the two. arXiv 2605.17757 abstracts: the kernels keep the paged
 // KV-cache layout and prefix caching (block tables may share pages).
 //
-// Three launches per layer:
+// Two or three launches per layer:
 //   1. q_prep: q_rot = q @ R_k for every query head, accumulated as two fp32
-//      (about 48 bits). It is split into three fp16 tensor-core operands on
-//      nested fixed-point grids. Also per-group sums of q_rot.
+//      (about 48 bits), one CTA per 32 rotated channels. It is cut into three
+//      11-bit fp16 tensor-core operands on a fixed-point grid whose exponent
+//      comes from a bound (|q| times the largest column norm of R_k), so the
+//      CTAs of one head agree on it without exchanging a maximum. Each CTA
+//      also writes the exact digit sums of its channels.
 //   2. split: one CTA per (split, KV head, sequence).
 //      - INT2 splits stream page blocks into shared memory with bulk async
 //        copies, four stages per warp. They compute q_rot . codes and
@@ -20,19 +23,22 @@
 //      - Each split writes a partial (m, l, acc[d]) per query head of the
 //        group, with m in log2 units.
 //   3. merge: combines the splits of each query head, un-rotates the INT2
-//      accumulator by R_v^T and normalises. When that merge is short
-//      (g x splits <= 128, i.e. large batches) the CTA of the split kernel that
-//      finishes a (sequence, KV head) last does it instead, and there are two
-//      launches per layer.
-//
+//      accumulator by R_v^T and normalises. Its R_v^T terms load before it
+//      waits for the split kernel. When that merge is short (g x splits <=
+//      128, i.e. large batches in several waves) the CTA of the split kernel
+//      that finishes a (sequence, KV head) last does it instead, found by an
+//      atomic ticket (zeroed by q_prep; nothing waits on another CTA), and
+//      there are two launches per layer.
+
 // Exactness of the INT2 logits. With codes c in {0..3}, scale s and zero z per
 // group:
 //   q . (c*s + z) = s * (q . c) + z * sum(q).
 // q . c is computed exactly: every q part is an 11-bit integer on a power-of-two
 // grid, so each tensor-core partial sum is an exactly representable fp32. s and
-// z then enter through error-free products. The logit is carried as hi + lo
-// into the softmax exponent, so INT2 logits keep about 1e-7 absolute accuracy
-// even where they are ~30 in log2 units.
+// z then enter through error-free products. The logit is carried as hi + lo into
+// the softmax exponent, so
+// INT2 logits keep about 1e-7 absolute accuracy even where they are ~30 in log2
+// units.
 //
 // Unpacking. A packed code pair at bit position p of a 32-bit word becomes an
 // fp16 (sub)normal c * 2^(2p-24) with a single mask (positions 5..7 after one
@@ -41,6 +47,7 @@
 
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+#include <atomic>
 #include <cfloat>
 #include <cmath>
 #include <type_traits>
@@ -58,7 +65,8 @@ constexpr float kNoMax = -1e30f;                   // running max before any tok
 constexpr int kMaxPagesPerSplit = 128;             // longest INT2 split when the grid has many waves
 // last-CTA merge only for short merges (one CTA walks GQ * splits partial rows): large batches;
 // bs1 decodes with ~80 splits keep the wider merge kernel
-constexpr size_t kFuseWeights = 128;
+constexpr int kFuseWeights = 128;
+constexpr int kSliceCh = 32;                       // rotated channels per q_prep CTA
 
 __device__ __forceinline__ float fast_exp2(float x) { return exp2f(x); }
 
@@ -86,6 +94,15 @@ __device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1
 // c_lo * 2^(2p'-24) in the low half, c_hi * 2^(2p'-24) in the high half.
 __host__ __device__ constexpr int pos_scale(int pos) { return pos <= 4 ? pos : pos - 5; }
 
+// 2^(-2 p'(pos)): undoes the code position's power of two in the P.V output.
+__host__ __device__ constexpr float pos_weight(int pos) {
+    return pos_scale(pos) == 0 ? 1.0f
+         : pos_scale(pos) == 1 ? 0x1p-2f
+         : pos_scale(pos) == 2 ? 0x1p-4f
+         : pos_scale(pos) == 3 ? 0x1p-6f
+                               : 0x1p-8f;
+}
+
 template <int POS>
 __device__ __forceinline__ uint32_t code_pair(uint32_t w, uint32_t w10) {
     if constexpr (POS <= 4) return w & (0x00030003u << (2 * POS));
@@ -104,12 +121,6 @@ __device__ __forceinline__ uint32_t code_pair_normal(uint32_t w, uint32_t w10) {
 
 __device__ __forceinline__ uint32_t pack_half2(__half lo, __half hi) {
     return (uint32_t)__half_as_ushort(lo) | ((uint32_t)__half_as_ushort(hi) << 16);
-}
-
-// hi or lo fp16 part of x: hi = fp16(x), lo = fp16((x - hi) * 2^11).
-__device__ __forceinline__ __half split_part(float x, bool lo) {
-    const __half h = __float2half_rn(x);
-    return lo ? __float2half_rn(__fmul_rn(__fsub_rn(x, __half2float(h)), 2048.0f)) : h;
 }
 
 // Programmatic dependent launch: wait for the preceding grid in the stream (a no-op without the
@@ -152,41 +163,56 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t phase) {
 // Query preparation
 // ---------------------------------------------------------------------------------------------
 
-// Per query head (one block of D threads):
-//   q_rot[c] = sum_i q_i R[i][c] as hi + lo fp32 (error-free products and sums);
-//   E with max|q_rot| < 2^E; r_hi, r_mid, r_lo integers (|r| <= 2048) with
+// One CTA of 128 threads per (query head, slice of 32 rotated channels): thread (channel, quarter)
+// accumulates D/4 terms of the dot product.
+//   q_rot[c] = sum_i q_i R[i][c] as hi + lo fp32 (error-free products and sums), times
+//     sm_scale * log2(e), so the INT2 logits come out in log2 units;
+//   E with 2^E > sm_scale log2(e) |q|_2 max_c |R[:, c]|_2 >= max_c |q_rot[c]| (the same in
+//     every CTA of the head: every CTA sums |q|^2 in the same order);
+//   r_hi, r_mid, r_lo integers (|r| <= 2048) with
 //     q_rot = (r_hi + r_mid 2^-11 + r_lo 2^-22) 2^(E-11)  (to ~2^(E-33));
 //   qb[part][c] = r_part * 2^(4 - 2p'(c)) as fp16 (exact), p'(c) the fp16 position of channel c
 //     in the K layout, so that code(c) * 2^(2p'-24) * qb = code * r_part * 2^-20;
 //   kap = 2^(E + 9): S_part = accumulator * kap * 2^(-11 part);
-//   qsum[g] = sum over group g of q_rot (hi, lo).
-// q_rot here already carries sm_scale * log2(e), so the INT2 logits come out in log2 units.
-template <int D, int G>
-__global__ void __launch_bounds__(4 * D)
-q_prep_kernel(const __nv_bfloat16* __restrict__ q, const float* __restrict__ r_k,
-              __half* __restrict__ qb, float* __restrict__ kap, float* __restrict__ qsum, int h_q, int g,
-              float sl2_hi, float sl2_lo, int* __restrict__ counters) {
-    constexpr int NG = D / G;
-    constexpr int Q4 = D / 4;                      // terms per thread: four threads per output channel
+//   qdig[slice][part] = sum over the slice's channels of r_part (exact integers).
+template <int D>
+__global__ void __launch_bounds__(128)
+q_prep_kernel(const __nv_bfloat16* __restrict__ q, const float* __restrict__ r_k, const float* __restrict__ colmax,
+              __half* __restrict__ qb, float* __restrict__ kap, float* __restrict__ qdig, int h_q, int g,
+              float sl2_hi, float sl2_lo, int* __restrict__ counters, int counters_per_unit) {
+    constexpr int Q4 = D / 4;
+    constexpr int NS = D / kSliceCh;
     __shared__ float qs[D];
-    __shared__ float hi_s[4][D], lo_s[4][D];
-    __shared__ float wmax[D / 32];
-    __shared__ double gsum[D / 32];
-    const int bh = blockIdx.x;
+    __shared__ float hi_s[4][kSliceCh], lo_s[4][kSliceCh];
+    __shared__ float nq2_s;
+    const int bh = blockIdx.x, slice = blockIdx.y;
     const int kv = (bh % h_q) / g;
-    const int c = threadIdx.x % D, quarter = threadIdx.x / D;
+    const int cl = threadIdx.x % kSliceCh, quarter = threadIdx.x / kSliceCh;
+    const int c = slice * kSliceCh + cl;
     // R_k terms of this thread: constant calibration data, so they load before the wait for the
     // previous kernel (all in flight at once)
     const float* r = r_k + (size_t)kv * D * D + (size_t)quarter * Q4 * D + c;
     float rv[Q4];
 #pragma unroll
     for (int i = 0; i < Q4; ++i) rv[i] = __ldg(r + (size_t)i * D);
+    const float cmax = __ldg(colmax + kv);
     pdl_wait();
     pdl_trigger();
-    // the split kernel's ticket counter of this (sequence, KV head) starts at zero
-    if (threadIdx.x == 0 && (bh % h_q) % g == 0) counters[(bh / h_q) * (h_q / g) + kv] = 0;
-    if (threadIdx.x < D) qs[c] = __bfloat162float(q[(size_t)bh * D + c]);
+    // the split kernel's merge tickets of this (sequence, KV head) start at zero
+    if (slice == 0 && (bh % h_q) % g == 0)
+        for (int i = threadIdx.x; i < counters_per_unit; i += blockDim.x)
+            counters[((size_t)(bh / h_q) * (h_q / g) + kv) * counters_per_unit + i] = 0;
+    for (int i = threadIdx.x; i < D; i += blockDim.x) qs[i] = __bfloat162float(q[(size_t)bh * D + i]);
     __syncthreads();
+    if (threadIdx.x < 32) {
+        // |q|^2 in a fixed order, identical in every CTA of the head
+        float s2 = 0.0f;
+#pragma unroll
+        for (int k = 0; k < D / 32; ++k) s2 = __fmaf_rn(qs[threadIdx.x + 32 * k], qs[threadIdx.x + 32 * k], s2);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) s2 = __fadd_rn(s2, __shfl_xor_sync(0xffffffffu, s2, o));
+        if (threadIdx.x == 0) nq2_s = s2;
+    }
     float hi = 0.0f, lo = 0.0f;
 #pragma unroll
     for (int i = 0; i < Q4; ++i) {
@@ -196,17 +222,17 @@ q_prep_kernel(const __nv_bfloat16* __restrict__ q, const float* __restrict__ r_k
         hi = s2;
         lo = __fadd_rn(lo, __fadd_rn(e, e2));
     }
-    hi_s[quarter][c] = hi;
-    lo_s[quarter][c] = lo;
+    hi_s[quarter][cl] = hi;
+    lo_s[quarter][cl] = lo;
     __syncthreads();
     if (quarter != 0) return;
     float h = 0.0f, l = 0.0f;
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
         float s2, e2;
-        two_sum(h, hi_s[u][c], s2, e2);
+        two_sum(h, hi_s[u][cl], s2, e2);
         h = s2;
-        l = __fadd_rn(l, __fadd_rn(lo_s[u][c], e2));
+        l = __fadd_rn(l, __fadd_rn(lo_s[u][cl], e2));
     }
     {
         float s2, e2;
@@ -223,43 +249,41 @@ q_prep_kernel(const __nv_bfloat16* __restrict__ q, const float* __restrict__ r_k
         h = s2;
         l = e2;
     }
-    // warp max |q_rot| and warp fp64 sums (a warp's 32 channels lie inside one group, G >= 32)
-    float m = fabsf(h);
-    double sum = (double)h + (double)l;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-        sum += __shfl_xor_sync(0xffffffffu, sum, o);
-    }
-    if (c % 32 == 0) { wmax[c / 32] = m; gsum[c / 32] = sum; }
-    asm volatile("bar.sync 1, %0;" :: "r"(D) : "memory");     // the D threads of quarter 0 only
-    m = 0.0f;
-#pragma unroll
-    for (int w = 0; w < D / 32; ++w) m = fmaxf(m, wmax[w]);
-    int ex = 0;
-    frexpf(m * 1.0000005f, &ex);                       // max|q_rot| < 2^ex
+    // exponent from the bound: (sl2 |q| cmax)^2 with a relative margin for the rounding of |q|^2
+    const float nq2 = nq2_s;
+    const float sc = sl2_hi * cmax;
+    const float bound2 = nq2 * sc * sc * 1.0001f;
+    int e2x = 0;
+    frexpf(bound2, &e2x);                              // bound2 < 2^e2x
+    const int ex = (e2x + 1) >> 1;                     // bound < 2^ex (arithmetic shift: ceil(e2x / 2))
+    const bool any = nq2 > 0.0f;
     // r_hi, r_mid, r_lo: successive 11-bit digits of q_rot / 2^(ex-11)
     const float xh = ldexpf(h, 11 - ex), xl = ldexpf(l, 11 - ex);
-    const float r_hi = rintf(xh);
+    const float r_hi = any ? rintf(xh) : 0.0f;
     const float rem1 = __fadd_rn(__fsub_rn(xh, r_hi), xl);                // |rem1| <= 0.5 + tiny
-    const float r_mid = rintf(__fmul_rn(rem1, 2048.0f));
+    const float r_mid = any ? rintf(__fmul_rn(rem1, 2048.0f)) : 0.0f;
     const float rem2 = __fsub_rn(__fmul_rn(rem1, 2048.0f), r_mid);
-    const float r_lo = rintf(__fmul_rn(rem2, 2048.0f));
+    const float r_lo = any ? rintf(__fmul_rn(rem2, 2048.0f)) : 0.0f;
     const int pos = 2 * ((c / 16) % 4) + (c % 4) / 2;                     // K-layout position of channel c
     const int sh = 4 - 2 * pos_scale(pos);
     __half* dst = qb + (size_t)bh * 3 * D;
-    const bool any = m > 0.0f;
-    dst[c] = __float2half_rn(any ? ldexpf(r_hi, sh) : 0.0f);
-    dst[D + c] = __float2half_rn(any ? ldexpf(r_mid, sh) : 0.0f);
-    dst[2 * D + c] = __float2half_rn(any ? ldexpf(r_lo, sh) : 0.0f);
-    if (c == 0) kap[bh] = any ? ldexpf(1.0f, ex + 9) : 0.0f;
-    if (c < NG) {
-        double gs = 0.0;
+    dst[c] = __float2half_rn(ldexpf(r_hi, sh));
+    dst[D + c] = __float2half_rn(ldexpf(r_mid, sh));
+    dst[2 * D + c] = __float2half_rn(ldexpf(r_lo, sh));
+    if (slice == 0 && cl == 0) kap[bh] = any ? ldexpf(1.0f, ex + 9) : 0.0f;
+    // exact integer digit sums of the slice (|sum| <= 32 * 2048)
+    float d0 = r_hi, d1 = r_mid, d2 = r_lo;
 #pragma unroll
-        for (int w = 0; w < G / 32; ++w) gs += gsum[c * (G / 32) + w];
-        const float sh2 = (float)gs;
-        qsum[((size_t)bh * NG + c) * 2 + 0] = sh2;
-        qsum[((size_t)bh * NG + c) * 2 + 1] = (float)(gs - (double)sh2);
+    for (int o = 16; o > 0; o >>= 1) {
+        d0 += __shfl_xor_sync(0xffffffffu, d0, o);
+        d1 += __shfl_xor_sync(0xffffffffu, d1, o);
+        d2 += __shfl_xor_sync(0xffffffffu, d2, o);
+    }
+    if (cl == 0) {
+        float* qd = qdig + ((size_t)bh * NS + slice) * 3;
+        qd[0] = d0;
+        qd[1] = d1;
+        qd[2] = d2;
     }
 }
 
@@ -270,7 +294,7 @@ q_prep_kernel(const __nv_bfloat16* __restrict__ q, const float* __restrict__ r_k
 struct SplitArgs {
     const __half* qb;             // [B][H_q][3][D] tensor-core query parts
     const float* kap;             // [B][H_q]
-    const float* qsum;            // [B][H_q][D/G][2]
+    const float* qdig;            // [B][H_q][D/32][3] digit sums per 32-channel slice
     const float* pv_scale;        // [H_kv] 2^sigma for the p * s_v operand
     const __nv_bfloat16* q;       // [B][H_q][D]
     const uint8_t* int2_pool; int64_t int2_pages;
@@ -283,9 +307,8 @@ struct SplitArgs {
     int h_kv, int2_splits, pages_per_split, bf16_splits, bf16_pages_per_split, total_splits;
     float scale_log2, scale_log2_lo;   // sm_scale * log2(e) as hi + lo
     int debug; DebugWord* dbg;
-    // last-CTA merge: the CTA that finishes a (sequence, KV head) last reduces its partials
-    int fuse_merge;
-    int* counters;                // [B][H_kv] tickets, zeroed by q_prep
+    int fuse_merge;               // the CTA finishing a (sequence, KV head) last merges it
+    int* counters;                // [B][H_kv] merge tickets, zeroed by q_prep
     const float* r_vt;            // [H_kv][D][D]
     float* out;                   // [B][H_q][D]
 };
@@ -435,8 +458,24 @@ __device__ void int2_split(const SplitArgs& a, int split, int kv, int b, uint8_t
         kap_l[hb] = kap_h[hb] * 0x1p-22f;
 #pragma unroll
         for (int gg = 0; gg < NG; ++gg) {
-            qs_hi[hb][gg] = hm < GQ ? a.qsum[((head0 + hm) * NG + gg) * 2 + 0] : 0.0f;
-            qs_lo[hb][gg] = hm < GQ ? a.qsum[((head0 + hm) * NG + gg) * 2 + 1] : 0.0f;
+            // sum over the group of q_rot = 2^(E-11) (S_hi + 2^-11 S_mid + 2^-22 S_lo) (kap 2^-20 =
+            // 2^(E-11)) as hi + lo fp32, without fp64: the digit sums are exact fp32 integers (<= 2^18),
+            // S_hi + 2^-11 S_mid is split error-free, and the 2^-22 S_lo term only enters the low part
+            float sh = 0.0f, sm = 0.0f, sl = 0.0f;
+            if (hm < GQ) {
+#pragma unroll
+                for (int s = gg * (G / kSliceCh); s < (gg + 1) * (G / kSliceCh); ++s) {
+                    const float* qd = a.qdig + ((head0 + hm) * (D / kSliceCh) + s) * 3;
+                    sh += qd[0];
+                    sm += qd[1];
+                    sl += qd[2];
+                }
+            }
+            float h1, e1;
+            two_sum(sh, sm * 0x1p-11f, h1, e1);
+            const float k20 = kap_h[hb] * 0x1p-20f;
+            qs_hi[hb][gg] = h1 * k20;
+            qs_lo[hb][gg] = __fmaf_rn(sl, 0x1p-22f, e1) * k20;
         }
     }
     {
@@ -451,6 +490,7 @@ __device__ void int2_split(const SplitArgs& a, int split, int kv, int b, uint8_t
         }
     }
     const float pvs = a.pv_scale[kv];
+    const float inv_pvs = 1.0f / pvs;         // a power of two: exact
 
 
     bool failed = false;
@@ -678,8 +718,8 @@ __device__ void int2_split(const SplitArgs& a, int split, int kv, int b, uint8_t
             // rows gid and gid+8 of m-step mm carry 2^(2p') of their code position and 2^sigma
             const int pos0 = mm;
             const int pos1 = (D == 128) ? mm : 4 + mm;
-            const float sc0 = ldexpf(1.0f, -2 * pos_scale(pos0)) / pvs;
-            const float sc1 = ldexpf(1.0f, -2 * pos_scale(pos1)) / pvs;
+            const float sc0 = pos_weight(pos0) * inv_pvs;
+            const float sc1 = pos_weight(pos1) * inv_pvs;
             const float o0 = __fmaf_rn(O[hb][mm][1], 0x1p-11f, O[hb][mm][0]) * sc0 + zacc[hb][gg];
             const float o1 = __fmaf_rn(O[hb][mm][3], 0x1p-11f, O[hb][mm][2]) * sc1 + zacc[hb][gg];
             atomicAdd(&acc_s[h * D + 16 * mm + gid], o0 * f);
@@ -824,9 +864,12 @@ __device__ void bf16_split(const SplitArgs& a, int split, int kv, int b, float* 
     }
 }
 
-// Online-softmax merge of one (sequence, KV head)'s splits, run by the CTA that finishes last:
-// per query head, weights 2^(m_s - M) over the split partials, the INT2 splits' sum un-rotated by
-// R_v^T, plus the BF16 split, over L. w_s holds GQ * total_splits floats.
+// Online-softmax merge of one (sequence, KV head)'s splits, run by the CTA that finishes last
+// (GQ * total_splits <= kFuseWeights): per query head, weights 2^(m_s - M) over the split partials,
+// the INT2 splits' sum un-rotated by R_v^T, plus the BF16 split, over L. w_s (the page-stage shared
+// memory) holds GQ * total_splits floats. Records written by other CTAs are read through L2
+// (ld.global.cg), never from a possibly stale L1 line; loads are batched so that each round has
+// many in flight.
 template <int D, int GQ>
 __device__ __noinline__ void merge_group(const SplitArgs& a, int kv, int b, float* acc_s, float* w_s) {
     __shared__ float l_s[GQ];
@@ -835,20 +878,28 @@ __device__ __noinline__ void merge_group(const SplitArgs& a, int kv, int b, floa
     const float* part0 = a.partials + (size_t)(b * h_q + kv * GQ) * T * (D + 2);
     for (int h = warp; h < GQ; h += kWarps) {
         const float* part = part0 + (size_t)h * T * (D + 2);
-        float m = -INFINITY;
-        for (int sp = lane; sp < T; sp += 32) m = fmaxf(m, part[(size_t)sp * (D + 2)]);
+        float m[kFuseWeights / 32], l[kFuseWeights / 32];
+        float M = -INFINITY;
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-        float l = 0.0f;
-        for (int sp = lane; sp < T; sp += 32) {
-            const float ms = part[(size_t)sp * (D + 2)];
-            const float w = (m == -INFINITY || ms == -INFINITY) ? 0.0f : fast_exp2(ms - m);
-            w_s[h * T + sp] = w;
-            l = fmaf(part[(size_t)sp * (D + 2) + 1], w, l);
+        for (int k = 0; k < kFuseWeights / 32; ++k) {
+            const int sp = lane + 32 * k;
+            m[k] = sp < T ? __ldcg(part + (size_t)sp * (D + 2)) : -INFINITY;
+            l[k] = sp < T ? __ldcg(part + (size_t)sp * (D + 2) + 1) : 0.0f;
+            M = fmaxf(M, m[k]);
         }
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
-        if (lane == 0) l_s[h] = l;
+        for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+        float L = 0.0f;
+#pragma unroll
+        for (int k = 0; k < kFuseWeights / 32; ++k) {
+            const int sp = lane + 32 * k;
+            const float w = (M == -INFINITY || m[k] == -INFINITY) ? 0.0f : fast_exp2(m[k] - M);
+            if (sp < T) w_s[h * T + sp] = w;
+            L = fmaf(l[k], w, L);
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
+        if (lane == 0) l_s[h] = L;
     }
     __syncthreads();
     const int c = tid;
@@ -859,10 +910,17 @@ __device__ __noinline__ void merge_group(const SplitArgs& a, int kv, int b, floa
         ab[h] = 0.0f;
         if (c < D) {
             const float* part = part0 + (size_t)h * T * (D + 2) + 2 + c;
-#pragma unroll 8
-            for (int sp = 0; sp < T; ++sp) {
-                const float v = part[(size_t)sp * (D + 2)] * w_s[h * T + sp];
-                if (sp < a.int2_splits) ai += v; else ab[h] += v;
+            for (int s0 = 0; s0 < T; s0 += 16) {
+                float v[16];
+#pragma unroll
+                for (int k = 0; k < 16; ++k) v[k] = s0 + k < T ? __ldcg(part + (size_t)(s0 + k) * (D + 2)) : 0.0f;
+#pragma unroll
+                for (int k = 0; k < 16; ++k) {
+                    const int sp = s0 + k;
+                    if (sp >= T) break;
+                    const float x = v[k] * w_s[h * T + sp];
+                    if (sp < a.int2_splits) ai += x; else ab[h] += x;
+                }
             }
             acc_s[h * D + c] = ai;
         }
@@ -873,11 +931,14 @@ __device__ __noinline__ void merge_group(const SplitArgs& a, int kv, int b, floa
 #pragma unroll
         for (int h = 0; h < GQ; ++h) o[h] = 0.0f;
         const float* rt = a.r_vt + (size_t)kv * D * D + c;
-#pragma unroll 4
-        for (int i = 0; i < D; ++i) {
-            const float r = __ldg(rt + (size_t)i * D);
+        for (int i0 = 0; i0 < D; i0 += 16) {
+            float r[16];
 #pragma unroll
-            for (int h = 0; h < GQ; ++h) o[h] = fmaf(acc_s[h * D + i], r, o[h]);
+            for (int i = 0; i < 16; ++i) r[i] = __ldg(rt + (size_t)(i0 + i) * D);
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+#pragma unroll
+                for (int h = 0; h < GQ; ++h) o[h] = fmaf(acc_s[h * D + i0 + i], r[i], o[h]);
         }
 #pragma unroll
         for (int h = 0; h < GQ; ++h) {
@@ -939,20 +1000,21 @@ split_kernel(SplitArgs a) {
     }
 }
 
-// Merge of all splits of one query head. Block of 4*D threads: thread (c, quarter) sums a quarter of
-// the splits for channel c and a quarter of the un-rotation terms, so its loads are independent.
+// Merge of all splits of one query head (plans with long merges: one wave of few units, or many
+// splits). Block of 4*D threads: thread (c, quarter) takes the splits s = quarter + 4k for channel c,
+// kPer of them per round with every load of the round in flight at once, and a quarter of the
+// un-rotation terms, which load before the wait for the split kernel.
 template <int D>
 __global__ void __launch_bounds__(4 * D)
-merge_kernel(const float* __restrict__ partials, const float* __restrict__ r_vt,
-             float* __restrict__ out, int h_q, int g, int int2_splits, int total_splits) {
-    extern __shared__ float w_s[];     // [total_splits]
+merge_kernel(const float* __restrict__ partials, const float* __restrict__ r_vt, float* __restrict__ out, int h_q,
+             int g, int int2_splits, int total_splits) {
+    constexpr int kPer = 16;
+    __shared__ float red_m[4], red_l[4];
     __shared__ float acc_rot[D];
     __shared__ float part_i[4][D], part_b[4][D];
-    __shared__ float red[4 * D / 32];
     const int bh = blockIdx.x;
     const int kv = (bh % h_q) / g;
     const int tid = threadIdx.x, c = tid % D, quarter = tid / D;
-    // R_v^T terms of this thread (constant calibration data) before waiting for the split kernel
     const float* rt = r_vt + (size_t)kv * D * D + (size_t)quarter * (D / 4) * D + c;
     float rv[D / 4];
 #pragma unroll
@@ -960,38 +1022,41 @@ merge_kernel(const float* __restrict__ partials, const float* __restrict__ r_vt,
     pdl_wait();
     pdl_trigger();
     const float* part = partials + (size_t)bh * total_splits * (D + 2);
-    float mloc = -INFINITY;
-    for (int s = tid; s < total_splits; s += 4 * D) mloc = fmaxf(mloc, part[(size_t)s * (D + 2)]);
+    float M = -INFINITY, L = 0.0f, ai = 0.0f, ab = 0.0f;
+    for (int s0 = 0; s0 < total_splits; s0 += 4 * kPer) {
+        float ms[kPer], ls[kPer], as[kPer];
+        float mloc = -INFINITY;
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) mloc = fmaxf(mloc, __shfl_xor_sync(0xffffffffu, mloc, o));
-    if (tid % 32 == 0) red[tid / 32] = mloc;
-    __syncthreads();
-    float mm = -INFINITY;
+        for (int k = 0; k < kPer; ++k) {
+            const int sp = s0 + 4 * k + quarter;
+            const bool ok = sp < total_splits;
+            const float* r = part + (size_t)sp * (D + 2);
+            ms[k] = ok ? __ldcg(r) : -INFINITY;
+            ls[k] = ok ? __ldcg(r + 1) : 0.0f;
+            as[k] = ok ? __ldcg(r + 2 + c) : 0.0f;
+            mloc = fmaxf(mloc, ms[k]);
+        }
+        // every channel of a quarter holds the same m values
+        if (c == 0) red_m[quarter] = mloc;
+        __syncthreads();
+        const float mn = fmaxf(M, fmaxf(fmaxf(red_m[0], red_m[1]), fmaxf(red_m[2], red_m[3])));
+        const float sc = M == -INFINITY ? 0.0f : fast_exp2(M - mn);
+        ai *= sc;
+        ab *= sc;
+        L *= sc;
 #pragma unroll
-    for (int w = 0; w < 4 * D / 32; ++w) mm = fmaxf(mm, red[w]);
-    __syncthreads();
-    float lloc = 0.0f;
-    for (int s = tid; s < total_splits; s += 4 * D) {
-        const float ms = part[(size_t)s * (D + 2)];
-        const float w = (mm == -INFINITY || ms == -INFINITY) ? 0.0f : fast_exp2(ms - mm);
-        w_s[s] = w;
-        lloc = fmaf(part[(size_t)s * (D + 2) + 1], w, lloc);
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) lloc += __shfl_xor_sync(0xffffffffu, lloc, o);
-    if (tid % 32 == 0) red[tid / 32] = lloc;
-    __syncthreads();
-    float L = 0.0f;
-#pragma unroll
-    for (int w = 0; w < 4 * D / 32; ++w) L += red[w];
-    float ai = 0.0f, ab = 0.0f;
-#pragma unroll 8
-    for (int s = quarter; s < total_splits; s += 4) {
-        const float v = part[(size_t)s * (D + 2) + 2 + c] * w_s[s];
-        if (s < int2_splits) ai += v; else ab += v;
+        for (int k = 0; k < kPer; ++k) {
+            const int sp = s0 + 4 * k + quarter;
+            const float w = ms[k] == -INFINITY ? 0.0f : fast_exp2(ms[k] - mn);
+            L = fmaf(ls[k], w, L);
+            if (sp < int2_splits) ai = fmaf(as[k], w, ai); else ab = fmaf(as[k], w, ab);
+        }
+        M = mn;
+        __syncthreads();
     }
     part_i[quarter][c] = ai;
     part_b[quarter][c] = ab;
+    if (c == 0) red_l[quarter] = L;
     __syncthreads();
     if (quarter == 0) acc_rot[c] = (part_i[0][c] + part_i[1][c]) + (part_i[2][c] + part_i[3][c]);
     __syncthreads();
@@ -1001,10 +1066,28 @@ merge_kernel(const float* __restrict__ partials, const float* __restrict__ r_vt,
     part_i[quarter][c] = o;
     __syncthreads();
     if (quarter == 0) {
+        const float Lt = (red_l[0] + red_l[1]) + (red_l[2] + red_l[3]);
         const float oi = (part_i[0][c] + part_i[1][c]) + (part_i[2][c] + part_i[3][c]);
         const float ob = (part_b[0][c] + part_b[1][c]) + (part_b[2][c] + part_b[3][c]);
-        out[(size_t)bh * D + c] = L > 0.0f ? (oi + ob) / L : 0.0f;
+        out[(size_t)bh * D + c] = Lt > 0.0f ? (oi + ob) / Lt : 0.0f;
     }
+}
+
+// Launch with programmatic stream serialization: the kernel may start while the previous grid in the
+// stream finishes; every kernel here waits (griddepcontrol.wait) before touching its predecessors' data.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, args...);
 }
 
 template <int D, int G, int GQ>
@@ -1029,23 +1112,6 @@ cudaError_t dispatch_gq(int gq, const SplitArgs& a, int batch, cudaStream_t st) 
 }
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
-
-// Launch with programmatic stream serialization: the kernel may start while the previous grid in the
-// stream finishes; every kernel here waits (griddepcontrol.wait) before touching its predecessors' data.
-template <typename... KArgs, typename... Args>
-cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st, Args... args) {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = grid;
-    cfg.blockDim = block;
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = st;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kern, args...);
-}
 
 // Resident split CTAs per SM for the shape on the current device (queried once per device).
 template <int D, int G, int GQ>
@@ -1113,9 +1179,10 @@ DecodePlan plan_decode(const Shape& s, int num_sms, int batch, int max_hist) {
     p.int2_splits = max_pages > 0 ? (max_pages + p.pages_per_split - 1) / p.pages_per_split : 1;
     p.total_splits = p.int2_splits + p.bf16_splits;
     p.ws_partials = align256((size_t)batch * s.h_q * p.total_splits * (s.d + 2) * sizeof(float));
-    p.ws_qrot = align256((size_t)batch * s.h_q * (3 * s.d * sizeof(__half) + sizeof(float) +
-                                                 2 * (s.d / s.group) * sizeof(float)) + 256);
-    p.ws_counters = align256((size_t)batch * s.h_kv * sizeof(int));
+    p.ws_qrot = align256((size_t)batch * s.h_q * 3 * s.d * sizeof(__half)) +
+                align256((size_t)batch * s.h_q * sizeof(float)) +
+                align256((size_t)batch * s.h_q * (s.d / kSliceCh) * 3 * sizeof(float));
+    p.ws_counters = align256((size_t)units * sizeof(int));
     p.ws_total = p.ws_partials + p.ws_qrot + p.ws_counters;
     // the last-CTA merge keeps its weights in the page-stage shared memory (at least 12 KB)
     p.fuse_merge = (size_t)(s.h_q / s.h_kv) * p.total_splits <= kFuseWeights;
@@ -1125,13 +1192,14 @@ DecodePlan plan_decode(const Shape& s, int num_sms, int batch, int max_hist) {
 cudaError_t launch_decode(const Shape& s, const LayerParams& prm, const DecodePlan& plan,
                           const DecodeArgs& a, DebugWord* dbg, Profiler* prof, cudaStream_t st) {
     const int g = s.h_q / s.h_kv;
-    float* partials = static_cast<float*>(a.ws);
-    char* qbase = static_cast<char*>(a.ws) + plan.ws_partials;
+    char* base = static_cast<char*>(a.ws);
+    float* partials = reinterpret_cast<float*>(base);
     const size_t nh = (size_t)a.batch * s.h_q;
+    char* qbase = base + plan.ws_partials;
     __half* qb = reinterpret_cast<__half*>(qbase);
     float* kap = reinterpret_cast<float*>(qbase + align256(nh * 3 * s.d * sizeof(__half)));
-    float* qsum = kap + nh;
-    int* counters = reinterpret_cast<int*>(static_cast<char*>(a.ws) + plan.ws_partials + plan.ws_qrot);
+    float* qdig = reinterpret_cast<float*>(reinterpret_cast<char*>(kap) + align256(nh * sizeof(float)));
+    int* counters = reinterpret_cast<int*>(base + plan.ws_partials + plan.ws_qrot);
     const __nv_bfloat16* q = static_cast<const __nv_bfloat16*>(a.q);
 
     const double sl2d = s.sm_scale * 1.4426950408889634073599;     // sm_scale * log2(e)
@@ -1139,20 +1207,18 @@ cudaError_t launch_decode(const Shape& s, const LayerParams& prm, const DecodePl
     cudaError_t e = cudaSuccess;
     {
         ProfScope ps(prof, OSCAR_KERNEL_QROT, st);
-#define OSCAR_QPREP_CASE(D_, G_) \
-        if (s.d == D_ && s.group == G_) \
-            e = launch_pdl(q_prep_kernel<D_, G_>, dim3(a.batch * s.h_q), dim3(4 * D_), 0, st, q, prm.r_k, qb, kap, qsum, s.h_q, g, sl2_hi, sl2_lo, counters);
-        OSCAR_QPREP_CASE(64, 32)
-        OSCAR_QPREP_CASE(64, 64)
-        OSCAR_QPREP_CASE(128, 32)
-        OSCAR_QPREP_CASE(128, 64)
-        OSCAR_QPREP_CASE(128, 128)
-#undef OSCAR_QPREP_CASE
+        const dim3 grid(a.batch * s.h_q, s.d / kSliceCh);
+        if (s.d == 128)
+            e = launch_pdl(q_prep_kernel<128>, grid, dim3(128), 0, st, q, prm.r_k, prm.rk_colmax, qb, kap, qdig,
+                           s.h_q, g, sl2_hi, sl2_lo, counters, 1);
+        else
+            e = launch_pdl(q_prep_kernel<64>, grid, dim3(128), 0, st, q, prm.r_k, prm.rk_colmax, qb, kap, qdig,
+                           s.h_q, g, sl2_hi, sl2_lo, counters, 1);
     }
     if (e != cudaSuccess) return e;
 
     SplitArgs sa{};
-    sa.qb = qb; sa.kap = kap; sa.qsum = qsum; sa.q = q; sa.pv_scale = prm.pv_scale;
+    sa.qb = qb; sa.kap = kap; sa.qdig = qdig; sa.q = q; sa.pv_scale = prm.pv_scale;
     sa.int2_pool = a.int2_pool; sa.int2_pages = a.int2_pages;
     sa.int2_tables = a.int2_tables; sa.int2_stride = a.int2_stride;
     sa.hist_len = a.hist_len; sa.max_hist = a.max_hist;
@@ -1187,11 +1253,10 @@ cudaError_t launch_decode(const Shape& s, const LayerParams& prm, const DecodePl
     if (plan.fuse_merge) return cudaSuccess;           // merged by the last CTA of each unit
 
     ProfScope ps_merge(prof, OSCAR_KERNEL_MERGE, st);
-    const size_t msmem = (size_t)plan.total_splits * sizeof(float);
     if (s.d == 128)
-        return launch_pdl(merge_kernel<128>, dim3(a.batch * s.h_q), dim3(4 * 128), msmem, st, (const float*)partials,
+        return launch_pdl(merge_kernel<128>, dim3(a.batch * s.h_q), dim3(4 * 128), 0, st, (const float*)partials,
                           prm.r_vt, a.out, s.h_q, g, plan.int2_splits, plan.total_splits);
-    return launch_pdl(merge_kernel<64>, dim3(a.batch * s.h_q), dim3(4 * 64), msmem, st, (const float*)partials,
+    return launch_pdl(merge_kernel<64>, dim3(a.batch * s.h_q), dim3(4 * 64), 0, st, (const float*)partials,
                       prm.r_vt, a.out, s.h_q, g, plan.int2_splits, plan.total_splits);
 }
 

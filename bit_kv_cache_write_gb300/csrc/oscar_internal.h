@@ -42,6 +42,7 @@ struct LayerParams {
     const float* t_k;      // [H_kv][d]
     const float* t_v;      // [H_kv][d]
     const float* pv_scale; // [H_kv] 2^sigma with 2^8 (2/3) max T_v 2^sigma <= 32752: keeps p s_v 2^sigma in fp16
+    const float* rk_colmax;  // [H_kv] upper bound of max_c |R_k[:, c]|_2 (follows pv_scale)
     const uint16_t* r_img; // [K,V][H_kv][3][d*d] bf16 pieces of R as tensor-core operand images
     const float* r_kt;     // [H_kv][d][d], r_kt[h][c][i] = r_k[h][i][c] (exact recompute of the bulk write)
 };
@@ -150,7 +151,7 @@ struct DecodePlan {
     int bf16_pages_per_split;  // BF16 pages per BF16 split
     int total_splits;
     size_t ws_partials;     // bytes of split partials
-    size_t ws_qrot;         // bytes of rotated queries
+    size_t ws_qrot;         // bytes of rotated-query digits, exponents and digit sums
     size_t ws_counters;     // bytes of per-(sequence, KV head) tickets of the last-CTA merge
     bool fuse_merge;        // the split kernel merges (else the merge kernel runs)
     size_t ws_total;

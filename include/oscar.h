@@ -132,8 +132,8 @@ typedef struct oscar_ctx oscar_ctx_t;
 /* Create a context on the current CUDA device.
  * Validates cfg, then allocates the per-layer calibration buffers and the
  * error word. Per layer:
- *   (3 * H_kv * d * d + 2 * H_kv * d + H_kv) * 4 bytes: R_k, R_v, R_v^T, T_k, T_v
- *     and one P.V exponent per KV head;
+ *   (3 * H_kv * d * d + 2 * H_kv * d + 2 * H_kv) * 4 bytes: R_k, R_v, R_v^T, T_k,
+ *     T_v, and per KV head one P.V exponent and a bound of R_k's column norms;
  *   H_kv * d * d * 4 bytes: R_k^T (the exact path of the tensor-core write);
  *   2 * 3 * H_kv * d * d * 2 bytes: R_k and R_v as three bf16 pieces each, in
  *     the shared-memory image the tensor-core write loads.
