@@ -141,7 +141,7 @@ class GpuWorkload:
     sequence owns one spare INT2 page, outside its history, that receives the per-step demote.
     Physical INT2 pages are a seeded permutation (non-contiguous tables)."""
 
-    def __init__(self, cfg, layers, dev, seed_offset=0):
+    def __init__(self, cfg, layers, dev, seed_offset=0, shared_prefix_call=False):
         import numpy as np
         import torch
         from bit_kv_cache_write_gb300 import calibration, synth
@@ -243,7 +243,18 @@ class GpuWorkload:
             li = synth.LayerInputs(cfg, layer + seed_offset)
             perm = synth.page_permutation(li.seed, "int2", total).astype(np.int64)
             self.dsts.append(torch.from_numpy(perm[total - B:] * P).to(dev))
-        self.ws = torch.empty(self.ctx.decode_workspace_size(B, self.max_hist), dtype=torch.uint8, device=dev)
+        # the shared-prefix call takes the prefix pages once and each sequence's own pages after them
+        self.shared_prefix_call = shared_prefix_call and shared_pages > 0
+        if self.shared_prefix_call:
+            self.prefix_tables = [t[0, :shared_pages].contiguous() for t in self.tables]
+            self.own_tables = [t[:, shared_pages:].contiguous() for t in self.tables]
+            own = (hist - shared_hist).astype(np.int32)
+            self.own_len = torch.from_numpy(own).to(dev)
+            self.own_max = int(own.max())
+            ws_bytes = self.ctx.decode_shared_prefix_workspace_size(B, shared_pages, self.own_max)
+        else:
+            ws_bytes = self.ctx.decode_workspace_size(B, self.max_hist)
+        self.ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
         self.out = torch.empty(layers, B, h_q, d, dtype=torch.float32, device=dev)
         self.q_all = torch.stack(self.qs, 0).contiguous()
         self.side = torch.cuda.Stream(device=dev)
@@ -267,9 +278,15 @@ class GpuWorkload:
                 self.ctx.demote_recent(layer, self.bf16_pools[layer], self.src, self.int2_pools[layer], self.dsts[layer])
                 self.demoted[layer].record(self.side)
             main.wait_event(self.demoted[layer])
-            self.ctx.decode(layer, self.q_all[layer], self.int2_pools[layer], self.tables[layer], self.hist_len,
-                            self.max_hist, self.bf16_pools[layer], self.bf16_table, self.bf16_len,
-                            self.out[layer], self.ws)
+            if self.shared_prefix_call:
+                self.ctx.decode_shared_prefix(layer, self.q_all[layer], self.int2_pools[layer],
+                                              self.prefix_tables[layer], self.own_tables[layer], self.own_len,
+                                              self.own_max, self.bf16_pools[layer], self.bf16_table, self.bf16_len,
+                                              self.out[layer], self.ws)
+            else:
+                self.ctx.decode(layer, self.q_all[layer], self.int2_pools[layer], self.tables[layer], self.hist_len,
+                                self.max_hist, self.bf16_pools[layer], self.bf16_table, self.bf16_len,
+                                self.out[layer], self.ws)
         main.wait_stream(self.side)
 
 
@@ -341,6 +358,46 @@ def bench_write(dev, steps, warmup):
     demote = {"batch": nb, "us_per_call": us_d, "tokens_per_s": nb / (us_d * 1e-6),
               "algorithmic_bytes": write_bytes(cfg, nb)}
     return {"bulk": bulk, "demote": demote}
+
+
+def bench_calibration(dev, steps, warmup):
+    """GPU calibration targets (Q^T Q and V^T S^T S V per KV head, fp64) at the 1,024-sample calibration
+    size of the Qwen3-8B-shape workload: 1,024 queries of each of the 32 query heads and 1,024 keys and
+    values of each of the 8 KV heads, d = 128. CUDA events on the launching stream."""
+    import torch
+    from bit_kv_cache_write_gb300 import oscar as O, synth
+    cfg = workload_cfg("qwen3_8b_bs1_100k")
+    q_cal, k_cal, v_cal = synth.LayerInputs(cfg, 0).calibration()
+    q = torch.from_numpy(q_cal).to(dev)
+    k = torch.from_numpy(k_cal).to(dev)
+    v = torch.from_numpy(v_cal).to(dev)
+    n, h_q, d = q.shape
+    m, h_kv = k.shape[0], k.shape[1]
+    tk = torch.empty(h_kv, d, d, dtype=torch.float64, device=dev)
+    tv = torch.empty_like(tk)
+    ws = torch.empty(O.oscar_calibration_workspace_size(n, h_q, h_kv, d), dtype=torch.uint8, device=dev)
+    sm = d ** -0.5
+    for _ in range(warmup):
+        O.oscar_calibration_targets(q, k, v, sm, tk, tv, ws)
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    stream = torch.cuda.current_stream()
+    a.record(stream)
+    for _ in range(steps):
+        O.oscar_calibration_targets(q, k, v, sm, tk, tv, ws)
+    b.record(stream)
+    torch.cuda.synchronize()
+    us = a.elapsed_time(b) * 1e3 / steps
+    rows = n * (h_q // h_kv)
+    # fp64 flops: two full d x d Gram products per KV head, and per (row, head) m x d logits and m x d S.V
+    flops = h_kv * (2 * 2.0 * rows * d * d + rows * 2 * 2.0 * m * d)
+    peak = 1250.0   # GFLOP/s: the part's nominal fp64 rate (not measured on this pool)
+    return {"workload": "calibration targets: %d queries x %d query heads, %d keys x %d KV heads, d = %d"
+                        % (n, h_q, m, h_kv, d),
+            "us_per_call": us, "fp64_gflop": flops / 1e9,
+            "roofline": {"bound": "fp64", "achieved": flops / (us * 1e-6) / 1e9, "peak": peak,
+                         "peak_kind": "nominal (fp64 is not in the measured peaks)", "unit": "GFLOP/s",
+                         "frac": flops / (us * 1e-6) / 1e9 / peak}}
 
 
 def kernel_traffic(kernel, workload):
@@ -429,14 +486,14 @@ def run_reference(args, cfg, world, rank):
 
 # --------------------------------------------------------------------------- main
 
-def measure_decode(cfg, layers, dev, steps, warmup, local, seed_offset=0):
+def measure_decode(cfg, layers, dev, steps, warmup, local, seed_offset=0, shared_prefix_call=False):
     """Build a workload's caches, capture one step in a CUDA graph and time K replays (max over ranks).
 
     Returns (workload, graph, metrics). The metrics hold the step time, per-kernel CUDA-event averages
     from an eager pass of the same launches, and the split kernel's achieved GB/s on unique bytes."""
     import torch
     from bit_kv_cache_write_gb300 import oscar as O
-    wl = GpuWorkload(cfg, layers, dev, seed_offset=seed_offset)
+    wl = GpuWorkload(cfg, layers, dev, seed_offset=seed_offset, shared_prefix_call=shared_prefix_call)
     stream = torch.cuda.current_stream()
 
     # ---- capture one step in a CUDA graph (the library launches on the capturing stream)
@@ -482,17 +539,19 @@ def measure_decode(cfg, layers, dev, steps, warmup, local, seed_offset=0):
                        "split_bytes": split_bytes, "launches_per_step": launches}
 
 
-def workload_line(name, layers, dev, steps, warmup, local):
-    """Throughput of one more decode workload at a reduced layer count (its per-layer pages exceed L2)."""
+def workload_line(name, layers, dev, steps, warmup, local, shared_prefix_call=False):
+    """Throughput of one more decode workload at a reduced layer count (its per-layer pages exceed L2).
+    shared_prefix_call: decode through oscar_decode_shared_prefix (the prefix pages given once)."""
     import torch
     cfg = workload_cfg(name)
-    wl, graph, m = measure_decode(cfg, layers, dev, steps, warmup, local)
+    wl, graph, m = measure_decode(cfg, layers, dev, steps, warmup, local, shared_prefix_call=shared_prefix_call)
     peak, peak_kind = measured_peak()
     us_layer = 1e6 * m["max_sec"] / steps / layers
     split_us = m["kernels"]["split"]["avg_us"]
     res = {"layers": layers, "batch": wl.batch, "h_q": cfg["h_q"], "h_kv": cfg["h_kv"], "group": cfg["group"],
            "int2_history": {"min": int(wl.hist.min()), "max": int(wl.hist.max()), "sum": int(wl.hist.sum())},
            "shared_prefix_int2_tokens": wl.shared_hist,
+           "call": "oscar_decode_shared_prefix" if wl.shared_prefix_call else "oscar_decode",
            "us_per_layer": us_layer, "kv_tokens_per_s": wl.tokens_per_layer / (us_layer * 1e-6),
            "kernels": m["kernels"],
            "split_roofline": {"bound": "hbm", "achieved": m["achieved"], "peak": peak, "peak_kind": peak_kind,
@@ -593,13 +652,16 @@ def main():
                                                                               case.bf16_lens[0], cfg["h_q"])}
 
     write = bench_write(dev, max(args.steps, 5), args.warmup) if rank == 0 and not args.no_write else None
+    calib = bench_calibration(dev, 5, 3) if rank == 0 and not args.no_write else None
 
     # ---- the batched and mixed-length decode workloads (N = 1), at layer counts whose pages exceed L2
     workloads = None
     if world == 1 and not args.no_workloads:
         workloads = {"qwen3_4b_b64_32k": workload_line("qwen3_4b_b64_32k", 2, dev, args.steps, args.warmup, local),
                      "qwen3_32b_mixed16": workload_line("qwen3_32b_mixed16", 4, dev, args.steps, args.warmup,
-                                                        local)}
+                                                        local),
+                     "qwen3_32b_mixed16_shared_prefix": workload_line("qwen3_32b_mixed16", 4, dev, args.steps,
+                                                                      args.warmup, local, shared_prefix_call=True)}
 
     if rank == 0:
         line = {
@@ -632,6 +694,7 @@ def main():
             "cpu_baseline": cpu_baseline,
             "write": write,
             "workloads": workloads,
+            "calibration": calib,
         }
         print(json.dumps(line))
     if world > 1:

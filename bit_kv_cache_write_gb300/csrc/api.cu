@@ -297,29 +297,40 @@ size_t oscar_decode_workspace_size(const oscar_ctx_t* ctx, int batch, int max_hi
     return oscar::plan_decode(ctx->shape, ctx->num_sms, batch, max_hist).ws_total;
 }
 
-oscar_status oscar_decode(oscar_ctx_t* ctx, int layer, const void* q,
-                          const void* int2_pool, int64_t int2_pool_pages,
-                          const int32_t* int2_tables, int int2_table_stride,
-                          const int32_t* hist_len, int max_hist,
-                          const void* bf16_pool, int64_t bf16_pool_pages,
-                          const int32_t* bf16_tables, int bf16_table_stride,
-                          const int32_t* bf16_len,
-                          float* out, void* workspace, size_t workspace_bytes,
-                          int batch, void* stream) {
+size_t oscar_decode_shared_prefix_workspace_size(const oscar_ctx_t* ctx, int batch, int prefix_pages, int max_hist) {
+    if (!ctx || batch < 0 || batch > oscar::kMaxBatch || max_hist < 0 || prefix_pages < 0) return 0;
+    return oscar::plan_decode(ctx->shape, ctx->num_sms, batch, max_hist, prefix_pages).ws_total;
+}
+
+}  // extern "C"
+
+namespace {
+
+// Shared body of oscar_decode and oscar_decode_shared_prefix (prefix_pages = 0: no shared prefix).
+oscar_status decode_call(oscar_ctx_t* ctx, int layer, const void* q, const void* int2_pool, int64_t int2_pool_pages,
+                         const int32_t* prefix_table, int prefix_pages, const int32_t* int2_tables,
+                         int int2_table_stride, const int32_t* hist_len, int max_hist, const void* bf16_pool,
+                         int64_t bf16_pool_pages, const int32_t* bf16_tables, int bf16_table_stride,
+                         const int32_t* bf16_len, float* out, void* workspace, size_t workspace_bytes, int batch,
+                         void* stream) {
     oscar_status st = check_ctx_layer(ctx, layer);
     if (st != OSCAR_OK) return st;
-    if (batch < 0 || max_hist < 0) return fail(OSCAR_ERR_INVALID_ARG, "batch %d / max_hist %d negative", batch, max_hist);
+    if (batch < 0 || max_hist < 0 || prefix_pages < 0)
+        return fail(OSCAR_ERR_INVALID_ARG, "batch %d / max_hist %d / prefix_pages %d negative", batch, max_hist,
+                    prefix_pages);
     if (batch == 0) return OSCAR_OK;
     if (batch > oscar::kMaxBatch)
         return fail(OSCAR_ERR_UNSUPPORTED, "batch %d above %d (one grid dimension per sequence)", batch, oscar::kMaxBatch);
     if (!q || !out || !hist_len || !bf16_len) return fail(OSCAR_ERR_INVALID_ARG, "device pointer is NULL");
     if (max_hist > 0 && (!int2_pool || !int2_tables || int2_table_stride <= 0 || int2_pool_pages <= 0))
         return fail(OSCAR_ERR_INVALID_ARG, "INT2 pool/tables missing while max_hist = %d", max_hist);
+    if (prefix_pages > 0 && (!int2_pool || !prefix_table || int2_pool_pages <= 0))
+        return fail(OSCAR_ERR_INVALID_ARG, "INT2 pool/prefix table missing while prefix_pages = %d", prefix_pages);
     if (!bf16_pool || !bf16_tables || bf16_table_stride <= 0 || bf16_pool_pages <= 0)
         return fail(OSCAR_ERR_INVALID_ARG, "BF16 pool/tables missing");
     if ((long long)max_hist > (long long)int2_table_stride * oscar::kPage && max_hist > 0)
         return fail(OSCAR_ERR_INVALID_ARG, "max_hist %d exceeds table stride %d pages", max_hist, int2_table_stride);
-    const oscar::DecodePlan plan = oscar::plan_decode(ctx->shape, ctx->num_sms, batch, max_hist);
+    const oscar::DecodePlan plan = oscar::plan_decode(ctx->shape, ctx->num_sms, batch, max_hist, prefix_pages);
     if (!workspace || workspace_bytes < plan.ws_total)
         return fail(OSCAR_ERR_WORKSPACE, "workspace %zu bytes, need %zu", workspace_bytes, plan.ws_total);
     if (reinterpret_cast<uintptr_t>(workspace) % 256)
@@ -327,6 +338,7 @@ oscar_status oscar_decode(oscar_ctx_t* ctx, int layer, const void* q,
     if (fault("launch")) return fail(OSCAR_ERR_CUDA, "injected launch failure (OSCAR_FAULT=launch)");
     oscar::DecodeArgs a;
     a.q = q;
+    a.prefix_table = prefix_table; a.prefix_pages = prefix_pages;
     a.int2_pool = static_cast<const uint8_t*>(int2_pool); a.int2_pages = int2_pool_pages;
     a.int2_tables = int2_tables; a.int2_stride = int2_table_stride;
     a.hist_len = hist_len; a.max_hist = max_hist;
@@ -337,6 +349,39 @@ oscar_status oscar_decode(oscar_ctx_t* ctx, int layer, const void* q,
     cudaError_t e = oscar::launch_decode(ctx->shape, oscar::layer_params(ctx, layer), plan, a, ctx->dbg,
                                          &ctx->prof, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? OSCAR_OK : cuda_fail(e, "decode launch");
+}
+
+}  // namespace
+
+extern "C" {
+
+oscar_status oscar_decode(oscar_ctx_t* ctx, int layer, const void* q,
+                          const void* int2_pool, int64_t int2_pool_pages,
+                          const int32_t* int2_tables, int int2_table_stride,
+                          const int32_t* hist_len, int max_hist,
+                          const void* bf16_pool, int64_t bf16_pool_pages,
+                          const int32_t* bf16_tables, int bf16_table_stride,
+                          const int32_t* bf16_len,
+                          float* out, void* workspace, size_t workspace_bytes,
+                          int batch, void* stream) {
+    return decode_call(ctx, layer, q, int2_pool, int2_pool_pages, nullptr, 0, int2_tables, int2_table_stride,
+                       hist_len, max_hist, bf16_pool, bf16_pool_pages, bf16_tables, bf16_table_stride, bf16_len,
+                       out, workspace, workspace_bytes, batch, stream);
+}
+
+oscar_status oscar_decode_shared_prefix(oscar_ctx_t* ctx, int layer, const void* q,
+                                        const void* int2_pool, int64_t int2_pool_pages,
+                                        const int32_t* prefix_table, int prefix_pages,
+                                        const int32_t* int2_tables, int int2_table_stride,
+                                        const int32_t* hist_len, int max_hist,
+                                        const void* bf16_pool, int64_t bf16_pool_pages,
+                                        const int32_t* bf16_tables, int bf16_table_stride,
+                                        const int32_t* bf16_len,
+                                        float* out, void* workspace, size_t workspace_bytes,
+                                        int batch, void* stream) {
+    return decode_call(ctx, layer, q, int2_pool, int2_pool_pages, prefix_table, prefix_pages, int2_tables,
+                       int2_table_stride, hist_len, max_hist, bf16_pool, bf16_pool_pages, bf16_tables,
+                       bf16_table_stride, bf16_len, out, workspace, workspace_bytes, batch, stream);
 }
 
 namespace {

@@ -304,7 +304,12 @@ struct SplitArgs {
     const int32_t* bf16_tables; int bf16_stride;
     const int32_t* bf16_len; int max_bf16;
     float* partials;              // [B][H_q][S][D+2]
-    int h_kv, int2_splits, pages_per_split, bf16_splits, bf16_pages_per_split, total_splits;
+    int h_kv, int2_splits, pages_per_split, bf16_splits, bf16_pages_per_split;
+    // shared prefix (cascade): pages every sequence's history starts with, read by prefix CTAs that
+    // each serve kWarps sequences; their partials take slots [0, prefix_splits), the per-sequence
+    // splits follow
+    const int32_t* prefix_table; int prefix_pages, prefix_pages_per_split, prefix_splits, n_prefix_ctas, batch;
+    int total_splits;             // partial slots per query head: prefix + INT2 + BF16 splits
     float scale_log2, scale_log2_lo;   // sm_scale * log2(e) as hi + lo
     int debug; DebugWord* dbg;
     int fuse_merge;               // the CTA finishing a (sequence, KV head) last merges it
@@ -358,89 +363,26 @@ __device__ __forceinline__ void static_for(F&& f) {
     }
 }
 
-// INT2 history split on tensor cores. Writes this warp's state into acc_s / ml_s.
+// Query operands of one (sequence, KV head) for this lane, constant over a split's pages: the three
+// digit parts as m16n8k16 B fragments, the digit scales and the per-group sums of q_rot (hi + lo).
 template <int D, int G, int GQ>
-__device__ void int2_split(const SplitArgs& a, int split, int kv, int b, uint8_t* stage_base, uint64_t* bars,
-                           float* acc_s, float (*ml_s)[GQ][2]) {
-    using GE = Geo<D, G>;
-    constexpr int NK = D / 16;          // k-steps (QK) = m-steps (PV)
-    constexpr int NG = D / G;
-    constexpr int KPG = G / 16;         // k-steps per group
-    constexpr int NHB = (GQ + 3) / 4;   // blocks of 4 query heads
-    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-    const int gid = lane >> 2, tig = lane & 3;
-    const int h_q = a.h_kv * GQ;
-    const size_t head0 = (size_t)b * h_q + kv * GQ;
-
-    int len = a.hist_len[b];
-    const int cap = min(a.max_hist, a.int2_stride * kPage);
-    if (len < 0 || len > cap) {
-        if (a.debug && threadIdx.x == 0) record_error(&a.dbg->kind, &a.dbg->index, 3, len);
-        len = len < 0 ? 0 : cap;
-    }
-    const int n_pages = (len + kPage - 1) / kPage;
-    const int pg0 = split * a.pages_per_split;
-    const int pg1 = min(n_pages, pg0 + a.pages_per_split);
-    const int first = pg0 + warp;
-    const int n_mine = first < pg1 ? (pg1 - first + kWarps - 1) / kWarps : 0;
-    const int32_t* table = a.int2_tables + (size_t)b * a.int2_stride;
-    // page ids of this warp, 32 at a time across the lanes: chunk c (pages 32c .. 32c+31 of the warp)
-    // lives in ids0 (c even) or ids1 (c odd) and is refilled with chunk c+2 once all its pages are issued
-    int32_t ids0 = lane < n_mine ? table[first + kWarps * lane] : -1;
-    int32_t ids1 = lane + 32 < n_mine ? table[first + kWarps * (lane + 32)] : -1;
-
-    float O[NHB][NK][4];
-#pragma unroll
-    for (int hb = 0; hb < NHB; ++hb)
-#pragma unroll
-        for (int mm = 0; mm < NK; ++mm)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) O[hb][mm][e] = 0.0f;
-    float m_run[NHB], l_run[NHB], zacc[NHB][NG];
-#pragma unroll
-    for (int hb = 0; hb < NHB; ++hb) {
-        m_run[hb] = kNoMax;          // finite: ex2(-inf - kNoMax) = 0 without a guard
-        l_run[hb] = 0.0f;
-#pragma unroll
-        for (int gg = 0; gg < NG; ++gg) zacc[hb][gg] = 0.0f;
-    }
-
-    // ---- page pipeline: kStages bulk copies in flight per warp
-    uint8_t* my_stage = stage_base + (size_t)warp * kStages * GE::kBlock;
-    const uint32_t stage_s = (uint32_t)__cvta_generic_to_shared(my_stage);
-    const uint32_t bar_s = (uint32_t)__cvta_generic_to_shared(bars + warp * kStages);
-    if (lane == 0) {
-        for (int s = 0; s < kStages; ++s) mbar_init(bar_s + 8 * s, 1);
-        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    }
-    __syncwarp();
-    uint32_t valid_mask = 0u;    // bit s: stage s holds a real page
-    // launch arguments used every page, held in registers
-    const uint8_t* const pool_kv = a.int2_pool + (size_t)kv * GE::kBlock;
-    const size_t page_stride = (size_t)a.h_kv * GE::kBlock;
-    const int64_t pool_pages = a.int2_pages;
-    const bool dbg_on = a.debug != 0;
-    auto issue = [&](int j) {
-        const int s = j % kStages;
-        const int32_t phys = __shfl_sync(0xffffffffu, ((j >> 5) & 1) ? ids1 : ids0, j & 31);
-        const bool ok = phys >= 0 && phys < pool_pages;
-        if (!ok && dbg_on && lane == 0) record_error(&a.dbg->kind, &a.dbg->index, 2, phys);
-        valid_mask = ok ? (valid_mask | (1u << s)) : (valid_mask & ~(1u << s));
-        if (lane == 0) {
-            if (ok)
-                bulk_load(stage_s + s * GE::kBlock, pool_kv + (size_t)phys * page_stride, GE::kBlock, bar_s + 8 * s);
-            else
-                mbar_arrive(bar_s + 8 * s);
-        }
-    };
-    for (int j = 0; j < kStages && j < n_mine; ++j) issue(j);
-
-    // the query operands come from q_prep: wait for it (the page copies above are already in flight)
-    pdl_wait();
-    pdl_trigger();
-    // ---- query operands (constant over pages)
+struct QueryOps {
+    static constexpr int NK = D / 16, NG = D / G, NHB = (GQ + 3) / 4;
     uint32_t qB1[NK][NHB][2], qB2[NK][2];
     float kap_h[NHB], kap_m[NHB], kap_l[NHB], qs_hi[NHB][NG], qs_lo[NHB][NG];
+};
+
+template <int D, int G, int GQ>
+__device__ __forceinline__ void load_query_ops(const SplitArgs& a, size_t head0, int gid, int tig,
+                                               QueryOps<D, G, GQ>& qo) {
+    constexpr int NK = D / 16, NG = D / G, NHB = (GQ + 3) / 4;
+    auto& qB1 = qo.qB1;
+    auto& qB2 = qo.qB2;
+    auto& kap_h = qo.kap_h;
+    auto& kap_m = qo.kap_m;
+    auto& kap_l = qo.kap_l;
+    auto& qs_hi = qo.qs_hi;
+    auto& qs_lo = qo.qs_lo;
 #pragma unroll
     for (int hb = 0; hb < NHB; ++hb) {
         const int h = 4 * hb + (gid >> 1);
@@ -489,6 +431,279 @@ __device__ void int2_split(const SplitArgs& a, int split, int kv, int b, uint8_t
             qB2[kk][1] = v.y;
         }
     }
+}
+
+// Online-softmax state of one warp: P.V accumulators (rotated basis, scaled by 2^sigma and the code
+// positions), running max and sum, and the zero-point sums.
+template <int D, int G, int GQ>
+struct WarpAcc {
+    static constexpr int NK = D / 16, NG = D / G, NHB = (GQ + 3) / 4;
+    float O[NHB][NK][4];
+    float m_run[NHB], l_run[NHB], zacc[NHB][NG];
+    __device__ __forceinline__ void init() {
+#pragma unroll
+        for (int hb = 0; hb < NHB; ++hb) {
+#pragma unroll
+            for (int mm = 0; mm < NK; ++mm)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) O[hb][mm][e] = 0.0f;
+            m_run[hb] = kNoMax;          // finite: ex2(-inf - kNoMax) = 0 without a guard
+            l_run[hb] = 0.0f;
+#pragma unroll
+            for (int gg = 0; gg < NG; ++gg) zacc[hb][gg] = 0.0f;
+        }
+    }
+};
+
+// One INT2 page (16 tokens, the first `nvalid` valid) of one KV head, staged in shared memory at sb,
+// folded into the warp's softmax state.
+template <int D, int G, int GQ>
+__device__ __forceinline__ void int2_page(const uint8_t* sb, int nvalid, int gid, int tig, float pvs,
+                                          const QueryOps<D, G, GQ>& qo, WarpAcc<D, G, GQ>& acc) {
+    using GE = Geo<D, G>;
+    constexpr int NK = D / 16, NG = D / G, KPG = G / 16, NHB = (GQ + 3) / 4;
+    const auto& qB1 = qo.qB1;
+    const auto& qB2 = qo.qB2;
+    const auto& kap_h = qo.kap_h;
+    const auto& kap_m = qo.kap_m;
+    const auto& kap_l = qo.kap_l;
+    const auto& qs_hi = qo.qs_hi;
+    const auto& qs_lo = qo.qs_lo;
+    auto& O = acc.O;
+    auto& m_run = acc.m_run;
+    auto& l_run = acc.l_run;
+    auto& zacc = acc.zacc;
+    const bool v0 = gid < nvalid, v1 = gid + 8 < nvalid;
+
+    // ---- QK^T on tensor cores: A = K codes [16 tokens x 16 channels], B = query parts
+    uint32_t kw0[2], kw1[2];
+    if constexpr (D == 128) {
+        const uint2 u0 = *reinterpret_cast<const uint2*>(sb + gid * GE::kCodeRow + 8 * tig);
+        const uint2 u1 = *reinterpret_cast<const uint2*>(sb + (gid + 8) * GE::kCodeRow + 8 * tig);
+        kw0[0] = u0.x; kw0[1] = u0.y; kw1[0] = u1.x; kw1[1] = u1.y;
+    } else {
+        kw0[0] = *reinterpret_cast<const uint32_t*>(sb + gid * GE::kCodeRow + 4 * tig);
+        kw1[0] = *reinterpret_cast<const uint32_t*>(sb + (gid + 8) * GE::kCodeRow + 4 * tig);
+        kw0[1] = kw1[1] = 0u;
+    }
+    float S1[NG][NHB][4], S2[NG][4];
+#pragma unroll
+    for (int gg = 0; gg < NG; ++gg) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) S2[gg][e] = 0.0f;
+#pragma unroll
+        for (int hb = 0; hb < NHB; ++hb)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) S1[gg][hb][e] = 0.0f;
+    }
+    static_for<NK>([&](auto kkc) {
+        constexpr int kk = decltype(kkc)::value;
+        uint32_t A0, A1, A2, A3;
+        k_operand<D, kk>(kw0, kw1, A0, A1, A2, A3);
+        constexpr int gg = kk / KPG;
+#pragma unroll
+        for (int hb = 0; hb < NHB; ++hb) mma16816(S1[gg][hb], A0, A1, A2, A3, qB1[kk][hb][0], qB1[kk][hb][1]);
+        mma16816(S2[gg], A0, A1, A2, A3, qB2[kk][0], qB2[kk][1]);
+    });
+
+    // ---- logits (hi + lo, log2 units) for tokens gid and gid+8 of head 4hb + tig
+    const __half2* ksz = reinterpret_cast<const __half2*>(sb + GE::kCodeBytes);
+    const __half2* vsz = reinterpret_cast<const __half2*>(sb + GE::kSeg + GE::kCodeBytes);
+    uint32_t Pv[NHB][NG][2];     // p * s_v * 2^sigma per token slot, as (hi, lo) fp16 pair
+#pragma unroll
+    for (int hb = 0; hb < NHB; ++hb) {
+        float lh[2], ll[2];
+#pragma unroll
+        for (int slot = 0; slot < 2; ++slot) {
+            const int tok = gid + 8 * slot;
+            float dh = 0.0f, dl = 0.0f;
+#pragma unroll
+            for (int gg = 0; gg < NG; ++gg) {
+                const float lo_raw = (GQ == 8) ? S2[gg][2 * slot + hb] : S2[gg][2 * slot];
+                const float s_hi = __fmul_rn(S1[gg][hb][2 * slot], kap_h[hb]);
+                const float s_r = __fmaf_rn(S1[gg][hb][2 * slot + 1], kap_m[hb], __fmul_rn(lo_raw, kap_l[hb]));
+                const float2 sz = __half22float2(ksz[tok * NG + gg]);
+                float p1, e1, p2, e2, t1, e3;
+                two_prod(sz.x, s_hi, p1, e1);
+                two_prod(sz.y, qs_hi[hb][gg], p2, e2);
+                two_sum(p1, p2, t1, e3);
+                const float low = __fadd_rn(__fadd_rn(e1, e2),
+                                            __fadd_rn(e3, __fmaf_rn(sz.x, s_r, __fmul_rn(sz.y, qs_lo[hb][gg]))));
+                if (NG == 1) {
+                    dh = t1;
+                    dl = low;
+                } else {
+                    float t2, e4;
+                    two_sum(dh, t1, t2, e4);
+                    dh = t2;
+                    dl = __fadd_rn(dl, __fadd_rn(low, e4));
+                }
+            }
+            lh[slot] = dh;          // already in log2 units (the query carries the scale)
+            ll[slot] = dl;
+        }
+        const bool ok0 = v0 && (4 * hb + tig < GQ), ok1 = v1 && (4 * hb + tig < GQ);
+        if (!ok0) { lh[0] = -INFINITY; ll[0] = 0.0f; }
+        if (!ok1) { lh[1] = -INFINITY; ll[1] = 0.0f; }
+        // online softmax over the page (lanes sharing tig hold the same head)
+        float mp = fmaxf(lh[0], lh[1]);
+        mp = fmaxf(mp, __shfl_xor_sync(0xffffffffu, mp, 4));
+        mp = fmaxf(mp, __shfl_xor_sync(0xffffffffu, mp, 8));
+        mp = fmaxf(mp, __shfl_xor_sync(0xffffffffu, mp, 16));
+        // lazy reference: raised only when a logit passes it by more than 2^kSoftmaxHeadroomLog2,
+        // so p <= 2^8 and the O rescale is rare
+        if (__any_sync(0xffffffffu, mp > m_run[hb] + (float)kSoftmaxHeadroomLog2)) {
+            const float mn = fmaxf(m_run[hb], mp);
+            const float alpha = ex2(m_run[hb] - mn);
+            m_run[hb] = mn;
+            l_run[hb] *= alpha;
+#pragma unroll
+            for (int mm = 0; mm < NK; ++mm)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) O[hb][mm][e] *= alpha;
+#pragma unroll
+            for (int gg = 0; gg < NG; ++gg) zacc[hb][gg] *= alpha;
+        }
+        const float p0 = ex2(__fadd_rn(__fsub_rn(lh[0], m_run[hb]), ll[0]));
+        const float p1 = ex2(__fadd_rn(__fsub_rn(lh[1], m_run[hb]), ll[1]));
+        l_run[hb] = __fadd_rn(l_run[hb], __fadd_rn(p0, p1));
+#pragma unroll
+        for (int gg = 0; gg < NG; ++gg) {
+            const float2 s0 = __half22float2(vsz[gid * NG + gg]);
+            const float2 s1 = __half22float2(vsz[(gid + 8) * NG + gg]);
+            // p <= 2^8 and s_v <= (2/3) max T_v, and 2^sigma leaves that headroom, so
+            // x <= 32752 (1 + tiny): fp16 without a clamp
+            const float x0 = ok0 ? __fmul_rn(__fmul_rn(p0, s0.x), pvs) : 0.0f;
+            const float x1 = ok1 ? __fmul_rn(__fmul_rn(p1, s1.x), pvs) : 0.0f;
+            const __half h0 = __float2half_rn(x0), h1 = __float2half_rn(x1);
+            Pv[hb][gg][0] = pack_half2(h0, __float2half_rn(__fmul_rn(__fsub_rn(x0, __half2float(h0)), 2048.0f)));
+            Pv[hb][gg][1] = pack_half2(h1, __float2half_rn(__fmul_rn(__fsub_rn(x1, __half2float(h1)), 2048.0f)));
+            if (ok0) zacc[hb][gg] = __fmaf_rn(p0, s0.y, zacc[hb][gg]);
+            if (ok1) zacc[hb][gg] = __fmaf_rn(p1, s1.y, zacc[hb][gg]);
+        }
+    }
+
+    // ---- PV on tensor cores: A = V codes^T [16 channels x 16 tokens], B = p * s_v (hi, lo)
+    uint32_t X01, Y01, X23, Y23;
+    const uint8_t* vc = sb + GE::kSeg;
+    if constexpr (D == 128) {
+        const uint32_t wa = *reinterpret_cast<const uint32_t*>(vc + (2 * tig) * GE::kCodeRow + 4 * gid);
+        const uint32_t wb = *reinterpret_cast<const uint32_t*>(vc + (2 * tig + 1) * GE::kCodeRow + 4 * gid);
+        const uint32_t wc = *reinterpret_cast<const uint32_t*>(vc + (2 * tig + 8) * GE::kCodeRow + 4 * gid);
+        const uint32_t wd = *reinterpret_cast<const uint32_t*>(vc + (2 * tig + 9) * GE::kCodeRow + 4 * gid);
+        X01 = __byte_perm(wa, wb, 0x5410);
+        Y01 = __byte_perm(wa, wb, 0x7632);
+        X23 = __byte_perm(wc, wd, 0x5410);
+        Y23 = __byte_perm(wc, wd, 0x7632);
+    } else {
+        const uint32_t wa = *reinterpret_cast<const uint16_t*>(vc + (2 * tig) * GE::kCodeRow + 2 * gid);
+        const uint32_t wb = *reinterpret_cast<const uint16_t*>(vc + (2 * tig + 1) * GE::kCodeRow + 2 * gid);
+        const uint32_t wc = *reinterpret_cast<const uint16_t*>(vc + (2 * tig + 8) * GE::kCodeRow + 2 * gid);
+        const uint32_t wd = *reinterpret_cast<const uint16_t*>(vc + (2 * tig + 9) * GE::kCodeRow + 2 * gid);
+        X01 = __byte_perm(wa, wb, 0x5410);
+        X23 = __byte_perm(wc, wd, 0x5410);
+        Y01 = X01;
+        Y23 = X23;
+    }
+    const uint32_t X01s = X01 >> 10, Y01s = Y01 >> 10, X23s = X23 >> 10, Y23s = Y23 >> 10;
+    // the (hi, lo) part this lane's B column needs: hi for even gid, lo for odd gid
+    const uint32_t sel = (gid & 1) ? 0x7632u : 0x5410u;
+    const int srcA = 8 * tig + (gid >> 1), srcB = srcA + 4;
+    uint32_t Bf[NHB][NG][2];
+#pragma unroll
+    for (int hb = 0; hb < NHB; ++hb)
+#pragma unroll
+        for (int gg = 0; gg < NG; ++gg) {
+            const uint32_t a0 = __shfl_sync(0xffffffffu, Pv[hb][gg][0], srcA);
+            const uint32_t a1 = __shfl_sync(0xffffffffu, Pv[hb][gg][1], srcA);
+            const uint32_t b0 = __shfl_sync(0xffffffffu, Pv[hb][gg][0], srcB);
+            const uint32_t b1 = __shfl_sync(0xffffffffu, Pv[hb][gg][1], srcB);
+            Bf[hb][gg][0] = __byte_perm(a0, b0, sel);
+            Bf[hb][gg][1] = __byte_perm(a1, b1, sel);
+        }
+    static_for<NK>([&](auto mc) {
+        constexpr int mm = decltype(mc)::value;
+        constexpr int gg = mm / KPG;
+        uint32_t A0, A1, A2, A3;
+        v_operand<D, mm>(X01, X01s, Y01, Y01s, X23, X23s, Y23, Y23s, A0, A1, A2, A3);
+#pragma unroll
+        for (int hb = 0; hb < NHB; ++hb) mma16816(O[hb][mm], A0, A1, A2, A3, Bf[hb][gg][0], Bf[hb][gg][1]);
+    });
+}
+
+// INT2 history split on tensor cores. Writes this warp's state into acc_s / ml_s.
+template <int D, int G, int GQ>
+__device__ void int2_split(const SplitArgs& a, int split, int kv, int b, uint8_t* stage_base, uint64_t* bars,
+                           float* acc_s, float (*ml_s)[GQ][2]) {
+    using GE = Geo<D, G>;
+    constexpr int NK = D / 16;          // k-steps (QK) = m-steps (PV)
+    constexpr int NG = D / G;
+    constexpr int KPG = G / 16;         // k-steps per group
+    constexpr int NHB = (GQ + 3) / 4;   // blocks of 4 query heads
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const int gid = lane >> 2, tig = lane & 3;
+    const int h_q = a.h_kv * GQ;
+    const size_t head0 = (size_t)b * h_q + kv * GQ;
+
+    int len = a.hist_len[b];
+    const int cap = min(a.max_hist, a.int2_stride * kPage);
+    if (len < 0 || len > cap) {
+        if (a.debug && threadIdx.x == 0) record_error(&a.dbg->kind, &a.dbg->index, 3, len);
+        len = len < 0 ? 0 : cap;
+    }
+    const int n_pages = (len + kPage - 1) / kPage;
+    const int pg0 = split * a.pages_per_split;
+    const int pg1 = min(n_pages, pg0 + a.pages_per_split);
+    const int first = pg0 + warp;
+    const int n_mine = first < pg1 ? (pg1 - first + kWarps - 1) / kWarps : 0;
+    const int32_t* table = a.int2_tables + (size_t)b * a.int2_stride;
+    // page ids of this warp, 32 at a time across the lanes: chunk c (pages 32c .. 32c+31 of the warp)
+    // lives in ids0 (c even) or ids1 (c odd) and is refilled with chunk c+2 once all its pages are issued
+    int32_t ids0 = lane < n_mine ? table[first + kWarps * lane] : -1;
+    int32_t ids1 = lane + 32 < n_mine ? table[first + kWarps * (lane + 32)] : -1;
+
+    WarpAcc<D, G, GQ> acc;
+    acc.init();
+    auto& O = acc.O;
+    auto& m_run = acc.m_run;
+    auto& l_run = acc.l_run;
+    auto& zacc = acc.zacc;
+
+    // ---- page pipeline: kStages bulk copies in flight per warp
+    uint8_t* my_stage = stage_base + (size_t)warp * kStages * GE::kBlock;
+    const uint32_t stage_s = (uint32_t)__cvta_generic_to_shared(my_stage);
+    const uint32_t bar_s = (uint32_t)__cvta_generic_to_shared(bars + warp * kStages);
+    if (lane == 0) {
+        for (int s = 0; s < kStages; ++s) mbar_init(bar_s + 8 * s, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncwarp();
+    uint32_t valid_mask = 0u;    // bit s: stage s holds a real page
+    // launch arguments used every page, held in registers
+    const uint8_t* const pool_kv = a.int2_pool + (size_t)kv * GE::kBlock;
+    const size_t page_stride = (size_t)a.h_kv * GE::kBlock;
+    const int64_t pool_pages = a.int2_pages;
+    const bool dbg_on = a.debug != 0;
+    auto issue = [&](int j) {
+        const int s = j % kStages;
+        const int32_t phys = __shfl_sync(0xffffffffu, ((j >> 5) & 1) ? ids1 : ids0, j & 31);
+        const bool ok = phys >= 0 && phys < pool_pages;
+        if (!ok && dbg_on && lane == 0) record_error(&a.dbg->kind, &a.dbg->index, 2, phys);
+        valid_mask = ok ? (valid_mask | (1u << s)) : (valid_mask & ~(1u << s));
+        if (lane == 0) {
+            if (ok)
+                bulk_load(stage_s + s * GE::kBlock, pool_kv + (size_t)phys * page_stride, GE::kBlock, bar_s + 8 * s);
+            else
+                mbar_arrive(bar_s + 8 * s);
+        }
+    };
+    for (int j = 0; j < kStages && j < n_mine; ++j) issue(j);
+
+    // the query operands come from q_prep: wait for it (the page copies above are already in flight)
+    pdl_wait();
+    pdl_trigger();
+    QueryOps<D, G, GQ> qo;
+    load_query_ops<D, G, GQ>(a, head0, gid, tig, qo);
     const float pvs = a.pv_scale[kv];
     const float inv_pvs = 1.0f / pvs;         // a power of two: exact
 
@@ -505,163 +720,7 @@ __device__ void int2_split(const SplitArgs& a, int split, int kv, int b, uint8_t
         const int pg = first + kWarps * j;
         const uint8_t* sb = my_stage + s * GE::kBlock;
         if (valid_mask & (1u << s)) {
-            const int nvalid = min(kPage, len - pg * kPage);
-            const bool v0 = gid < nvalid, v1 = gid + 8 < nvalid;
-
-            // ---- QK^T on tensor cores: A = K codes [16 tokens x 16 channels], B = query parts
-            uint32_t kw0[2], kw1[2];
-            if constexpr (D == 128) {
-                const uint2 u0 = *reinterpret_cast<const uint2*>(sb + gid * GE::kCodeRow + 8 * tig);
-                const uint2 u1 = *reinterpret_cast<const uint2*>(sb + (gid + 8) * GE::kCodeRow + 8 * tig);
-                kw0[0] = u0.x; kw0[1] = u0.y; kw1[0] = u1.x; kw1[1] = u1.y;
-            } else {
-                kw0[0] = *reinterpret_cast<const uint32_t*>(sb + gid * GE::kCodeRow + 4 * tig);
-                kw1[0] = *reinterpret_cast<const uint32_t*>(sb + (gid + 8) * GE::kCodeRow + 4 * tig);
-                kw0[1] = kw1[1] = 0u;
-            }
-            float S1[NG][NHB][4], S2[NG][4];
-#pragma unroll
-            for (int gg = 0; gg < NG; ++gg) {
-#pragma unroll
-                for (int e = 0; e < 4; ++e) S2[gg][e] = 0.0f;
-#pragma unroll
-                for (int hb = 0; hb < NHB; ++hb)
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) S1[gg][hb][e] = 0.0f;
-            }
-            static_for<NK>([&](auto kkc) {
-                constexpr int kk = decltype(kkc)::value;
-                uint32_t A0, A1, A2, A3;
-                k_operand<D, kk>(kw0, kw1, A0, A1, A2, A3);
-                constexpr int gg = kk / KPG;
-#pragma unroll
-                for (int hb = 0; hb < NHB; ++hb) mma16816(S1[gg][hb], A0, A1, A2, A3, qB1[kk][hb][0], qB1[kk][hb][1]);
-                mma16816(S2[gg], A0, A1, A2, A3, qB2[kk][0], qB2[kk][1]);
-            });
-
-            // ---- logits (hi + lo, log2 units) for tokens gid and gid+8 of head 4hb + tig
-            const __half2* ksz = reinterpret_cast<const __half2*>(sb + GE::kCodeBytes);
-            const __half2* vsz = reinterpret_cast<const __half2*>(sb + GE::kSeg + GE::kCodeBytes);
-            uint32_t Pv[NHB][NG][2];     // p * s_v * 2^sigma per token slot, as (hi, lo) fp16 pair
-#pragma unroll
-            for (int hb = 0; hb < NHB; ++hb) {
-                float lh[2], ll[2];
-#pragma unroll
-                for (int slot = 0; slot < 2; ++slot) {
-                    const int tok = gid + 8 * slot;
-                    float dh = 0.0f, dl = 0.0f;
-#pragma unroll
-                    for (int gg = 0; gg < NG; ++gg) {
-                        const float lo_raw = (GQ == 8) ? S2[gg][2 * slot + hb] : S2[gg][2 * slot];
-                        const float s_hi = __fmul_rn(S1[gg][hb][2 * slot], kap_h[hb]);
-                        const float s_r = __fmaf_rn(S1[gg][hb][2 * slot + 1], kap_m[hb], __fmul_rn(lo_raw, kap_l[hb]));
-                        const float2 sz = __half22float2(ksz[tok * NG + gg]);
-                        float p1, e1, p2, e2, t1, e3;
-                        two_prod(sz.x, s_hi, p1, e1);
-                        two_prod(sz.y, qs_hi[hb][gg], p2, e2);
-                        two_sum(p1, p2, t1, e3);
-                        const float low = __fadd_rn(__fadd_rn(e1, e2),
-                                                    __fadd_rn(e3, __fmaf_rn(sz.x, s_r, __fmul_rn(sz.y, qs_lo[hb][gg]))));
-                        if (NG == 1) {
-                            dh = t1;
-                            dl = low;
-                        } else {
-                            float t2, e4;
-                            two_sum(dh, t1, t2, e4);
-                            dh = t2;
-                            dl = __fadd_rn(dl, __fadd_rn(low, e4));
-                        }
-                    }
-                    lh[slot] = dh;          // already in log2 units (the query carries the scale)
-                    ll[slot] = dl;
-                }
-                const bool ok0 = v0 && (4 * hb + tig < GQ), ok1 = v1 && (4 * hb + tig < GQ);
-                if (!ok0) { lh[0] = -INFINITY; ll[0] = 0.0f; }
-                if (!ok1) { lh[1] = -INFINITY; ll[1] = 0.0f; }
-                // online softmax over the page (lanes sharing tig hold the same head)
-                float mp = fmaxf(lh[0], lh[1]);
-                mp = fmaxf(mp, __shfl_xor_sync(0xffffffffu, mp, 4));
-                mp = fmaxf(mp, __shfl_xor_sync(0xffffffffu, mp, 8));
-                mp = fmaxf(mp, __shfl_xor_sync(0xffffffffu, mp, 16));
-                // lazy reference: raised only when a logit passes it by more than 2^kSoftmaxHeadroomLog2,
-                // so p <= 2^8 and the O rescale is rare
-                if (__any_sync(0xffffffffu, mp > m_run[hb] + (float)kSoftmaxHeadroomLog2)) {
-                    const float mn = fmaxf(m_run[hb], mp);
-                    const float alpha = ex2(m_run[hb] - mn);
-                    m_run[hb] = mn;
-                    l_run[hb] *= alpha;
-#pragma unroll
-                    for (int mm = 0; mm < NK; ++mm)
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) O[hb][mm][e] *= alpha;
-#pragma unroll
-                    for (int gg = 0; gg < NG; ++gg) zacc[hb][gg] *= alpha;
-                }
-                const float p0 = ex2(__fadd_rn(__fsub_rn(lh[0], m_run[hb]), ll[0]));
-                const float p1 = ex2(__fadd_rn(__fsub_rn(lh[1], m_run[hb]), ll[1]));
-                l_run[hb] = __fadd_rn(l_run[hb], __fadd_rn(p0, p1));
-#pragma unroll
-                for (int gg = 0; gg < NG; ++gg) {
-                    const float2 s0 = __half22float2(vsz[gid * NG + gg]);
-                    const float2 s1 = __half22float2(vsz[(gid + 8) * NG + gg]);
-                    // p <= 2^8 and s_v <= (2/3) max T_v, and 2^sigma leaves that headroom, so
-                    // x <= 32752 (1 + tiny): fp16 without a clamp
-                    const float x0 = ok0 ? __fmul_rn(__fmul_rn(p0, s0.x), pvs) : 0.0f;
-                    const float x1 = ok1 ? __fmul_rn(__fmul_rn(p1, s1.x), pvs) : 0.0f;
-                    const __half h0 = __float2half_rn(x0), h1 = __float2half_rn(x1);
-                    Pv[hb][gg][0] = pack_half2(h0, __float2half_rn(__fmul_rn(__fsub_rn(x0, __half2float(h0)), 2048.0f)));
-                    Pv[hb][gg][1] = pack_half2(h1, __float2half_rn(__fmul_rn(__fsub_rn(x1, __half2float(h1)), 2048.0f)));
-                    if (ok0) zacc[hb][gg] = __fmaf_rn(p0, s0.y, zacc[hb][gg]);
-                    if (ok1) zacc[hb][gg] = __fmaf_rn(p1, s1.y, zacc[hb][gg]);
-                }
-            }
-
-            // ---- PV on tensor cores: A = V codes^T [16 channels x 16 tokens], B = p * s_v (hi, lo)
-            uint32_t X01, Y01, X23, Y23;
-            const uint8_t* vc = sb + GE::kSeg;
-            if constexpr (D == 128) {
-                const uint32_t wa = *reinterpret_cast<const uint32_t*>(vc + (2 * tig) * GE::kCodeRow + 4 * gid);
-                const uint32_t wb = *reinterpret_cast<const uint32_t*>(vc + (2 * tig + 1) * GE::kCodeRow + 4 * gid);
-                const uint32_t wc = *reinterpret_cast<const uint32_t*>(vc + (2 * tig + 8) * GE::kCodeRow + 4 * gid);
-                const uint32_t wd = *reinterpret_cast<const uint32_t*>(vc + (2 * tig + 9) * GE::kCodeRow + 4 * gid);
-                X01 = __byte_perm(wa, wb, 0x5410);
-                Y01 = __byte_perm(wa, wb, 0x7632);
-                X23 = __byte_perm(wc, wd, 0x5410);
-                Y23 = __byte_perm(wc, wd, 0x7632);
-            } else {
-                const uint32_t wa = *reinterpret_cast<const uint16_t*>(vc + (2 * tig) * GE::kCodeRow + 2 * gid);
-                const uint32_t wb = *reinterpret_cast<const uint16_t*>(vc + (2 * tig + 1) * GE::kCodeRow + 2 * gid);
-                const uint32_t wc = *reinterpret_cast<const uint16_t*>(vc + (2 * tig + 8) * GE::kCodeRow + 2 * gid);
-                const uint32_t wd = *reinterpret_cast<const uint16_t*>(vc + (2 * tig + 9) * GE::kCodeRow + 2 * gid);
-                X01 = __byte_perm(wa, wb, 0x5410);
-                X23 = __byte_perm(wc, wd, 0x5410);
-                Y01 = X01;
-                Y23 = X23;
-            }
-            const uint32_t X01s = X01 >> 10, Y01s = Y01 >> 10, X23s = X23 >> 10, Y23s = Y23 >> 10;
-            // the (hi, lo) part this lane's B column needs: hi for even gid, lo for odd gid
-            const uint32_t sel = (gid & 1) ? 0x7632u : 0x5410u;
-            const int srcA = 8 * tig + (gid >> 1), srcB = srcA + 4;
-            uint32_t Bf[NHB][NG][2];
-#pragma unroll
-            for (int hb = 0; hb < NHB; ++hb)
-#pragma unroll
-                for (int gg = 0; gg < NG; ++gg) {
-                    const uint32_t a0 = __shfl_sync(0xffffffffu, Pv[hb][gg][0], srcA);
-                    const uint32_t a1 = __shfl_sync(0xffffffffu, Pv[hb][gg][1], srcA);
-                    const uint32_t b0 = __shfl_sync(0xffffffffu, Pv[hb][gg][0], srcB);
-                    const uint32_t b1 = __shfl_sync(0xffffffffu, Pv[hb][gg][1], srcB);
-                    Bf[hb][gg][0] = __byte_perm(a0, b0, sel);
-                    Bf[hb][gg][1] = __byte_perm(a1, b1, sel);
-                }
-            static_for<NK>([&](auto mc) {
-                constexpr int mm = decltype(mc)::value;
-                constexpr int gg = mm / KPG;
-                uint32_t A0, A1, A2, A3;
-                v_operand<D, mm>(X01, X01s, Y01, Y01s, X23, X23s, Y23, Y23s, A0, A1, A2, A3);
-#pragma unroll
-                for (int hb = 0; hb < NHB; ++hb) mma16816(O[hb][mm], A0, A1, A2, A3, Bf[hb][gg][0], Bf[hb][gg][1]);
-            });
+            int2_page<D, G, GQ>(sb, min(kPage, len - pg * kPage), gid, tig, pvs, qo, acc);
         }
         __syncwarp();
         if (j + kStages < n_mine) {
@@ -724,6 +783,131 @@ __device__ void int2_split(const SplitArgs& a, int split, int kv, int b, uint8_t
             const float o1 = __fmaf_rn(O[hb][mm][3], 0x1p-11f, O[hb][mm][2]) * sc1 + zacc[hb][gg];
             atomicAdd(&acc_s[h * D + 16 * mm + gid], o0 * f);
             atomicAdd(&acc_s[h * D + 16 * mm + gid + 8], o1 * f);
+        }
+    }
+}
+
+// Shared-prefix split: prefix pages [pg0, pg1) of one KV head for a group of kWarps sequences
+// (warp w serves sequence kWarps * sg + w). Each page is copied once into the CTA's ring of
+// kWarps * kStages stages and read by every warp, so the prefix crosses HBM once per group rather than
+// once per sequence. Thread 0 issues the copies; a stage is refilled once all warps have released it
+// (an mbarrier with one arrival per warp). Every wait is bounded. Each warp writes the partial of its
+// own sequence's query heads to slot ps.
+template <int D, int G, int GQ>
+__device__ void prefix_split(const SplitArgs& a, int ps, int kv, int sg, uint8_t* stage_base, uint64_t* bars) {
+    using GE = Geo<D, G>;
+    constexpr int NK = D / 16, NG = D / G, KPG = G / 16, NHB = (GQ + 3) / 4;
+    constexpr int S = kWarps * kStages;
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const int gid = lane >> 2, tig = lane & 3;
+    const int h_q = a.h_kv * GQ;
+    const int b = sg * kWarps + warp;
+    const bool active = b < a.batch;
+    const int pg0 = ps * a.prefix_pages_per_split;
+    const int n = max(0, min(a.prefix_pages, pg0 + a.prefix_pages_per_split) - pg0);
+    const uint32_t stage_s = (uint32_t)__cvta_generic_to_shared(stage_base);
+    const uint32_t full_s = (uint32_t)__cvta_generic_to_shared(bars);     // S barriers: page landed
+    const uint32_t empty_s = full_s + 8 * S;                                // S barriers: all warps done
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < S; ++i) {
+            mbar_init(full_s + 8 * i, 1);
+            mbar_init(empty_s + 8 * i, kWarps);
+        }
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+    const uint8_t* const pool_kv = a.int2_pool + (size_t)kv * GE::kBlock;
+    const size_t page_stride = (size_t)a.h_kv * GE::kBlock;
+    const int32_t* table = a.prefix_table + pg0;
+    int issued = 0;                                  // thread 0: pages copied (or marked) so far
+    auto issue = [&](int i) {
+        const int st = i % S;
+        const int32_t phys = table[i];
+        if (phys >= 0 && phys < a.int2_pages) {
+            bulk_load(stage_s + st * GE::kBlock, pool_kv + (size_t)phys * page_stride, GE::kBlock, full_s + 8 * st);
+        } else {
+            if (a.debug) record_error(&a.dbg->kind, &a.dbg->index, 2, phys);
+            mbar_arrive(full_s + 8 * st);
+        }
+        issued = i + 1;
+    };
+    if (threadIdx.x == 0)
+        for (int i = 0; i < S && i < n; ++i) issue(i);
+
+    // the query operands come from q_prep: wait for it (the first copies are already in flight)
+    pdl_wait();
+    pdl_trigger();
+    QueryOps<D, G, GQ> qo;
+    WarpAcc<D, G, GQ> acc;
+    acc.init();
+    const size_t head0 = (size_t)(active ? b : 0) * h_q + kv * GQ;
+    if (active) load_query_ops<D, G, GQ>(a, head0, gid, tig, qo);
+    const float pvs = a.pv_scale[kv];
+
+    bool failed = false;
+    int i = 0;
+    for (; i < n; ++i) {
+        const int st = i % S;
+        const uint32_t phase = (i / S) & 1;
+        if (!__all_sync(0xffffffffu, mbar_wait(full_s + 8 * st, phase))) {
+            failed = true;
+            break;
+        }
+        const int32_t phys = table[i];
+        if (active && phys >= 0 && phys < a.int2_pages)
+            int2_page<D, G, GQ>(stage_base + (size_t)st * GE::kBlock, kPage, gid, tig, pvs, qo, acc);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(empty_s + 8 * st);
+        if (threadIdx.x == 0 && i + S < n) {
+            // the stage is reused once every warp has released page i
+            if (mbar_wait(empty_s + 8 * st, phase)) issue(i + S);
+            else record_error(&a.dbg->kind, &a.dbg->index, 4, pg0 + i);
+        }
+    }
+    if (failed && lane == 0) record_error(&a.dbg->kind, &a.dbg->index, 4, pg0 + i);
+    if (threadIdx.x == 0) {
+        // copies still in flight land before the CTA (and its shared memory) goes away (bounded)
+        for (int j = i; j < issued; ++j) (void)mbar_wait(full_s + 8 * (j % S), (j / S) & 1);
+    }
+    if (!active) return;
+    auto& O = acc.O;
+    auto& m_run = acc.m_run;
+    auto& l_run = acc.l_run;
+    auto& zacc = acc.zacc;
+    if (failed) {
+#pragma unroll
+        for (int hb = 0; hb < NHB; ++hb) { m_run[hb] = -INFINITY; l_run[hb] = 0.0f; }
+    }
+    // ---- this warp's partial: m = its running max, l and acc relative to it
+    const float inv_pvs = 1.0f / pvs;
+#pragma unroll
+    for (int hb = 0; hb < NHB; ++hb) {
+        float l = l_run[hb];
+        l += __shfl_xor_sync(0xffffffffu, l, 4);
+        l += __shfl_xor_sync(0xffffffffu, l, 8);
+        l += __shfl_xor_sync(0xffffffffu, l, 16);
+        float z[NG];
+#pragma unroll
+        for (int gg = 0; gg < NG; ++gg) {
+            z[gg] = zacc[hb][gg];
+            z[gg] += __shfl_xor_sync(0xffffffffu, z[gg], 4);
+            z[gg] += __shfl_xor_sync(0xffffffffu, z[gg], 8);
+            z[gg] += __shfl_xor_sync(0xffffffffu, z[gg], 16);
+        }
+        const int h = 4 * hb + tig;
+        if (h >= GQ) continue;
+        float* dst = a.partials + (((size_t)b * h_q + kv * GQ + h) * a.total_splits + ps) * (D + 2);
+        if (gid == 0) {
+            dst[0] = m_run[hb];
+            dst[1] = l;
+        }
+#pragma unroll
+        for (int mm = 0; mm < NK; ++mm) {
+            const int gg = mm / KPG;
+            const float sc0 = pos_weight(mm) * inv_pvs;
+            const float sc1 = pos_weight((D == 128) ? mm : 4 + mm) * inv_pvs;
+            dst[2 + 16 * mm + gid] = __fmaf_rn(O[hb][mm][1], 0x1p-11f, O[hb][mm][0]) * sc0 + z[gg];
+            dst[2 + 16 * mm + gid + 8] = __fmaf_rn(O[hb][mm][3], 0x1p-11f, O[hb][mm][2]) * sc1 + z[gg];
         }
     }
 }
@@ -919,7 +1103,7 @@ __device__ __noinline__ void merge_group(const SplitArgs& a, int kv, int b, floa
                     const int sp = s0 + k;
                     if (sp >= T) break;
                     const float x = v[k] * w_s[h * T + sp];
-                    if (sp < a.int2_splits) ai += x; else ab[h] += x;
+                    if (sp < a.prefix_splits + a.int2_splits) ai += x; else ab[h] += x;
                 }
             }
             acc_s[h * D + c] = ai;
@@ -952,12 +1136,22 @@ template <int D, int G, int GQ>
 __global__ void __launch_bounds__(kWarps * 32, GQ == 8 ? 3 : 4)
 split_kernel(SplitArgs a) {
     extern __shared__ __align__(128) uint8_t dyn_smem[];
-    __shared__ __align__(8) uint64_t bars[kWarps * kStages];
+    __shared__ __align__(8) uint64_t bars[2 * kWarps * kStages];
     __shared__ __align__(16) float acc_s[GQ * D];
     __shared__ float ml_s[kWarps][GQ][2];
     __shared__ float p_s[kWarps][16][GQ];
 
-    const int split = blockIdx.x, kv = blockIdx.y, b = blockIdx.z;
+    // flat grid: the shared-prefix CTAs (prefix split fastest, then KV head, then sequence group),
+    // then one CTA per (split, KV head, sequence), split fastest
+    const int cta = blockIdx.x;
+    if (cta < a.n_prefix_ctas) {
+        const int ps = cta % a.prefix_splits, rest = cta / a.prefix_splits;
+        prefix_split<D, G, GQ>(a, ps, rest % a.h_kv, rest / a.h_kv, dyn_smem, bars);
+        return;
+    }
+    const int reg = cta - a.n_prefix_ctas;
+    const int t_reg = a.int2_splits + a.bf16_splits;
+    const int split = reg % t_reg, kv = (reg / t_reg) % a.h_kv, b = reg / t_reg / a.h_kv;
     const int h_q = a.h_kv * GQ;
     for (int i = threadIdx.x; i < GQ * D; i += blockDim.x) acc_s[i] = 0.0f;
     __syncthreads();
@@ -980,7 +1174,7 @@ split_kernel(SplitArgs a) {
             const float mw = ml_s[w2][h][0];
             if (mw != -INFINITY) ll += ml_s[w2][h][1] * fast_exp2(mw - mm);
         }
-        float* dst = a.partials + (((size_t)b * h_q + kv * GQ + h) * a.total_splits + split) * (D + 2);
+        float* dst = a.partials + (((size_t)b * h_q + kv * GQ + h) * a.total_splits + a.prefix_splits + split) * (D + 2);
         for (int c = threadIdx.x; c < D; c += blockDim.x) dst[2 + c] = acc_s[h * D + c];
         if (threadIdx.x == 0) { dst[0] = mm; dst[1] = ll; }
     }
@@ -993,7 +1187,7 @@ split_kernel(SplitArgs a) {
             ticket_s = atomicAdd(a.counters + (size_t)b * a.h_kv + kv, 1);
         }
         __syncthreads();
-        if (ticket_s == a.total_splits - 1) {
+        if (ticket_s == t_reg - 1) {
             __threadfence();
             merge_group<D, GQ>(a, kv, b, acc_s, reinterpret_cast<float*>(dyn_smem));
         }
@@ -1096,8 +1290,9 @@ cudaError_t launch_split(const SplitArgs& a, int batch, cudaStream_t st) {
     const size_t smem = SplitSmem<D, G, GQ>::kDynamic;
     const cudaError_t attr = smem_opt_in<split_kernel<D, G, GQ>>(smem);
     if (attr != cudaSuccess) return attr;
-    dim3 grid(a.total_splits, a.h_kv, batch);
-    return launch_pdl(kern, grid, dim3(kWarps * 32), smem, st, a);
+    const long long ctas = a.n_prefix_ctas + (long long)(a.int2_splits + a.bf16_splits) * a.h_kv * batch;
+    if (ctas > 0x7fffffffLL) return cudaErrorInvalidValue;
+    return launch_pdl(kern, dim3((unsigned)ctas), dim3(kWarps * 32), smem, st, a);
 }
 
 template <int D, int G>
@@ -1155,7 +1350,7 @@ int split_ctas_per_sm(const Shape& s) {
 
 }  // namespace
 
-DecodePlan plan_decode(const Shape& s, int num_sms, int batch, int max_hist) {
+DecodePlan plan_decode(const Shape& s, int num_sms, int batch, int max_hist, int prefix_pages) {
     DecodePlan p{};
     const int max_pages = (max_hist + kPage - 1) / kPage;
     const long long units_ll = (long long)batch * s.h_kv;     // batch <= 65535 is checked by every caller
@@ -1178,6 +1373,14 @@ DecodePlan plan_decode(const Shape& s, int num_sms, int batch, int max_hist) {
     p.pages_per_split = max_pages > 0 ? (max_pages + splits - 1) / splits : 1;
     p.int2_splits = max_pages > 0 ? (max_pages + p.pages_per_split - 1) / p.pages_per_split : 1;
     p.total_splits = p.int2_splits + p.bf16_splits;
+    if (prefix_pages > 0) {
+        // shared prefix: each prefix CTA serves kWarps sequences, every warp walks all the CTA's pages, so
+        // a prefix split of kMaxPagesPerSplit / kWarps pages costs about one INT2 split of the longest size
+        p.prefix_pages_per_split = kMaxPagesPerSplit / kWarps;
+        p.prefix_splits = (prefix_pages + p.prefix_pages_per_split - 1) / p.prefix_pages_per_split;
+        p.n_prefix_ctas = p.prefix_splits * s.h_kv * ((batch + kWarps - 1) / kWarps);
+        p.total_splits += p.prefix_splits;
+    }
     p.ws_partials = align256((size_t)batch * s.h_q * p.total_splits * (s.d + 2) * sizeof(float));
     p.ws_qrot = align256((size_t)batch * s.h_q * 3 * s.d * sizeof(__half)) +
                 align256((size_t)batch * s.h_q * sizeof(float)) +
@@ -1185,7 +1388,7 @@ DecodePlan plan_decode(const Shape& s, int num_sms, int batch, int max_hist) {
     p.ws_counters = align256((size_t)units * sizeof(int));
     p.ws_total = p.ws_partials + p.ws_qrot + p.ws_counters;
     // the last-CTA merge keeps its weights in the page-stage shared memory (at least 12 KB)
-    p.fuse_merge = (size_t)(s.h_q / s.h_kv) * p.total_splits <= kFuseWeights;
+    p.fuse_merge = prefix_pages == 0 && (size_t)(s.h_q / s.h_kv) * p.total_splits <= kFuseWeights;
     return p;
 }
 
@@ -1230,6 +1433,9 @@ cudaError_t launch_decode(const Shape& s, const LayerParams& prm, const DecodePl
     sa.bf16_splits = plan.bf16_splits;
     sa.bf16_pages_per_split = plan.bf16_pages_per_split;
     sa.total_splits = plan.total_splits;
+    sa.prefix_table = a.prefix_table; sa.prefix_pages = a.prefix_pages;
+    sa.prefix_pages_per_split = plan.prefix_pages_per_split; sa.prefix_splits = plan.prefix_splits;
+    sa.n_prefix_ctas = plan.n_prefix_ctas; sa.batch = a.batch;
     sa.scale_log2 = sl2_hi;
     sa.scale_log2_lo = sl2_lo;
     sa.debug = s.debug; sa.dbg = dbg;
@@ -1255,9 +1461,9 @@ cudaError_t launch_decode(const Shape& s, const LayerParams& prm, const DecodePl
     ProfScope ps_merge(prof, OSCAR_KERNEL_MERGE, st);
     if (s.d == 128)
         return launch_pdl(merge_kernel<128>, dim3(a.batch * s.h_q), dim3(4 * 128), 0, st, (const float*)partials,
-                          prm.r_vt, a.out, s.h_q, g, plan.int2_splits, plan.total_splits);
+                          prm.r_vt, a.out, s.h_q, g, plan.prefix_splits + plan.int2_splits, plan.total_splits);
     return launch_pdl(merge_kernel<64>, dim3(a.batch * s.h_q), dim3(4 * 64), 0, st, (const float*)partials,
-                      prm.r_vt, a.out, s.h_q, g, plan.int2_splits, plan.total_splits);
+                      prm.r_vt, a.out, s.h_q, g, plan.prefix_splits + plan.int2_splits, plan.total_splits);
 }
 
 }  // namespace oscar

@@ -149,7 +149,10 @@ struct DecodePlan {
     int pages_per_split;    // INT2 pages per split
     int bf16_splits;        // splits over the BF16 segment
     int bf16_pages_per_split;  // BF16 pages per BF16 split
-    int total_splits;
+    int prefix_pages_per_split;  // shared-prefix pages per prefix CTA (0 without a shared prefix)
+    int prefix_splits;      // prefix partial slots per query head
+    int n_prefix_ctas;      // prefix CTAs: prefix_splits x H_kv x sequence groups of the CTA's warp count
+    int total_splits;       // partial slots per query head: prefix + INT2 + BF16
     size_t ws_partials;     // bytes of split partials
     size_t ws_qrot;         // bytes of rotated-query digits, exponents and digit sums
     size_t ws_counters;     // bytes of per-(sequence, KV head) tickets of the last-CTA merge
@@ -157,10 +160,11 @@ struct DecodePlan {
     size_t ws_total;
 };
 
-DecodePlan plan_decode(const Shape& s, int num_sms, int batch, int max_hist);
+DecodePlan plan_decode(const Shape& s, int num_sms, int batch, int max_hist, int prefix_pages = 0);
 
 struct DecodeArgs {
     const void* q;
+    const int32_t* prefix_table = nullptr; int prefix_pages = 0;   // shared prefix (cascade), or none
     const uint8_t* int2_pool; int64_t int2_pages;
     const int32_t* int2_tables; int int2_stride;
     const int32_t* hist_len; int max_hist;

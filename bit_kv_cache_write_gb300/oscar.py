@@ -45,6 +45,9 @@ _SIGS = {
     "oscar_decode_workspace_size": (_sz, [_vp, _i, _i]),
     "oscar_decode": (_i, [_vp, _i, _vp, _vp, _i64, _vp, _i, _vp, _i, _vp, _i64, _vp, _i, _vp,
                           _vp, _vp, _sz, _i, _vp]),
+    "oscar_decode_shared_prefix_workspace_size": (_sz, [_vp, _i, _i, _i]),
+    "oscar_decode_shared_prefix": (_i, [_vp, _i, _vp, _vp, _i64, _vp, _i, _vp, _i, _vp, _i, _vp, _i64, _vp, _i, _vp,
+                                        _vp, _vp, _sz, _i, _vp]),
     "oscar_int2_page_bytes": (_sz, [_vp]),
     "oscar_bf16_page_bytes": (_sz, [_vp]),
     "oscar_status_string": (ctypes.c_char_p, [_i]),
@@ -188,6 +191,31 @@ def oscar_decode(ctx, layer, q, int2_pool, int2_tables, hist_len, max_hist, bf16
         workspace.numel() * workspace.element_size(), batch, _stream(stream)), "oscar_decode")
 
 
+def oscar_decode_shared_prefix_workspace_size(ctx, batch, prefix_pages, max_hist):
+    return lib().oscar_decode_shared_prefix_workspace_size(ctx, batch, prefix_pages, max_hist)
+
+
+def oscar_decode_shared_prefix(ctx, layer, q, int2_pool, prefix_table, int2_tables, hist_len, max_hist, bf16_pool,
+                               bf16_tables, bf16_len, out, workspace, stream=None):
+    """oscar_decode with a prefix shared by the whole batch: prefix_table int32 [P] (full pages), then each
+    sequence's own pages in int2_tables [B][stride] with hist_len counting the tokens after the prefix."""
+    import torch
+    batch = q.shape[0]
+    i2_pages = int2_pool.numel() // oscar_int2_page_bytes(ctx)
+    bf_pages = bf16_pool.numel() * 2 // oscar_bf16_page_bytes(ctx)
+    _check(lib().oscar_decode_shared_prefix(
+        ctx, layer, _dptr(q, torch.bfloat16, "q"),
+        _dptr(int2_pool, torch.uint8, "int2_pool"), i2_pages,
+        _dptr(prefix_table, torch.int32, "prefix_table"), prefix_table.numel() if prefix_table is not None else 0,
+        _dptr(int2_tables, torch.int32, "int2_tables"), int2_tables.shape[1] if int2_tables is not None else 0,
+        _dptr(hist_len, torch.int32, "hist_len"), int(max_hist),
+        _dptr(bf16_pool, torch.bfloat16, "bf16_pool"), bf_pages,
+        _dptr(bf16_tables, torch.int32, "bf16_tables"), bf16_tables.shape[1],
+        _dptr(bf16_len, torch.int32, "bf16_len"),
+        _dptr(out, torch.float32, "out"), _dptr(workspace, None, "workspace"),
+        workspace.numel() * workspace.element_size(), batch, _stream(stream)), "oscar_decode_shared_prefix")
+
+
 def oscar_calibration_workspace_size(n, n_q_heads, n_kv_heads, head_dim):
     return lib().oscar_calibration_workspace_size(n, n_q_heads, n_kv_heads, head_dim)
 
@@ -287,6 +315,14 @@ class Oscar:
                                 bf16_len, out, stream=None):
         oscar_decode_static_workspace(self.ctx, layer, q, int2_pool, int2_tables, hist_len, max_hist, bf16_pool,
                                       bf16_tables, bf16_len, out, stream)
+
+    def decode_shared_prefix_workspace_size(self, batch, prefix_pages, max_hist):
+        return oscar_decode_shared_prefix_workspace_size(self.ctx, batch, prefix_pages, max_hist)
+
+    def decode_shared_prefix(self, layer, q, int2_pool, prefix_table, int2_tables, hist_len, max_hist, bf16_pool,
+                             bf16_tables, bf16_len, out, workspace, stream=None):
+        oscar_decode_shared_prefix(self.ctx, layer, q, int2_pool, prefix_table, int2_tables, hist_len, max_hist,
+                                   bf16_pool, bf16_tables, bf16_len, out, workspace, stream)
 
     def int2_page_bytes(self):
         return oscar_int2_page_bytes(self.ctx)

@@ -220,6 +220,35 @@ OSCAR_API oscar_status oscar_decode(oscar_ctx_t* ctx, int layer, const void* q,
                           float* out, void* workspace, size_t workspace_bytes,
                           int batch, void* stream);
 
+/* Paged decode attention when every sequence of the batch starts with the
+ * same INT2 pages (a radix prefix-cache hit; [QBIT] serving pipeline: radix
+ * prefix cache; [ABS]: prefix caching preserved). Sequence b's INT2 history
+ * is the shared prefix, prefix_pages full pages (16 * prefix_pages tokens)
+ * listed once in prefix_table, followed by its own hist_len[b] tokens in
+ * int2_tables[b] (logical page 0 of that table holds token 16*prefix_pages).
+ * The result equals oscar_decode over the concatenated tables. The shared
+ * pages are read once per (KV head, group of four sequences) instead of once
+ * per sequence.
+ *   prefix_table: DEVICE int32 [prefix_pages] page ids in the INT2 pool.
+ *   prefix_pages: >= 0; 0 makes the call an oscar_decode.
+ * Other arguments as for oscar_decode; hist_len / max_hist count only the
+ * tokens after the prefix. The BF16 segment (sink + recent) stays per
+ * sequence. workspace: >= oscar_decode_shared_prefix_workspace_size(ctx,
+ * batch, prefix_pages, max_hist) bytes, 256-byte aligned. Asynchronous on
+ * `stream`. */
+OSCAR_API size_t oscar_decode_shared_prefix_workspace_size(const oscar_ctx_t* ctx, int batch, int prefix_pages,
+                                                          int max_hist);
+OSCAR_API oscar_status oscar_decode_shared_prefix(oscar_ctx_t* ctx, int layer, const void* q,
+                                                  const void* int2_pool, int64_t int2_pool_pages,
+                                                  const int32_t* prefix_table, int prefix_pages,
+                                                  const int32_t* int2_tables, int int2_table_stride,
+                                                  const int32_t* hist_len, int max_hist,
+                                                  const void* bf16_pool, int64_t bf16_pool_pages,
+                                                  const int32_t* bf16_tables, int bf16_table_stride,
+                                                  const int32_t* bf16_len,
+                                                  float* out, void* workspace, size_t workspace_bytes,
+                                                  int batch, void* stream);
+
 /* oscar_decode without a caller workspace. The pages have no counterpart for
  * this call. It exists for callers that cannot allocate device memory:
  *   - a host engine that only hands the op its input and output buffers;
