@@ -152,3 +152,60 @@ def test_lloyd_max_against_the_uniform_grid_in_attention():
     for name in rel:
         print("%s: out rel-L2 %.3f | K rel %.3f | V rel %.3f" % (name, rel[name]["out"], rel[name]["k"], rel[name]["v"]))
     assert rel["lloyd_max"]["k"] < rel["uniform"]["k"] and rel["lloyd_max"]["v"] < rel["uniform"]["v"]
+
+
+# ---- the stored ("dyadic") codebook: Lloyd-Max levels rounded to multiples of y_1 / 8
+
+def test_dyadic_codebook_rounds_the_published_levels():
+    delta, levels, cut = lloyd_max.dyadic_codebook()
+    y, _ = lloyd_max.lloyd_max_gaussian(4)
+    assert abs(delta * 8 - 0.4528) < 5e-4                      # inner level kept (Max 1960)
+    assert abs(levels[3] - 1.510) < 0.02                       # outer level 27 delta ~ 1.528
+    assert round(y[3] / delta) == 27                           # 26.7 rounds to 27
+    np.testing.assert_allclose(cut, [-17.5 * delta, 0.0, 17.5 * delta], atol=1e-15)
+    # distortion on N(0, 1) within 0.1 % of the unrounded quantizer's 0.1175
+    d_dyadic = lloyd_max.gaussian_distortion(levels, cut)
+    d_exact = lloyd_max.gaussian_distortion(*lloyd_max.lloyd_max_gaussian(4))
+    assert d_exact <= d_dyadic < d_exact * 1.001
+
+
+def test_dyadic_levels_are_linear_in_the_code_and_its_low_bit():
+    # l(c) = -27 + 17.5 c + 1.5 b0: what lets a decoder keep exact integer dot products with one bit plane
+    for c in range(4):
+        assert lloyd_max.DYADIC_STEPS[c] == -27 + 17.5 * c + 1.5 * (c & 1)
+
+
+def test_dyadic_quantizer_brute_force_and_degenerate_groups():
+    rng = np.random.default_rng(7)
+    d, group = 16, 8
+    r = np.eye(d)
+    t = np.full(d, 50.0)
+    x = rng.standard_normal((200, d)) * 3.0 + 1.0
+    x[0, :group] = 2.5                                         # a flat group: sigma = 0
+    q = lloyd_max.quantize_dyadic(x, r, t, group)
+    delta, levels, _ = lloyd_max.dyadic_codebook()
+    xh = x.astype(np.float32).astype(np.float64)
+    for i in range(1, 200):
+        for gi in range(d // group):
+            seg = xh[i, gi * group:(gi + 1) * group]
+            mu, sigma = seg.mean(), seg.std()
+            for j, v in enumerate(seg):
+                dist = np.abs((v - mu) / sigma - levels)
+                best = int(np.flatnonzero(dist == dist.min())[0])       # ties take the lower level
+                assert q["codes"][i, gi * group + j] == best
+            assert q["scale"][i, gi] == np.float16(sigma * delta) and q["zero"][i, gi] == np.float16(mu)
+    assert (q["codes"][0, :group] == 0).all() and q["scale"][0, 0] == 0
+    deq = lloyd_max.dequantize_dyadic(q["codes"], q["scale"], q["zero"], group)
+    np.testing.assert_allclose(deq[0, :group], np.float16(2.5))    # flat group dequantizes to its mean
+
+
+def test_dyadic_mse_on_gaussian_groups_matches_the_codebook_distortion():
+    rng = np.random.default_rng(11)
+    d = group = 128
+    x = rng.standard_normal((4000, d))
+    q = lloyd_max.quantize_dyadic(x, np.eye(d), np.full(d, 1e9), group)
+    deq = lloyd_max.dequantize_dyadic(q["codes"], q["scale"], q["zero"], group)
+    sig = q["sigma"][:, 0:1]
+    mse = np.mean(((x - deq) / sig) ** 2)
+    delta, levels, cut = lloyd_max.dyadic_codebook()
+    assert abs(mse - lloyd_max.gaussian_distortion(levels, cut)) < 0.01
