@@ -125,6 +125,8 @@ oscar_status oscar_create(const oscar_config_t* cfg, oscar_ctx_t** out) {
     if (c.page_size != oscar::kPage) return fail(OSCAR_ERR_UNSUPPORTED, "page_size %d != 16", c.page_size);
     if (c.n_q_heads % c.n_kv_heads || !pow2_in(c.n_q_heads / c.n_kv_heads, 1, 8))
         return fail(OSCAR_ERR_UNSUPPORTED, "H_q/H_kv = %d/%d not in {1, 2, 4, 8}", c.n_q_heads, c.n_kv_heads);
+    if (c.codebook != OSCAR_CODEBOOK_UNIFORM && c.codebook != OSCAR_CODEBOOK_LLOYD_MAX)
+        return fail(OSCAR_ERR_UNSUPPORTED, "codebook %d not in {0 (uniform), 1 (Lloyd-Max)}", c.codebook);
     if (c.sink + c.recent > oscar::kMaxBf16)
         return fail(OSCAR_ERR_UNSUPPORTED, "sink + recent = %d above %d", c.sink + c.recent, oscar::kMaxBf16);
     if (fault("alloc")) return fail(OSCAR_ERR_NO_MEMORY, "injected allocation failure (OSCAR_FAULT=alloc)");
@@ -137,6 +139,7 @@ oscar_status oscar_create(const oscar_config_t* cfg, oscar_ctx_t** out) {
     s.page = c.page_size; s.sink = c.sink; s.recent = c.recent;
     s.sm_scale = c.sm_scale > 0.0f ? (double)c.sm_scale : 1.0 / std::sqrt((double)c.head_dim);
     s.debug = c.debug_bounds ? 1 : 0;
+    s.codebook = c.codebook;
     ctx->calibrated.assign(c.n_layers, 0);
 
     cudaError_t e = cudaGetDevice(&ctx->device);

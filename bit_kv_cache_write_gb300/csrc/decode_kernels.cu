@@ -631,8 +631,254 @@ __device__ __forceinline__ void int2_page(const uint8_t* sb, int nvalid, int gid
     });
 }
 
-// INT2 history split on tensor cores. Writes this warp's state into acc_s / ml_s.
+// K operand of the low-bit plane: b0 * 2^(2p'-24) per code, the same positions and scale as k_operand.
+template <int POS>
+__device__ __forceinline__ uint32_t low_bit_pair(uint32_t w, uint32_t w10) {
+    if constexpr (POS <= 4) return w & (0x00010001u << (2 * POS));
+    else return w10 & (0x00010001u << (2 * (POS - 5)));
+}
+
+template <int D, int KK>
+__device__ __forceinline__ void k_operand_b0(const uint32_t (&kw0)[2], const uint32_t (&kw1)[2], uint32_t& A0,
+                                             uint32_t& A1, uint32_t& A2, uint32_t& A3) {
+    constexpr int W = KK / 4, P = 2 * (KK % 4);
+    const uint32_t w0 = kw0[W], w1 = kw1[W];
+    A0 = low_bit_pair<P>(w0, w0 >> 10); A1 = low_bit_pair<P>(w1, w1 >> 10);
+    A2 = low_bit_pair<P + 1>(w0, w0 >> 10); A3 = low_bit_pair<P + 1>(w1, w1 >> 10);
+}
+
+// V operand of the Lloyd-Max codebook at position POS: (17.5 c + 1.5 b0) 2^(2p') as an exact normal
+// fp16 pair, from c 2^(2p') (as code_pair_normal) and the fused 1.5 (1024 + b0 2^(2p')) - 1536.
+template <int POS>
+__device__ __forceinline__ uint32_t level_pair_normal(uint32_t w, uint32_t w10) {
+    const uint32_t c = code_pair_normal<POS>(w, w10);
+    const uint32_t hb = low_bit_pair<POS>(w, w10) | 0x64006400u;
+    const __half2 b = __hfma2(*reinterpret_cast<const __half2*>(&hb), __float2half2_rn(1.5f), __float2half2_rn(-1536.0f));
+    const __half2 r = __hfma2(*reinterpret_cast<const __half2*>(&c), __float2half2_rn(17.5f), b);
+    return *reinterpret_cast<const uint32_t*>(&r);
+}
+
+template <int D, int MM>
+__device__ __forceinline__ void v_operand_lm(uint32_t X01, uint32_t X01s, uint32_t Y01, uint32_t Y01s, uint32_t X23,
+                                             uint32_t X23s, uint32_t Y23, uint32_t Y23s, uint32_t& A0, uint32_t& A1,
+                                             uint32_t& A2, uint32_t& A3) {
+    if constexpr (D == 128) {
+        A0 = level_pair_normal<MM>(X01, X01s); A1 = level_pair_normal<MM>(Y01, Y01s);
+        A2 = level_pair_normal<MM>(X23, X23s); A3 = level_pair_normal<MM>(Y23, Y23s);
+    } else {
+        A0 = level_pair_normal<MM>(X01, X01s); A1 = level_pair_normal<4 + MM>(X01, X01s);
+        A2 = level_pair_normal<MM>(X23, X23s); A3 = level_pair_normal<4 + MM>(X23, X23s);
+    }
+}
+
+// int2_page for the Lloyd-Max codebook: code c holds level l(c) = -27 + 17.5 c + 1.5 b0 (b0 the code's
+// low bit) in units of the stored scale, k = zero + scale * l(c). Q.K runs on two exact planes, the
+// codes (as in int2_page) and their low bits, each with its own accumulators:
+//   q . k = scale * (17.5 q.c + 1.5 q.b0) + (zero - 27 scale) * sum(q).
+// P.V takes A = (17.5 c + 1.5 b0) 2^(2p'), exact normal fp16 values (at most 54 * 2^8), and the
+// zero-point sums use zero - 27 scale.
 template <int D, int G, int GQ>
+__device__ __forceinline__ void int2_page_lm(const uint8_t* sb, int nvalid, int gid, int tig, float pvs,
+                                          const QueryOps<D, G, GQ>& qo, WarpAcc<D, G, GQ>& acc) {
+    using GE = Geo<D, G>;
+    constexpr int NK = D / 16, NG = D / G, KPG = G / 16, NHB = (GQ + 3) / 4;
+    const auto& qB1 = qo.qB1;
+    const auto& qB2 = qo.qB2;
+    const auto& kap_h = qo.kap_h;
+    const auto& kap_m = qo.kap_m;
+    const auto& kap_l = qo.kap_l;
+    const auto& qs_hi = qo.qs_hi;
+    const auto& qs_lo = qo.qs_lo;
+    auto& O = acc.O;
+    auto& m_run = acc.m_run;
+    auto& l_run = acc.l_run;
+    auto& zacc = acc.zacc;
+    const bool v0 = gid < nvalid, v1 = gid + 8 < nvalid;
+
+    // ---- QK^T on tensor cores: A = K codes [16 tokens x 16 channels], B = query parts
+    uint32_t kw0[2], kw1[2];
+    if constexpr (D == 128) {
+        const uint2 u0 = *reinterpret_cast<const uint2*>(sb + gid * GE::kCodeRow + 8 * tig);
+        const uint2 u1 = *reinterpret_cast<const uint2*>(sb + (gid + 8) * GE::kCodeRow + 8 * tig);
+        kw0[0] = u0.x; kw0[1] = u0.y; kw1[0] = u1.x; kw1[1] = u1.y;
+    } else {
+        kw0[0] = *reinterpret_cast<const uint32_t*>(sb + gid * GE::kCodeRow + 4 * tig);
+        kw1[0] = *reinterpret_cast<const uint32_t*>(sb + (gid + 8) * GE::kCodeRow + 4 * tig);
+        kw0[1] = kw1[1] = 0u;
+    }
+    float S1[NG][NHB][4], S2[NG][4], T1[NG][NHB][4], T2[NG][4];
+#pragma unroll
+    for (int gg = 0; gg < NG; ++gg) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) { S2[gg][e] = 0.0f; T2[gg][e] = 0.0f; }
+#pragma unroll
+        for (int hb = 0; hb < NHB; ++hb)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) { S1[gg][hb][e] = 0.0f; T1[gg][hb][e] = 0.0f; }
+    }
+    static_for<NK>([&](auto kkc) {
+        constexpr int kk = decltype(kkc)::value;
+        uint32_t A0, A1, A2, A3, B0, B1, B2, B3;
+        k_operand<D, kk>(kw0, kw1, A0, A1, A2, A3);
+        k_operand_b0<D, kk>(kw0, kw1, B0, B1, B2, B3);
+        constexpr int gg = kk / KPG;
+#pragma unroll
+        for (int hb = 0; hb < NHB; ++hb) {
+            mma16816(S1[gg][hb], A0, A1, A2, A3, qB1[kk][hb][0], qB1[kk][hb][1]);
+            mma16816(T1[gg][hb], B0, B1, B2, B3, qB1[kk][hb][0], qB1[kk][hb][1]);
+        }
+        mma16816(S2[gg], A0, A1, A2, A3, qB2[kk][0], qB2[kk][1]);
+        mma16816(T2[gg], B0, B1, B2, B3, qB2[kk][0], qB2[kk][1]);
+    });
+
+    // ---- logits (hi + lo, log2 units) for tokens gid and gid+8 of head 4hb + tig
+    const __half2* ksz = reinterpret_cast<const __half2*>(sb + GE::kCodeBytes);
+    const __half2* vsz = reinterpret_cast<const __half2*>(sb + GE::kSeg + GE::kCodeBytes);
+    uint32_t Pv[NHB][NG][2];     // p * s_v * 2^sigma per token slot, as (hi, lo) fp16 pair
+#pragma unroll
+    for (int hb = 0; hb < NHB; ++hb) {
+        float lh[2], ll[2];
+#pragma unroll
+        for (int slot = 0; slot < 2; ++slot) {
+            const int tok = gid + 8 * slot;
+            float dh = 0.0f, dl = 0.0f;
+#pragma unroll
+            for (int gg = 0; gg < NG; ++gg) {
+                const float lo_c = (GQ == 8) ? S2[gg][2 * slot + hb] : S2[gg][2 * slot];
+                const float lo_b = (GQ == 8) ? T2[gg][2 * slot + hb] : T2[gg][2 * slot];
+                // q.c and q.b0: exact hi parts (integers on the digit grid) and rounded low parts
+                const float c_hi = __fmul_rn(S1[gg][hb][2 * slot], kap_h[hb]);
+                const float c_r = __fmaf_rn(S1[gg][hb][2 * slot + 1], kap_m[hb], __fmul_rn(lo_c, kap_l[hb]));
+                const float b_hi = __fmul_rn(T1[gg][hb][2 * slot], kap_h[hb]);
+                const float b_r = __fmaf_rn(T1[gg][hb][2 * slot + 1], kap_m[hb], __fmul_rn(lo_b, kap_l[hb]));
+                // y = 17.5 q.c + 1.5 q.b0 as y_hi + y_lo (1.5 b_hi is exact: b0 sums have one bit per code)
+                float a1, ea, y_hi, ey;
+                two_prod(17.5f, c_hi, a1, ea);
+                two_sum(a1, __fmul_rn(1.5f, b_hi), y_hi, ey);
+                const float y_lo = __fadd_rn(__fadd_rn(ea, ey), __fmaf_rn(17.5f, c_r, __fmul_rn(1.5f, b_r)));
+                const float2 sz = __half22float2(ksz[tok * NG + gg]);
+                // zero - 27 scale as zp_hi + zp_lo (27 scale is exact)
+                float zp_hi, zp_lo;
+                two_sum(sz.y, __fmul_rn(-27.0f, sz.x), zp_hi, zp_lo);
+                float p1, e1, p2, e2, t1, e3;
+                two_prod(sz.x, y_hi, p1, e1);
+                two_prod(zp_hi, qs_hi[hb][gg], p2, e2);
+                two_sum(p1, p2, t1, e3);
+                const float low = __fadd_rn(__fadd_rn(__fadd_rn(e1, e2), e3),
+                                            __fmaf_rn(sz.x, y_lo, __fmaf_rn(zp_hi, qs_lo[hb][gg],
+                                                                            __fmul_rn(zp_lo, qs_hi[hb][gg]))));
+                if (NG == 1) {
+                    dh = t1;
+                    dl = low;
+                } else {
+                    float t2, e4;
+                    two_sum(dh, t1, t2, e4);
+                    dh = t2;
+                    dl = __fadd_rn(dl, __fadd_rn(low, e4));
+                }
+            }
+            lh[slot] = dh;          // already in log2 units (the query carries the scale)
+            ll[slot] = dl;
+        }
+        const bool ok0 = v0 && (4 * hb + tig < GQ), ok1 = v1 && (4 * hb + tig < GQ);
+        if (!ok0) { lh[0] = -INFINITY; ll[0] = 0.0f; }
+        if (!ok1) { lh[1] = -INFINITY; ll[1] = 0.0f; }
+        // online softmax over the page (lanes sharing tig hold the same head)
+        float mp = fmaxf(lh[0], lh[1]);
+        mp = fmaxf(mp, __shfl_xor_sync(0xffffffffu, mp, 4));
+        mp = fmaxf(mp, __shfl_xor_sync(0xffffffffu, mp, 8));
+        mp = fmaxf(mp, __shfl_xor_sync(0xffffffffu, mp, 16));
+        // lazy reference: raised only when a logit passes it by more than 2^kSoftmaxHeadroomLog2,
+        // so p <= 2^8 and the O rescale is rare
+        if (__any_sync(0xffffffffu, mp > m_run[hb] + (float)kSoftmaxHeadroomLog2)) {
+            const float mn = fmaxf(m_run[hb], mp);
+            const float alpha = ex2(m_run[hb] - mn);
+            m_run[hb] = mn;
+            l_run[hb] *= alpha;
+#pragma unroll
+            for (int mm = 0; mm < NK; ++mm)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) O[hb][mm][e] *= alpha;
+#pragma unroll
+            for (int gg = 0; gg < NG; ++gg) zacc[hb][gg] *= alpha;
+        }
+        const float p0 = ex2(__fadd_rn(__fsub_rn(lh[0], m_run[hb]), ll[0]));
+        const float p1 = ex2(__fadd_rn(__fsub_rn(lh[1], m_run[hb]), ll[1]));
+        l_run[hb] = __fadd_rn(l_run[hb], __fadd_rn(p0, p1));
+#pragma unroll
+        for (int gg = 0; gg < NG; ++gg) {
+            const float2 s0 = __half22float2(vsz[gid * NG + gg]);
+            const float2 s1 = __half22float2(vsz[(gid + 8) * NG + gg]);
+            // p <= 2^8 and s_v <= (2/3) max T_v, and 2^sigma leaves that headroom, so
+            // x <= 32752 (1 + tiny): fp16 without a clamp
+            const float x0 = ok0 ? __fmul_rn(__fmul_rn(p0, s0.x), pvs) : 0.0f;
+            const float x1 = ok1 ? __fmul_rn(__fmul_rn(p1, s1.x), pvs) : 0.0f;
+            const __half h0 = __float2half_rn(x0), h1 = __float2half_rn(x1);
+            Pv[hb][gg][0] = pack_half2(h0, __float2half_rn(__fmul_rn(__fsub_rn(x0, __half2float(h0)), 2048.0f)));
+            Pv[hb][gg][1] = pack_half2(h1, __float2half_rn(__fmul_rn(__fsub_rn(x1, __half2float(h1)), 2048.0f)));
+            if (ok0) zacc[hb][gg] = __fmaf_rn(p0, __fmaf_rn(-27.0f, s0.x, s0.y), zacc[hb][gg]);
+            if (ok1) zacc[hb][gg] = __fmaf_rn(p1, __fmaf_rn(-27.0f, s1.x, s1.y), zacc[hb][gg]);
+        }
+    }
+
+    // ---- PV on tensor cores: A = V codes^T [16 channels x 16 tokens], B = p * s_v (hi, lo)
+    uint32_t X01, Y01, X23, Y23;
+    const uint8_t* vc = sb + GE::kSeg;
+    if constexpr (D == 128) {
+        const uint32_t wa = *reinterpret_cast<const uint32_t*>(vc + (2 * tig) * GE::kCodeRow + 4 * gid);
+        const uint32_t wb = *reinterpret_cast<const uint32_t*>(vc + (2 * tig + 1) * GE::kCodeRow + 4 * gid);
+        const uint32_t wc = *reinterpret_cast<const uint32_t*>(vc + (2 * tig + 8) * GE::kCodeRow + 4 * gid);
+        const uint32_t wd = *reinterpret_cast<const uint32_t*>(vc + (2 * tig + 9) * GE::kCodeRow + 4 * gid);
+        X01 = __byte_perm(wa, wb, 0x5410);
+        Y01 = __byte_perm(wa, wb, 0x7632);
+        X23 = __byte_perm(wc, wd, 0x5410);
+        Y23 = __byte_perm(wc, wd, 0x7632);
+    } else {
+        const uint32_t wa = *reinterpret_cast<const uint16_t*>(vc + (2 * tig) * GE::kCodeRow + 2 * gid);
+        const uint32_t wb = *reinterpret_cast<const uint16_t*>(vc + (2 * tig + 1) * GE::kCodeRow + 2 * gid);
+        const uint32_t wc = *reinterpret_cast<const uint16_t*>(vc + (2 * tig + 8) * GE::kCodeRow + 2 * gid);
+        const uint32_t wd = *reinterpret_cast<const uint16_t*>(vc + (2 * tig + 9) * GE::kCodeRow + 2 * gid);
+        X01 = __byte_perm(wa, wb, 0x5410);
+        X23 = __byte_perm(wc, wd, 0x5410);
+        Y01 = X01;
+        Y23 = X23;
+    }
+    const uint32_t X01s = X01 >> 10, Y01s = Y01 >> 10, X23s = X23 >> 10, Y23s = Y23 >> 10;
+    // the (hi, lo) part this lane's B column needs: hi for even gid, lo for odd gid
+    const uint32_t sel = (gid & 1) ? 0x7632u : 0x5410u;
+    const int srcA = 8 * tig + (gid >> 1), srcB = srcA + 4;
+    uint32_t Bf[NHB][NG][2];
+#pragma unroll
+    for (int hb = 0; hb < NHB; ++hb)
+#pragma unroll
+        for (int gg = 0; gg < NG; ++gg) {
+            const uint32_t a0 = __shfl_sync(0xffffffffu, Pv[hb][gg][0], srcA);
+            const uint32_t a1 = __shfl_sync(0xffffffffu, Pv[hb][gg][1], srcA);
+            const uint32_t b0 = __shfl_sync(0xffffffffu, Pv[hb][gg][0], srcB);
+            const uint32_t b1 = __shfl_sync(0xffffffffu, Pv[hb][gg][1], srcB);
+            Bf[hb][gg][0] = __byte_perm(a0, b0, sel);
+            Bf[hb][gg][1] = __byte_perm(a1, b1, sel);
+        }
+    static_for<NK>([&](auto mc) {
+        constexpr int mm = decltype(mc)::value;
+        constexpr int gg = mm / KPG;
+        uint32_t A0, A1, A2, A3;
+        v_operand_lm<D, mm>(X01, X01s, Y01, Y01s, X23, X23s, Y23, Y23s, A0, A1, A2, A3);
+#pragma unroll
+        for (int hb = 0; hb < NHB; ++hb) mma16816(O[hb][mm], A0, A1, A2, A3, Bf[hb][gg][0], Bf[hb][gg][1]);
+    });
+}
+
+// The page body of the context's codebook.
+template <int D, int G, int GQ, int CB>
+__device__ __forceinline__ void page_body(const uint8_t* sb, int nvalid, int gid, int tig, float pvs,
+                                          const QueryOps<D, G, GQ>& qo, WarpAcc<D, G, GQ>& acc) {
+    if constexpr (CB == OSCAR_CODEBOOK_LLOYD_MAX) int2_page_lm<D, G, GQ>(sb, nvalid, gid, tig, pvs, qo, acc);
+    else int2_page<D, G, GQ>(sb, nvalid, gid, tig, pvs, qo, acc);
+}
+
+// INT2 history split on tensor cores. Writes this warp's state into acc_s / ml_s.
+template <int D, int G, int GQ, int CB>
 __device__ void int2_split(const SplitArgs& a, int split, int kv, int b, uint8_t* stage_base, uint64_t* bars,
                            float* acc_s, float (*ml_s)[GQ][2]) {
     using GE = Geo<D, G>;
@@ -720,7 +966,7 @@ __device__ void int2_split(const SplitArgs& a, int split, int kv, int b, uint8_t
         const int pg = first + kWarps * j;
         const uint8_t* sb = my_stage + s * GE::kBlock;
         if (valid_mask & (1u << s)) {
-            int2_page<D, G, GQ>(sb, min(kPage, len - pg * kPage), gid, tig, pvs, qo, acc);
+            page_body<D, G, GQ, CB>(sb, min(kPage, len - pg * kPage), gid, tig, pvs, qo, acc);
         }
         __syncwarp();
         if (j + kStages < n_mine) {
@@ -793,7 +1039,7 @@ __device__ void int2_split(const SplitArgs& a, int split, int kv, int b, uint8_t
 // once per sequence. Thread 0 issues the copies; a stage is refilled once all warps have released it
 // (an mbarrier with one arrival per warp). Every wait is bounded. Each warp writes the partial of its
 // own sequence's query heads to slot ps.
-template <int D, int G, int GQ>
+template <int D, int G, int GQ, int CB>
 __device__ void prefix_split(const SplitArgs& a, int ps, int kv, int sg, uint8_t* stage_base, uint64_t* bars) {
     using GE = Geo<D, G>;
     constexpr int NK = D / 16, NG = D / G, KPG = G / 16, NHB = (GQ + 3) / 4;
@@ -855,7 +1101,7 @@ __device__ void prefix_split(const SplitArgs& a, int ps, int kv, int sg, uint8_t
         }
         const int32_t phys = table[i];
         if (active && phys >= 0 && phys < a.int2_pages)
-            int2_page<D, G, GQ>(stage_base + (size_t)st * GE::kBlock, kPage, gid, tig, pvs, qo, acc);
+            page_body<D, G, GQ, CB>(stage_base + (size_t)st * GE::kBlock, kPage, gid, tig, pvs, qo, acc);
         __syncwarp();
         if (lane == 0) mbar_arrive(empty_s + 8 * st);
         if (threadIdx.x == 0 && i + S < n) {
@@ -1132,8 +1378,14 @@ __device__ __noinline__ void merge_group(const SplitArgs& a, int kv, int b, floa
     }
 }
 
-template <int D, int G, int GQ>
-__global__ void __launch_bounds__(kWarps * 32, GQ == 8 ? 3 : 4)
+// Resident CTAs per SM the split kernel is compiled for: the Lloyd-Max body holds a second set of
+// Q.K accumulators.
+__host__ __device__ constexpr int split_min_blocks(int gq, int cb) {
+    return cb == OSCAR_CODEBOOK_LLOYD_MAX ? (gq == 8 ? 2 : 3) : (gq == 8 ? 3 : 4);
+}
+
+template <int D, int G, int GQ, int CB>
+__global__ void __launch_bounds__(kWarps * 32, split_min_blocks(GQ, CB))
 split_kernel(SplitArgs a) {
     extern __shared__ __align__(128) uint8_t dyn_smem[];
     __shared__ __align__(8) uint64_t bars[2 * kWarps * kStages];
@@ -1146,7 +1398,7 @@ split_kernel(SplitArgs a) {
     const int cta = blockIdx.x;
     if (cta < a.n_prefix_ctas) {
         const int ps = cta % a.prefix_splits, rest = cta / a.prefix_splits;
-        prefix_split<D, G, GQ>(a, ps, rest % a.h_kv, rest / a.h_kv, dyn_smem, bars);
+        prefix_split<D, G, GQ, CB>(a, ps, rest % a.h_kv, rest / a.h_kv, dyn_smem, bars);
         return;
     }
     const int reg = cta - a.n_prefix_ctas;
@@ -1157,7 +1409,7 @@ split_kernel(SplitArgs a) {
     __syncthreads();
 
     if (split < a.int2_splits) {
-        int2_split<D, G, GQ>(a, split, kv, b, dyn_smem, bars, acc_s, ml_s);
+        int2_split<D, G, GQ, CB>(a, split, kv, b, dyn_smem, bars, acc_s, ml_s);
     } else {
         pdl_wait();
         pdl_trigger();
@@ -1284,24 +1536,24 @@ cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t sme
     return cudaLaunchKernelEx(&cfg, kern, args...);
 }
 
-template <int D, int G, int GQ>
+template <int D, int G, int GQ, int CB>
 cudaError_t launch_split(const SplitArgs& a, int batch, cudaStream_t st) {
-    auto kern = split_kernel<D, G, GQ>;
+    auto kern = split_kernel<D, G, GQ, CB>;
     const size_t smem = SplitSmem<D, G, GQ>::kDynamic;
-    const cudaError_t attr = smem_opt_in<split_kernel<D, G, GQ>>(smem);
+    const cudaError_t attr = smem_opt_in<split_kernel<D, G, GQ, CB>>(smem);
     if (attr != cudaSuccess) return attr;
     const long long ctas = a.n_prefix_ctas + (long long)(a.int2_splits + a.bf16_splits) * a.h_kv * batch;
     if (ctas > 0x7fffffffLL) return cudaErrorInvalidValue;
     return launch_pdl(kern, dim3((unsigned)ctas), dim3(kWarps * 32), smem, st, a);
 }
 
-template <int D, int G>
+template <int D, int G, int CB>
 cudaError_t dispatch_gq(int gq, const SplitArgs& a, int batch, cudaStream_t st) {
     switch (gq) {
-        case 1: return launch_split<D, G, 1>(a, batch, st);
-        case 2: return launch_split<D, G, 2>(a, batch, st);
-        case 4: return launch_split<D, G, 4>(a, batch, st);
-        case 8: return launch_split<D, G, 8>(a, batch, st);
+        case 1: return launch_split<D, G, 1, CB>(a, batch, st);
+        case 2: return launch_split<D, G, 2, CB>(a, batch, st);
+        case 4: return launch_split<D, G, 4, CB>(a, batch, st);
+        case 8: return launch_split<D, G, 8, CB>(a, batch, st);
     }
     return cudaErrorInvalidValue;
 }
@@ -1309,7 +1561,7 @@ cudaError_t dispatch_gq(int gq, const SplitArgs& a, int batch, cudaStream_t st) 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 // Resident split CTAs per SM for the shape on the current device (queried once per device).
-template <int D, int G, int GQ>
+template <int D, int G, int GQ, int CB>
 int split_occupancy() {
     static std::atomic<int> occ[64];
     int dev = 0;
@@ -1319,8 +1571,8 @@ int split_occupancy() {
         if (cached > 0) return cached;
     }
     int n = 0;
-    auto kern = split_kernel<D, G, GQ>;
-    if (smem_opt_in<split_kernel<D, G, GQ>>(SplitSmem<D, G, GQ>::kDynamic) != cudaSuccess ||
+    auto kern = split_kernel<D, G, GQ, CB>;
+    if (smem_opt_in<split_kernel<D, G, GQ, CB>>(SplitSmem<D, G, GQ>::kDynamic) != cudaSuccess ||
         cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, kWarps * 32, SplitSmem<D, G, GQ>::kDynamic) !=
             cudaSuccess || n < 1) {
         cudaGetLastError();
@@ -1330,22 +1582,28 @@ int split_occupancy() {
     return n;
 }
 
-template <int D, int G>
+template <int D, int G, int CB>
 int occupancy_gq(int gq) {
     switch (gq) {
-        case 1: return split_occupancy<D, G, 1>();
-        case 2: return split_occupancy<D, G, 2>();
-        case 4: return split_occupancy<D, G, 4>();
-        default: return split_occupancy<D, G, 8>();
+        case 1: return split_occupancy<D, G, 1, CB>();
+        case 2: return split_occupancy<D, G, 2, CB>();
+        case 4: return split_occupancy<D, G, 4, CB>();
+        default: return split_occupancy<D, G, 8, CB>();
     }
 }
 
-int split_ctas_per_sm(const Shape& s) {
+template <int CB>
+int split_ctas_per_sm_cb(const Shape& s) {
     const int gq = s.h_q / s.h_kv;
-    if (s.d == 64) return s.group == 32 ? occupancy_gq<64, 32>(gq) : occupancy_gq<64, 64>(gq);
-    if (s.group == 32) return occupancy_gq<128, 32>(gq);
-    if (s.group == 64) return occupancy_gq<128, 64>(gq);
-    return occupancy_gq<128, 128>(gq);
+    if (s.d == 64) return s.group == 32 ? occupancy_gq<64, 32, CB>(gq) : occupancy_gq<64, 64, CB>(gq);
+    if (s.group == 32) return occupancy_gq<128, 32, CB>(gq);
+    if (s.group == 64) return occupancy_gq<128, 64, CB>(gq);
+    return occupancy_gq<128, 128, CB>(gq);
+}
+
+int split_ctas_per_sm(const Shape& s) {
+    return s.codebook == OSCAR_CODEBOOK_LLOYD_MAX ? split_ctas_per_sm_cb<OSCAR_CODEBOOK_LLOYD_MAX>(s)
+                                                  : split_ctas_per_sm_cb<OSCAR_CODEBOOK_UNIFORM>(s);
 }
 
 }  // namespace
@@ -1445,8 +1703,12 @@ cudaError_t launch_decode(const Shape& s, const LayerParams& prm, const DecodePl
     sa.out = a.out;
 
     ProfScope ps_split(prof, OSCAR_KERNEL_SPLIT, st);
-#define OSCAR_SPLIT_CASE(D_, G_) \
-    if (s.d == D_ && s.group == G_) e = dispatch_gq<D_, G_>(g, sa, a.batch, st); else
+#define OSCAR_SPLIT_CASE(D_, G_)                                                                  \
+    if (s.d == D_ && s.group == G_)                                                               \
+        e = s.codebook == OSCAR_CODEBOOK_LLOYD_MAX                                                \
+                ? dispatch_gq<D_, G_, OSCAR_CODEBOOK_LLOYD_MAX>(g, sa, a.batch, st)               \
+                : dispatch_gq<D_, G_, OSCAR_CODEBOOK_UNIFORM>(g, sa, a.batch, st);                \
+    else
     OSCAR_SPLIT_CASE(64, 32)
     OSCAR_SPLIT_CASE(64, 64)
     OSCAR_SPLIT_CASE(128, 32)

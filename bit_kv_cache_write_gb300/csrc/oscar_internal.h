@@ -51,6 +51,7 @@ struct Shape {
     int h_q, h_kv, d, group, page, sink, recent;
     double sm_scale;
     int debug;
+    int codebook;      // OSCAR_CODEBOOK_UNIFORM or OSCAR_CODEBOOK_LLOYD_MAX
 };
 
 // Opt-in launch timing: event pairs on the launching stream, per kernel class.
@@ -121,6 +122,12 @@ cudaError_t launch_write(const Shape& s, const LayerParams& p, int num_sms,
                          void* int2_pool, int64_t int2_pages, DebugWord* dbg, Profiler* prof, cudaStream_t st);
 
 cudaError_t launch_transpose(const float* src, float* dst, int h, int d, cudaStream_t st);
+
+// Lloyd-Max codebook write / demote (write_lm.cu), same arguments as launch_write.
+cudaError_t launch_write_lm(const Shape& s, const LayerParams& p, int num_sms, const void* k, const void* v,
+                            const int64_t* slots, int n, const void* bf16_pool, int64_t bf16_pages,
+                            const int64_t* src_slots, void* int2_pool, int64_t int2_pages, DebugWord* dbg,
+                            Profiler* prof, cudaStream_t st);
 
 // Offline calibration targets (calib_kernels.cu): Q^T Q and (S V)^T (S V) per KV head, fp64.
 constexpr int kCalibMaxKeys = 8192;                                     // m: calibration keys per head

@@ -377,6 +377,9 @@ cudaError_t launch_write(const Shape& s, const LayerParams& p, int num_sms,
                          cudaStream_t st) {
     // many tokens straight from K/V rows: the tcgen05 kernel (OSCAR_WRITE_PATH=cuda keeps the
     // CUDA-core kernel, for comparisons)
+    if (s.codebook == OSCAR_CODEBOOK_LLOYD_MAX)
+        return launch_write_lm(s, p, num_sms, k, v, slots, n, bf16_pool, bf16_pages, src_slots, int2_pool,
+                               int2_pages, dbg, prof, st);
     const char* path = std::getenv("OSCAR_WRITE_PATH");
     const bool force_cuda = path && std::strcmp(path, "cuda") == 0;
     if (!src_slots && !force_cuda && write_tc_eligible(s, k, v, int2_pool, n))

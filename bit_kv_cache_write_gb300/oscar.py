@@ -31,7 +31,9 @@ class oscar_config_t(ctypes.Structure):
     _fields_ = [("n_layers", ctypes.c_int), ("n_q_heads", ctypes.c_int), ("n_kv_heads", ctypes.c_int),
                 ("head_dim", ctypes.c_int), ("group", ctypes.c_int), ("page_size", ctypes.c_int),
                 ("sink", ctypes.c_int), ("recent", ctypes.c_int), ("sm_scale", ctypes.c_float),
-                ("debug_bounds", ctypes.c_int)]
+                ("debug_bounds", ctypes.c_int), ("codebook", ctypes.c_int)]
+
+OSCAR_CODEBOOK_UNIFORM, OSCAR_CODEBOOK_LLOYD_MAX = 0, 1
 
 
 _lib = None
@@ -117,10 +119,10 @@ def _dptr(t, dtype, name):
 
 
 def oscar_create(n_layers, n_q_heads, n_kv_heads, head_dim, group, page_size=16, sink=64, recent=256,
-                 sm_scale=0.0, debug_bounds=0):
+                 sm_scale=0.0, debug_bounds=0, codebook=OSCAR_CODEBOOK_UNIFORM):
     """Create a context on the current CUDA device; returns an opaque handle (int)."""
     cfg = oscar_config_t(n_layers, n_q_heads, n_kv_heads, head_dim, group, page_size, sink, recent,
-                         float(sm_scale), int(debug_bounds))
+                         float(sm_scale), int(debug_bounds), int(codebook))
     ctx = _vp()
     _check(lib().oscar_create(ctypes.byref(cfg), ctypes.byref(ctx)), "oscar_create")
     return ctx.value

@@ -34,6 +34,16 @@
  *       with every step done in fp32 round-to-nearest-even, in this order.
  *     scale = fp16(rng / 3), zero = fp16(mn).
  *   Dequant: x_deq = code * scale + zero, in the rotated basis.
+ * - With codebook OSCAR_CODEBOOK_LLOYD_MAX (the stronger codebook the [QBIT]
+ *   article's closing part pairs with the rotation) every group is
+ *   normalised by its own mean mu and standard deviation sigma (fp64, over
+ *   the G clipped rotated values) and takes the nearest of the four levels
+ *   delta * (-27, -8, 8, 27): the Gaussian Lloyd-Max levels (+-0.4528,
+ *   +-1.510) rounded to multiples of delta = 0.45278 / 8 (0.0566). The code
+ *   is 0..3 for those levels (ties to the lower one); scale = fp16(sigma *
+ *   delta), zero = fp16(mu); sigma = 0 gives scale 0 and codes 0.
+ *   Dequant: x_deq = zero + scale * l(code), l = (-27, -8, 8, 27). Layout,
+ *   bit order and page size are unchanged.
  * - Decode, per query head h with KV head h / (H_q / H_kv):
  *     logits over the BF16 segment use the unrotated q;
  *     logits over the INT2 history use q_rot = q @ R_k;
@@ -114,6 +124,12 @@ typedef enum {
     OSCAR_ERR_WORKSPACE = -7       /* workspace null or smaller than required */
 } oscar_status;
 
+/* 2-bit codebook of the INT2 history (oscar_config_t.codebook). */
+typedef enum {
+    OSCAR_CODEBOOK_UNIFORM = 0,    /* 4 uniform levels between the group min and max (the pages' OSCAR) */
+    OSCAR_CODEBOOK_LLOYD_MAX = 1   /* 4 Gaussian Lloyd-Max levels, rounded (see below) */
+} oscar_codebook;
+
 typedef struct {
     int n_layers;     /* layers with their own calibration (R_k, R_v, T_k, T_v) */
     int n_q_heads;    /* H_q */
@@ -125,6 +141,7 @@ typedef struct {
     int recent;       /* BF16 recent window (256 in the pages' system) */
     float sm_scale;   /* logit scale; 1/sqrt(d) if <= 0 */
     int debug_bounds; /* nonzero: kernels bounds-check indices into the error word */
+    int codebook;     /* oscar_codebook; 0 (uniform) when zero-initialised */
 } oscar_config_t;
 
 typedef struct oscar_ctx oscar_ctx_t;

@@ -67,8 +67,12 @@ def compare_int2_head(gpu_pool, ref_pool, geo, slots, kind, h, q):
     bad = diff != 0
     if not bad.any():
         return 0
-    lo = np.minimum(g_codes, r_codes).astype(np.float64)
-    near = np.abs(q["u"] - (lo + 0.5)) <= 1e-5
+    lo = np.minimum(g_codes, r_codes).astype(np.int64)
+    if "thresholds" in q:      # Lloyd-Max: the normalised value z against the cut between the two codes
+        cut = np.asarray(q["thresholds"])[np.minimum(lo, 2)]
+        near = np.abs(q["z"] - cut) <= 1e-6
+    else:
+        near = np.abs(q["u"] - (lo + 0.5)) <= 1e-5
     tolerated = bad & (np.abs(diff) == 1) & near
     assert (bad == tolerated).all(), "%s head %d: %d code mismatches outside the boundary band" % (
         kind, h, int((bad & ~tolerated).sum()))
@@ -106,6 +110,7 @@ class DecodeCase:
     def __init__(self, cfg, hist_lens, bf16_lens, layer=0, shared_pages=0, shared_bf16_pages=0,
                  extra_pages=3, stride_pad=2):
         self.cfg = cfg
+        self.codebook = cfg.get("codebook", "uniform")
         d, group, h_kv, h_q = cfg["d"], cfg["group"], cfg["h_kv"], cfg["h_q"]
         self.li, (self.rk, self.rv, self.tk, self.tv) = calibration(cfg, layer)
         self.geo = layout.Int2Geometry(d, group, h_kv)
@@ -140,7 +145,7 @@ class DecodeCase:
             t = np.arange(first, n)
             slots = self.int2_tables[b, t // P].astype(np.int64) * P + t % P
             cache.write_tokens(self.int2_pool, self.geo, k[first:], v[first:], slots,
-                               self.rk, self.rv, self.tk, self.tv, keep=False)
+                               self.rk, self.rv, self.tk, self.tv, keep=False, codebook=self.codebook)
 
         # ---- BF16 pages
         own_bf = [max(0, synth.pages_for(int(n)) - shared_bf16_pages) for n in bf16_lens]
@@ -177,7 +182,7 @@ class DecodeCase:
     def oracle_out(self, seqs=None, heads=None):
         return cache.decode_batch(self.q, self.int2_pool, self.geo, self.int2_tables, self.hist_lens,
                                   self.bf16_pool, self.bf16_tables, self.bf16_lens, self.rk, self.rv,
-                                  self.sm_scale, seqs=seqs, heads=heads)
+                                  self.sm_scale, seqs=seqs, heads=heads, codebook=self.codebook)
 
 
 def check_decode(got, want, max_abs=2e-3, rel_l2=1e-3):
