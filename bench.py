@@ -167,7 +167,10 @@ class GpuWorkload:
         unique = [p_ - shared_pages for p_ in pages]
         total = shared_pages + sum(unique) + B
         max_pages = max(pages)
-        self.ctx = O.Oscar(n_layers=layers, n_q_heads=h_q, n_kv_heads=h_kv, head_dim=d, group=group)
+        self.codebook = cfg.get("codebook", "uniform")
+        self.ctx = O.Oscar(n_layers=layers, n_q_heads=h_q, n_kv_heads=h_kv, head_dim=d, group=group,
+                           codebook=O.OSCAR_CODEBOOK_LLOYD_MAX if self.codebook == "lloyd_max"
+                           else O.OSCAR_CODEBOOK_UNIFORM)
         pb = self.ctx.int2_page_bytes()
         # the sink pages belong to the shared prefix when there is one; otherwise every sequence owns its sink
         self.shared_sink = shared_hist > 0
@@ -539,11 +542,13 @@ def measure_decode(cfg, layers, dev, steps, warmup, local, seed_offset=0, shared
                        "split_bytes": split_bytes, "launches_per_step": launches}
 
 
-def workload_line(name, layers, dev, steps, warmup, local, shared_prefix_call=False):
+def workload_line(name, layers, dev, steps, warmup, local, shared_prefix_call=False, codebook="uniform"):
     """Throughput of one more decode workload at a reduced layer count (its per-layer pages exceed L2).
-    shared_prefix_call: decode through oscar_decode_shared_prefix (the prefix pages given once)."""
+    shared_prefix_call: decode through oscar_decode_shared_prefix (the prefix pages given once);
+    codebook: "uniform" or "lloyd_max" (the cache is written and decoded with it)."""
     import torch
     cfg = workload_cfg(name)
+    cfg["codebook"] = codebook
     wl, graph, m = measure_decode(cfg, layers, dev, steps, warmup, local, shared_prefix_call=shared_prefix_call)
     peak, peak_kind = measured_peak()
     us_layer = 1e6 * m["max_sec"] / steps / layers
@@ -552,6 +557,7 @@ def workload_line(name, layers, dev, steps, warmup, local, shared_prefix_call=Fa
            "int2_history": {"min": int(wl.hist.min()), "max": int(wl.hist.max()), "sum": int(wl.hist.sum())},
            "shared_prefix_int2_tokens": wl.shared_hist,
            "call": "oscar_decode_shared_prefix" if wl.shared_prefix_call else "oscar_decode",
+           "codebook": codebook,
            "us_per_layer": us_layer, "kv_tokens_per_s": wl.tokens_per_layer / (us_layer * 1e-6),
            "kernels": m["kernels"],
            "split_roofline": {"bound": "hbm", "achieved": m["achieved"], "peak": peak, "peak_kind": peak_kind,
@@ -559,7 +565,8 @@ def workload_line(name, layers, dev, steps, warmup, local, shared_prefix_call=Fa
                               "algorithmic_bytes_per_launch": wl.unique_bytes,
                               "logical_bytes_per_launch": wl.logical_bytes,
                               "logical_gbs": wl.logical_bytes / (split_us * 1e-6) / 1e9,
-                              "traffic": kernel_traffic("split", name)},
+                              "traffic": kernel_traffic("split", name + ("_shared_prefix" if shared_prefix_call else "")
+                                                        + ("_lloyd_max" if codebook == "lloyd_max" else ""))},
            "step_gbs": (wl.unique_bytes + demote_bytes(cfg, wl.batch)) / (us_layer * 1e-6) / 1e9,
            "clocks": m["clocks"],
            "l2": "inputs larger than L2: %.2f GB of distinct pages per step" % (layers * wl.unique_bytes / 1e9)}
@@ -661,7 +668,9 @@ def main():
                      "qwen3_32b_mixed16": workload_line("qwen3_32b_mixed16", 4, dev, args.steps, args.warmup,
                                                         local),
                      "qwen3_32b_mixed16_shared_prefix": workload_line("qwen3_32b_mixed16", 4, dev, args.steps,
-                                                                      args.warmup, local, shared_prefix_call=True)}
+                                                                      args.warmup, local, shared_prefix_call=True),
+                     "qwen3_8b_bs1_100k_lloyd_max": workload_line("qwen3_8b_bs1_100k", 8, dev, args.steps,
+                                                                  args.warmup, local, codebook="lloyd_max")}
 
     if rank == 0:
         line = {
