@@ -14,10 +14,11 @@
 //      CTAs of one head agree on it without exchanging a maximum. Each CTA
 //      also writes the exact digit sums of its channels.
 //   2. split: one CTA per (split, KV head, sequence).
-//      - INT2 splits stream page blocks into shared memory with bulk async
-//        copies, four stages per warp. They compute q_rot . codes and
-//        p . codes with mma.sync m16n8k16 on the packed codes, and keep an
-//        online softmax.
+//      - INT2 splits stream page blocks into shared memory, each lane copying
+//        its 16-byte chunks with cp.async, three slots of two pages per warp.
+//        They compute q_rot . codes and p . codes with mma.sync m16n8k16 on
+//        the packed codes, and keep an online softmax; full pages take a body
+//        without per-token masks.
 //      - BF16 splits handle sink + recent on CUDA cores: the last split of each
 //        (sequence, KV head), or the last two when one wave serves few units.
 //      - Each split writes a partial (m, l, acc[d]) per query head of the
@@ -59,7 +60,8 @@ namespace oscar {
 namespace {
 
 constexpr int kWarps = 4;
-constexpr int kStages = 4;
+constexpr int kStages = 4;                         // ring stages per warp of the shared-prefix CTAs
+constexpr int kSlots = 3;                          // two-page pipeline slots per warp of the INT2 splits
 constexpr long long kWaitCycles = 2000000000LL;   // give up on a page copy after ~1 s
 constexpr float kNoMax = -1e30f;                   // running max before any token
 constexpr int kMaxPagesPerSplit = 128;             // longest INT2 split when the grid has many waves
@@ -112,9 +114,17 @@ __device__ __forceinline__ uint32_t code_pair(uint32_t w, uint32_t w10) {
 // Code pair at position POS as a normal fp16 pair c * 2^(2p'): the masked bits form the mantissa of
 // 1024 + c * 2^(2p'), then 1024 is subtracted exactly. Normal operands keep the tensor-core products
 // of P.V at full precision (fp16 subnormal operands lose low bits against larger products).
+// (w & mask) | bias as one three-input logic instruction (lookup table 0xEA = (a & b) | c).
+__device__ __forceinline__ uint32_t and_or(uint32_t w, uint32_t mask, uint32_t bias) {
+    uint32_t r;
+    asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(r) : "r"(w), "r"(mask), "r"(bias));
+    return r;
+}
+
 template <int POS>
 __device__ __forceinline__ uint32_t code_pair_normal(uint32_t w, uint32_t w10) {
-    const uint32_t h = code_pair<POS>(w, w10) | 0x64006400u;
+    const uint32_t h = POS <= 4 ? and_or(w, 0x00030003u << (2 * POS), 0x64006400u)
+                                : and_or(w10, 0x00030003u << (2 * (POS - 5)), 0x64006400u);
     const __half2 r = __hsub2(*reinterpret_cast<const __half2*>(&h), __half2(__ushort_as_half(0x6400), __ushort_as_half(0x6400)));
     return *reinterpret_cast<const uint32_t*>(&r);
 }
@@ -142,6 +152,17 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
     asm volatile("cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
                  :: "r"(dst), "l"(src), "r"(bytes), "r"(bar) : "memory");
 }
+
+// 16-byte asynchronous copy global -> shared (bypassing L1), issued only where `pred` holds, and its
+// commit groups: the issuing thread waits for its own copies; a warp barrier then publishes them to the
+// other lanes.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool pred) {
+    asm volatile("{ .reg .pred p; setp.ne.b32 p, %2, 0; @p cp.async.cg.shared.global [%0], [%1], 16; }"
+                 :: "r"(dst), "l"(src), "r"((int)pred) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" :: "n"(N) : "memory"); }
 
 __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t phase) {
     uint32_t ok;
@@ -321,7 +342,7 @@ struct SplitArgs {
 template <int D, int G, int GQ>
 struct SplitSmem {
     static constexpr int kBlock = Geo<D, G>::kBlock;
-    static constexpr size_t kDynamic = (size_t)kWarps * kStages * kBlock;
+    static constexpr size_t kDynamic = (size_t)kWarps * (kStages > 2 * kSlots ? kStages : 2 * kSlots) * kBlock;
 };
 
 __device__ __forceinline__ float ex2(float x) {
@@ -457,7 +478,7 @@ struct WarpAcc {
 
 // One INT2 page (16 tokens, the first `nvalid` valid) of one KV head, staged in shared memory at sb,
 // folded into the warp's softmax state.
-template <int D, int G, int GQ>
+template <int D, int G, int GQ, bool FULL>
 __device__ __forceinline__ void int2_page(const uint8_t* sb, int nvalid, int gid, int tig, float pvs,
                                           const QueryOps<D, G, GQ>& qo, WarpAcc<D, G, GQ>& acc) {
     using GE = Geo<D, G>;
@@ -473,7 +494,7 @@ __device__ __forceinline__ void int2_page(const uint8_t* sb, int nvalid, int gid
     auto& m_run = acc.m_run;
     auto& l_run = acc.l_run;
     auto& zacc = acc.zacc;
-    const bool v0 = gid < nvalid, v1 = gid + 8 < nvalid;
+    const bool v0 = FULL || gid < nvalid, v1 = FULL || gid + 8 < nvalid;
 
     // ---- QK^T on tensor cores: A = K codes [16 tokens x 16 channels], B = query parts
     uint32_t kw0[2], kw1[2];
@@ -542,17 +563,18 @@ __device__ __forceinline__ void int2_page(const uint8_t* sb, int nvalid, int gid
             lh[slot] = dh;          // already in log2 units (the query carries the scale)
             ll[slot] = dl;
         }
-        const bool ok0 = v0 && (4 * hb + tig < GQ), ok1 = v1 && (4 * hb + tig < GQ);
+        const bool hv = GQ % 4 == 0 || 4 * hb + tig < GQ;
+        const bool ok0 = v0 && hv, ok1 = v1 && hv;
         if (!ok0) { lh[0] = -INFINITY; ll[0] = 0.0f; }
         if (!ok1) { lh[1] = -INFINITY; ll[1] = 0.0f; }
-        // online softmax over the page (lanes sharing tig hold the same head)
-        float mp = fmaxf(lh[0], lh[1]);
-        mp = fmaxf(mp, __shfl_xor_sync(0xffffffffu, mp, 4));
-        mp = fmaxf(mp, __shfl_xor_sync(0xffffffffu, mp, 8));
-        mp = fmaxf(mp, __shfl_xor_sync(0xffffffffu, mp, 16));
-        // lazy reference: raised only when a logit passes it by more than 2^kSoftmaxHeadroomLog2,
-        // so p <= 2^8 and the O rescale is rare
-        if (__any_sync(0xffffffffu, mp > m_run[hb] + (float)kSoftmaxHeadroomLog2)) {
+        // online softmax over the page (lanes sharing tig hold the same head). The reference is lazy:
+        // raised only when a logit passes it by more than 2^kSoftmaxHeadroomLog2, so p <= 2^8 and the
+        // O rescale is rare; only then is the page maximum of each head reduced across its lanes
+        if (__any_sync(0xffffffffu, fmaxf(lh[0], lh[1]) > m_run[hb] + (float)kSoftmaxHeadroomLog2)) {
+            float mp = fmaxf(lh[0], lh[1]);
+            mp = fmaxf(mp, __shfl_xor_sync(0xffffffffu, mp, 4));
+            mp = fmaxf(mp, __shfl_xor_sync(0xffffffffu, mp, 8));
+            mp = fmaxf(mp, __shfl_xor_sync(0xffffffffu, mp, 16));
             const float mn = fmaxf(m_run[hb], mp);
             const float alpha = ex2(m_run[hb] - mn);
             m_run[hb] = mn;
@@ -652,7 +674,8 @@ __device__ __forceinline__ void k_operand_b0(const uint32_t (&kw0)[2], const uin
 template <int POS>
 __device__ __forceinline__ uint32_t level_pair_normal(uint32_t w, uint32_t w10) {
     const uint32_t c = code_pair_normal<POS>(w, w10);
-    const uint32_t hb = low_bit_pair<POS>(w, w10) | 0x64006400u;
+    const uint32_t hb = POS <= 4 ? and_or(w, 0x00010001u << (2 * POS), 0x64006400u)
+                                 : and_or(w10, 0x00010001u << (2 * (POS - 5)), 0x64006400u);
     const __half2 b = __hfma2(*reinterpret_cast<const __half2*>(&hb), __float2half2_rn(1.5f), __float2half2_rn(-1536.0f));
     const __half2 r = __hfma2(*reinterpret_cast<const __half2*>(&c), __float2half2_rn(17.5f), b);
     return *reinterpret_cast<const uint32_t*>(&r);
@@ -677,7 +700,7 @@ __device__ __forceinline__ void v_operand_lm(uint32_t X01, uint32_t X01s, uint32
 //   q . k = scale * (17.5 q.c + 1.5 q.b0) + (zero - 27 scale) * sum(q).
 // P.V takes A = (17.5 c + 1.5 b0) 2^(2p'), exact normal fp16 values (at most 54 * 2^8), and the
 // zero-point sums use zero - 27 scale.
-template <int D, int G, int GQ>
+template <int D, int G, int GQ, bool FULL>
 __device__ __forceinline__ void int2_page_lm(const uint8_t* sb, int nvalid, int gid, int tig, float pvs,
                                           const QueryOps<D, G, GQ>& qo, WarpAcc<D, G, GQ>& acc) {
     using GE = Geo<D, G>;
@@ -693,7 +716,7 @@ __device__ __forceinline__ void int2_page_lm(const uint8_t* sb, int nvalid, int 
     auto& m_run = acc.m_run;
     auto& l_run = acc.l_run;
     auto& zacc = acc.zacc;
-    const bool v0 = gid < nvalid, v1 = gid + 8 < nvalid;
+    const bool v0 = FULL || gid < nvalid, v1 = FULL || gid + 8 < nvalid;
 
     // ---- QK^T on tensor cores: A = K codes [16 tokens x 16 channels], B = query parts
     uint32_t kw0[2], kw1[2];
@@ -780,17 +803,18 @@ __device__ __forceinline__ void int2_page_lm(const uint8_t* sb, int nvalid, int 
             lh[slot] = dh;          // already in log2 units (the query carries the scale)
             ll[slot] = dl;
         }
-        const bool ok0 = v0 && (4 * hb + tig < GQ), ok1 = v1 && (4 * hb + tig < GQ);
+        const bool hv = GQ % 4 == 0 || 4 * hb + tig < GQ;
+        const bool ok0 = v0 && hv, ok1 = v1 && hv;
         if (!ok0) { lh[0] = -INFINITY; ll[0] = 0.0f; }
         if (!ok1) { lh[1] = -INFINITY; ll[1] = 0.0f; }
-        // online softmax over the page (lanes sharing tig hold the same head)
-        float mp = fmaxf(lh[0], lh[1]);
-        mp = fmaxf(mp, __shfl_xor_sync(0xffffffffu, mp, 4));
-        mp = fmaxf(mp, __shfl_xor_sync(0xffffffffu, mp, 8));
-        mp = fmaxf(mp, __shfl_xor_sync(0xffffffffu, mp, 16));
-        // lazy reference: raised only when a logit passes it by more than 2^kSoftmaxHeadroomLog2,
-        // so p <= 2^8 and the O rescale is rare
-        if (__any_sync(0xffffffffu, mp > m_run[hb] + (float)kSoftmaxHeadroomLog2)) {
+        // online softmax over the page (lanes sharing tig hold the same head). The reference is lazy:
+        // raised only when a logit passes it by more than 2^kSoftmaxHeadroomLog2, so p <= 2^8 and the
+        // O rescale is rare; only then is the page maximum of each head reduced across its lanes
+        if (__any_sync(0xffffffffu, fmaxf(lh[0], lh[1]) > m_run[hb] + (float)kSoftmaxHeadroomLog2)) {
+            float mp = fmaxf(lh[0], lh[1]);
+            mp = fmaxf(mp, __shfl_xor_sync(0xffffffffu, mp, 4));
+            mp = fmaxf(mp, __shfl_xor_sync(0xffffffffu, mp, 8));
+            mp = fmaxf(mp, __shfl_xor_sync(0xffffffffu, mp, 16));
             const float mn = fmaxf(m_run[hb], mp);
             const float alpha = ex2(m_run[hb] - mn);
             m_run[hb] = mn;
@@ -870,11 +894,12 @@ __device__ __forceinline__ void int2_page_lm(const uint8_t* sb, int nvalid, int 
 }
 
 // The page body of the context's codebook.
-template <int D, int G, int GQ, int CB>
+// The page body of the context's codebook; FULL: all 16 tokens of the page are valid.
+template <int D, int G, int GQ, int CB, bool FULL>
 __device__ __forceinline__ void page_body(const uint8_t* sb, int nvalid, int gid, int tig, float pvs,
                                           const QueryOps<D, G, GQ>& qo, WarpAcc<D, G, GQ>& acc) {
-    if constexpr (CB == OSCAR_CODEBOOK_LLOYD_MAX) int2_page_lm<D, G, GQ>(sb, nvalid, gid, tig, pvs, qo, acc);
-    else int2_page<D, G, GQ>(sb, nvalid, gid, tig, pvs, qo, acc);
+    if constexpr (CB == OSCAR_CODEBOOK_LLOYD_MAX) int2_page_lm<D, G, GQ, FULL>(sb, nvalid, gid, tig, pvs, qo, acc);
+    else int2_page<D, G, GQ, FULL>(sb, nvalid, gid, tig, pvs, qo, acc);
 }
 
 // INT2 history split on tensor cores. Writes this warp's state into acc_s / ml_s.
@@ -915,35 +940,48 @@ __device__ void int2_split(const SplitArgs& a, int split, int kv, int b, uint8_t
     auto& l_run = acc.l_run;
     auto& zacc = acc.zacc;
 
-    // ---- page pipeline: kStages bulk copies in flight per warp
-    uint8_t* my_stage = stage_base + (size_t)warp * kStages * GE::kBlock;
-    const uint32_t stage_s = (uint32_t)__cvta_generic_to_shared(my_stage);
-    const uint32_t bar_s = (uint32_t)__cvta_generic_to_shared(bars + warp * kStages);
-    if (lane == 0) {
-        for (int s = 0; s < kStages; ++s) mbar_init(bar_s + 8 * s, 1);
-        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    }
-    __syncwarp();
-    uint32_t valid_mask = 0u;    // bit s: stage s holds a real page
+    // ---- page pipeline: kSlots slots of two pages per warp. Every lane copies its 16-byte chunks of a
+    // page with cp.async; one commit group per slot, so waiting for all but the kSlots - 1 newest groups
+    // completes the oldest slot.
+    uint8_t* my_stage = stage_base + (size_t)warp * kSlots * 2 * GE::kBlock;
+    const uint32_t stage_s = (uint32_t)__cvta_generic_to_shared(my_stage) + 16 * lane;
+    constexpr int kChunks = GE::kBlock / 16;                 // 16-byte chunks per page block
+    constexpr int kPerLane = (kChunks + 31) / 32;
+    const int n_pairs = (n_mine + 1) / 2;
+    uint32_t valid_bits = 0u;    // bit 2s + e: page e of slot s holds a real page
     // launch arguments used every page, held in registers
-    const uint8_t* const pool_kv = a.int2_pool + (size_t)kv * GE::kBlock;
+    const uint8_t* const pool_kv = a.int2_pool + (size_t)kv * GE::kBlock + 16 * lane;
     const size_t page_stride = (size_t)a.h_kv * GE::kBlock;
     const int64_t pool_pages = a.int2_pages;
     const bool dbg_on = a.debug != 0;
-    auto issue = [&](int j) {
-        const int s = j % kStages;
-        const int32_t phys = __shfl_sync(0xffffffffu, ((j >> 5) & 1) ? ids1 : ids0, j & 31);
-        const bool ok = phys >= 0 && phys < pool_pages;
-        if (!ok && dbg_on && lane == 0) record_error(&a.dbg->kind, &a.dbg->index, 2, phys);
-        valid_mask = ok ? (valid_mask | (1u << s)) : (valid_mask & ~(1u << s));
-        if (lane == 0) {
-            if (ok)
-                bulk_load(stage_s + s * GE::kBlock, pool_kv + (size_t)phys * page_stride, GE::kBlock, bar_s + 8 * s);
-            else
-                mbar_arrive(bar_s + 8 * s);
-        }
+    auto copy_page = [&](uint32_t dst, int32_t phys, bool ok) {
+        const uint8_t* src = pool_kv + (size_t)(ok ? phys : 0) * page_stride;
+#pragma unroll
+        for (int k = 0; k < kPerLane; ++k)
+            cp_async16(dst + 512 * k, src + 512 * k, ok && (kChunks % 32 == 0 || lane + 32 * k < kChunks));
     };
-    for (int j = 0; j < kStages && j < n_mine; ++j) issue(j);
+    // pages 2i and 2i+1 of the warp into slot s (both in one 32-page chunk of ids: 2i is even)
+    auto issue = [&](int i, int s) {
+        const int j0 = 2 * i;
+        const int32_t cur = ((j0 >> 5) & 1) ? ids1 : ids0;
+        const int32_t p0 = __shfl_sync(0xffffffffu, cur, j0 & 31);
+        const int32_t p1 = __shfl_sync(0xffffffffu, cur, (j0 & 31) + 1);
+        const bool ok0 = p0 >= 0 && p0 < pool_pages;
+        const bool ok1 = j0 + 1 < n_mine && p1 >= 0 && p1 < pool_pages;
+        if (dbg_on && lane == 0) {
+            if (!ok0) record_error(&a.dbg->kind, &a.dbg->index, 2, p0);
+            if (!ok1 && j0 + 1 < n_mine) record_error(&a.dbg->kind, &a.dbg->index, 2, p1);
+        }
+        valid_bits = (valid_bits & ~(3u << (2 * s))) | ((uint32_t)ok0 << (2 * s)) | ((uint32_t)ok1 << (2 * s + 1));
+        const uint32_t dst = stage_s + s * 2 * GE::kBlock;
+        copy_page(dst, p0, ok0);
+        copy_page(dst + GE::kBlock, p1, ok1);
+        cp_async_commit();
+    };
+    for (int i = 0; i < kSlots; ++i) {
+        if (i < n_pairs) issue(i, i);
+        else cp_async_commit();              // empty group: the wait count stays uniform
+    }
 
     // the query operands come from q_prep: wait for it (the page copies above are already in flight)
     pdl_wait();
@@ -953,40 +991,35 @@ __device__ void int2_split(const SplitArgs& a, int split, int kv, int b, uint8_t
     const float pvs = a.pv_scale[kv];
     const float inv_pvs = 1.0f / pvs;         // a power of two: exact
 
-
-    bool failed = false;
-    int j = 0;
-    for (; j < n_mine; ++j) {
-        const int s = j % kStages;
-        const uint32_t phase = (j / kStages) & 1;
-        if (!__all_sync(0xffffffffu, mbar_wait(bar_s + 8 * s, phase))) {
-            failed = true;
-            break;
-        }
-        const int pg = first + kWarps * j;
-        const uint8_t* sb = my_stage + s * GE::kBlock;
-        if (valid_mask & (1u << s)) {
-            page_body<D, G, GQ, CB>(sb, min(kPage, len - pg * kPage), gid, tig, pvs, qo, acc);
-        }
-        __syncwarp();
-        if (j + kStages < n_mine) {
-            const int ji = j + kStages;
-            issue(ji);
-            if ((ji & 31) == 31) {                // chunk ji/32 fully issued: load chunk ji/32 + 2 into its slot
-                const int nj = ji + 33 + lane;
-                const int32_t v = nj < n_mine ? table[first + kWarps * nj] : -1;
-                if ((ji >> 5) & 1) ids1 = v; else ids0 = v;
+    int slot = 0;
+    for (int i = 0; i < n_pairs; ++i) {
+        cp_async_wait<kSlots - 1>();         // this lane's copies of pair i have landed
+        __syncwarp();                        // ... and every other lane's
+        const uint8_t* sb = my_stage + slot * 2 * GE::kBlock;
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            if (valid_bits & (1u << (2 * slot + e))) {
+                // tokens of this page in the sequence: all 16 except on its last page
+                const int nv = len - (first + kWarps * (2 * i + e)) * kPage;
+                if (nv >= kPage) page_body<D, G, GQ, CB, true>(sb + e * GE::kBlock, kPage, gid, tig, pvs, qo, acc);
+                else page_body<D, G, GQ, CB, false>(sb + e * GE::kBlock, nv, gid, tig, pvs, qo, acc);
             }
         }
+        __syncwarp();                        // every lane is done reading the slot before it is refilled
+        if (i + kSlots < n_pairs) {
+            const int ii = i + kSlots;
+            issue(ii, slot);
+            if (((2 * ii + 1) & 31) == 31) {      // chunk (2ii+1)/32 fully issued: load chunk + 2 into its slot
+                const int nj = 2 * ii + 1 + 33 + lane;
+                const int32_t v = nj < n_mine ? table[first + kWarps * nj] : -1;
+                if (((2 * ii + 1) >> 5) & 1) ids1 = v; else ids0 = v;
+            }
+        } else {
+            cp_async_commit();
+        }
+        if (++slot == kSlots) slot = 0;
     }
-    if (failed) {
-        // record the stalled page, then drain the copies still in flight (bounded) before leaving
-        if (lane == 0) record_error(&a.dbg->kind, &a.dbg->index, 4, first + kWarps * j);
-        for (int jj = j; jj < n_mine && jj < j + kStages; ++jj)
-            (void)mbar_wait(bar_s + 8 * (jj % kStages), (jj / kStages) & 1);
-#pragma unroll
-        for (int hb = 0; hb < NHB; ++hb) { m_run[hb] = -INFINITY; l_run[hb] = 0.0f; }
-    }
+    cp_async_wait<0>();
 
     // ---- this warp's state -> shared memory (scaled to the CTA max)
 #pragma unroll
@@ -1101,7 +1134,7 @@ __device__ void prefix_split(const SplitArgs& a, int ps, int kv, int sg, uint8_t
         }
         const int32_t phys = table[i];
         if (active && phys >= 0 && phys < a.int2_pages)
-            page_body<D, G, GQ, CB>(stage_base + (size_t)st * GE::kBlock, kPage, gid, tig, pvs, qo, acc);
+            page_body<D, G, GQ, CB, true>(stage_base + (size_t)st * GE::kBlock, kPage, gid, tig, pvs, qo, acc);
         __syncwarp();
         if (lane == 0) mbar_arrive(empty_s + 8 * st);
         if (threadIdx.x == 0 && i + S < n) {
