@@ -437,8 +437,10 @@ __device__ __forceinline__ void load_query_ops(const SplitArgs& a, size_t head0,
             float h1, e1;
             two_sum(sh, sm * 0x1p-11f, h1, e1);
             const float k20 = kap_h[hb] * 0x1p-20f;
-            qs_hi[hb][gg] = h1 * k20;
-            qs_lo[hb][gg] = __fmaf_rn(sl, 0x1p-22f, e1) * k20;
+            const float qh = h1 * k20;
+            // hi cut to 13 significant bits, so that z * hi is exact for an fp16 zero point z
+            qs_hi[hb][gg] = __uint_as_float(__float_as_uint(qh) & 0xFFFFF800u);
+            qs_lo[hb][gg] = __fadd_rn(__fsub_rn(qh, qs_hi[hb][gg]), __fmaf_rn(sl, 0x1p-22f, e1) * k20);
         }
     }
     {
@@ -461,6 +463,7 @@ struct WarpAcc {
     static constexpr int NK = D / 16, NG = D / G, NHB = (GQ + 3) / 4;
     float O[NHB][NK][4];
     float m_run[NHB], l_run[NHB], zacc[NHB][NG];
+    bool valid[NHB];                 // relative-logit bodies: m_run holds the integer reference (warp-uniform)
     __device__ __forceinline__ void init() {
 #pragma unroll
         for (int hb = 0; hb < NHB; ++hb) {
@@ -469,6 +472,7 @@ struct WarpAcc {
 #pragma unroll
                 for (int e = 0; e < 4; ++e) O[hb][mm][e] = 0.0f;
             m_run[hb] = kNoMax;          // finite: ex2(-inf - kNoMax) = 0 without a guard
+            valid[hb] = false;
             l_run[hb] = 0.0f;
 #pragma unroll
             for (int gg = 0; gg < NG; ++gg) zacc[hb][gg] = 0.0f;
@@ -527,67 +531,118 @@ __device__ __forceinline__ void int2_page(const uint8_t* sb, int nvalid, int gid
         mma16816(S2[gg], A0, A1, A2, A3, qB2[kk][0], qB2[kk][1]);
     });
 
-    // ---- logits (hi + lo, log2 units) for tokens gid and gid+8 of head 4hb + tig
+    // ---- logits for tokens gid and gid+8 of head 4hb + tig (log2 units: the query carries the scale)
     const __half2* ksz = reinterpret_cast<const __half2*>(sb + GE::kCodeBytes);
     const __half2* vsz = reinterpret_cast<const __half2*>(sb + GE::kSeg + GE::kCodeBytes);
     uint32_t Pv[NHB][NG][2];     // p * s_v * 2^sigma per token slot, as (hi, lo) fp16 pair
 #pragma unroll
     for (int hb = 0; hb < NHB; ++hb) {
-        float lh[2], ll[2];
+        const bool hv = GQ % 4 == 0 || 4 * hb + tig < GQ;
+        const bool ok0 = v0 && hv, ok1 = v1 && hv;
+        float p0, p1;
+        if constexpr (NG == 1) {
+            // relative to the integer reference m: l - m = s X_hi + (z Q_hi - m) + z Q_lo + s X_lo, with
+            // z Q_hi exact (Q_hi has 13 significant bits, z 11), z Q_hi - m an exact two-sum, and s X_hi
+            // exact inside one fused multiply-add whose rounding is at the scale of l - m
+            float xh[2], xl[2], sk[2], zk[2];
 #pragma unroll
-        for (int slot = 0; slot < 2; ++slot) {
-            const int tok = gid + 8 * slot;
-            float dh = 0.0f, dl = 0.0f;
+            for (int slot = 0; slot < 2; ++slot) {
+                const float lo_raw = (GQ == 8) ? S2[0][2 * slot + hb] : S2[0][2 * slot];
+                xh[slot] = __fmul_rn(S1[0][hb][2 * slot], kap_h[hb]);
+                xl[slot] = __fmaf_rn(S1[0][hb][2 * slot + 1], kap_m[hb], __fmul_rn(lo_raw, kap_l[hb]));
+                const float2 sz = __half22float2(ksz[gid + 8 * slot]);
+                sk[slot] = sz.x;
+                zk[slot] = sz.y;
+            }
+            auto rel = [&](int slot, float m) {
+                float vh, vl;
+                two_sum(__fmul_rn(zk[slot], qs_hi[hb][0]), -m, vh, vl);
+                float t = __fmaf_rn(sk[slot], xh[slot], vh);
+                t = __fadd_rn(t, vl);
+                t = __fmaf_rn(zk[slot], qs_lo[hb][0], t);
+                return __fmaf_rn(sk[slot], xl[slot], t);
+            };
+            const float m0 = acc.valid[hb] ? m_run[hb] : 0.0f;
+            float t0 = ok0 ? rel(0, m0) : -INFINITY;
+            float t1 = ok1 ? rel(1, m0) : -INFINITY;
+            // lazy reference: set on the warp's first page, then raised (to an integer) only when a logit
+            // passes it by more than 2^kSoftmaxHeadroomLog2, so p <= 2^8 and the O rescale is rare; only
+            // then is the page maximum of each head reduced across its lanes and the page re-evaluated
+            if (__any_sync(0xffffffffu, !acc.valid[hb] || fmaxf(t0, t1) > (float)kSoftmaxHeadroomLog2)) {
+                float mp = fmaxf(t0, t1);
+                mp = fmaxf(mp, __shfl_xor_sync(0xffffffffu, mp, 4));
+                mp = fmaxf(mp, __shfl_xor_sync(0xffffffffu, mp, 8));
+                mp = fmaxf(mp, __shfl_xor_sync(0xffffffffu, mp, 16));
+                if (!acc.valid[hb]) {
+                    if (hv) m_run[hb] = ceilf(mp);                  // every page holds a valid token
+                } else if (mp > (float)kSoftmaxHeadroomLog2) {
+                    const float mn = ceilf(m_run[hb] + mp);
+                    const float k = mn - m_run[hb];                // an integer >= 9
+                    const float alpha = k > 126.0f ? 0.0f : __int_as_float((127 - (int)k) << 23);   // 2^-k exactly
+                    m_run[hb] = mn;
+                    l_run[hb] *= alpha;
 #pragma unroll
-            for (int gg = 0; gg < NG; ++gg) {
-                const float lo_raw = (GQ == 8) ? S2[gg][2 * slot + hb] : S2[gg][2 * slot];
-                const float s_hi = __fmul_rn(S1[gg][hb][2 * slot], kap_h[hb]);
-                const float s_r = __fmaf_rn(S1[gg][hb][2 * slot + 1], kap_m[hb], __fmul_rn(lo_raw, kap_l[hb]));
-                const float2 sz = __half22float2(ksz[tok * NG + gg]);
-                float p1, e1, p2, e2, t1, e3;
-                two_prod(sz.x, s_hi, p1, e1);
-                two_prod(sz.y, qs_hi[hb][gg], p2, e2);
-                two_sum(p1, p2, t1, e3);
-                const float low = __fadd_rn(__fadd_rn(e1, e2),
-                                            __fadd_rn(e3, __fmaf_rn(sz.x, s_r, __fmul_rn(sz.y, qs_lo[hb][gg]))));
-                if (NG == 1) {
-                    dh = t1;
-                    dl = low;
-                } else {
+                    for (int mm = 0; mm < NK; ++mm)
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) O[hb][mm][e] *= alpha;
+                    zacc[hb][0] *= alpha;
+                }
+                acc.valid[hb] = true;
+                t0 = ok0 ? rel(0, m_run[hb]) : -INFINITY;
+                t1 = ok1 ? rel(1, m_run[hb]) : -INFINITY;
+            }
+            p0 = ex2(t0);
+            p1 = ex2(t1);
+        } else {
+            float lh[2], ll[2];
+#pragma unroll
+            for (int slot = 0; slot < 2; ++slot) {
+                const int tok = gid + 8 * slot;
+                float dh = 0.0f, dl = 0.0f;
+#pragma unroll
+                for (int gg = 0; gg < NG; ++gg) {
+                    const float lo_raw = (GQ == 8) ? S2[gg][2 * slot + hb] : S2[gg][2 * slot];
+                    const float s_hi = __fmul_rn(S1[gg][hb][2 * slot], kap_h[hb]);
+                    const float s_r = __fmaf_rn(S1[gg][hb][2 * slot + 1], kap_m[hb], __fmul_rn(lo_raw, kap_l[hb]));
+                    const float2 sz = __half22float2(ksz[tok * NG + gg]);
+                    float p1, e1, p2, e2, t1, e3;
+                    two_prod(sz.x, s_hi, p1, e1);
+                    two_prod(sz.y, qs_hi[hb][gg], p2, e2);
+                    two_sum(p1, p2, t1, e3);
+                    const float low = __fadd_rn(__fadd_rn(e1, e2),
+                                                __fadd_rn(e3, __fmaf_rn(sz.x, s_r, __fmul_rn(sz.y, qs_lo[hb][gg]))));
                     float t2, e4;
                     two_sum(dh, t1, t2, e4);
                     dh = t2;
                     dl = __fadd_rn(dl, __fadd_rn(low, e4));
                 }
+                lh[slot] = dh;
+                ll[slot] = dl;
             }
-            lh[slot] = dh;          // already in log2 units (the query carries the scale)
-            ll[slot] = dl;
+            if (!ok0) { lh[0] = -INFINITY; ll[0] = 0.0f; }
+            if (!ok1) { lh[1] = -INFINITY; ll[1] = 0.0f; }
+            // several groups: the logit as hi + lo against a lazy running maximum. Online softmax over the page (lanes sharing tig hold the same head). The reference is lazy:
+            // raised only when a logit passes it by more than 2^kSoftmaxHeadroomLog2, so p <= 2^8 and the
+            // O rescale is rare; only then is the page maximum of each head reduced across its lanes
+            if (__any_sync(0xffffffffu, fmaxf(lh[0], lh[1]) > m_run[hb] + (float)kSoftmaxHeadroomLog2)) {
+                float mp = fmaxf(lh[0], lh[1]);
+                mp = fmaxf(mp, __shfl_xor_sync(0xffffffffu, mp, 4));
+                mp = fmaxf(mp, __shfl_xor_sync(0xffffffffu, mp, 8));
+                mp = fmaxf(mp, __shfl_xor_sync(0xffffffffu, mp, 16));
+                const float mn = fmaxf(m_run[hb], mp);
+                const float alpha = ex2(m_run[hb] - mn);
+                m_run[hb] = mn;
+                l_run[hb] *= alpha;
+#pragma unroll
+                for (int mm = 0; mm < NK; ++mm)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) O[hb][mm][e] *= alpha;
+#pragma unroll
+                for (int gg = 0; gg < NG; ++gg) zacc[hb][gg] *= alpha;
+            }
+            p0 = ex2(__fadd_rn(__fsub_rn(lh[0], m_run[hb]), ll[0]));
+            p1 = ex2(__fadd_rn(__fsub_rn(lh[1], m_run[hb]), ll[1]));
         }
-        const bool hv = GQ % 4 == 0 || 4 * hb + tig < GQ;
-        const bool ok0 = v0 && hv, ok1 = v1 && hv;
-        if (!ok0) { lh[0] = -INFINITY; ll[0] = 0.0f; }
-        if (!ok1) { lh[1] = -INFINITY; ll[1] = 0.0f; }
-        // online softmax over the page (lanes sharing tig hold the same head). The reference is lazy:
-        // raised only when a logit passes it by more than 2^kSoftmaxHeadroomLog2, so p <= 2^8 and the
-        // O rescale is rare; only then is the page maximum of each head reduced across its lanes
-        if (__any_sync(0xffffffffu, fmaxf(lh[0], lh[1]) > m_run[hb] + (float)kSoftmaxHeadroomLog2)) {
-            float mp = fmaxf(lh[0], lh[1]);
-            mp = fmaxf(mp, __shfl_xor_sync(0xffffffffu, mp, 4));
-            mp = fmaxf(mp, __shfl_xor_sync(0xffffffffu, mp, 8));
-            mp = fmaxf(mp, __shfl_xor_sync(0xffffffffu, mp, 16));
-            const float mn = fmaxf(m_run[hb], mp);
-            const float alpha = ex2(m_run[hb] - mn);
-            m_run[hb] = mn;
-            l_run[hb] *= alpha;
-#pragma unroll
-            for (int mm = 0; mm < NK; ++mm)
-#pragma unroll
-                for (int e = 0; e < 4; ++e) O[hb][mm][e] *= alpha;
-#pragma unroll
-            for (int gg = 0; gg < NG; ++gg) zacc[hb][gg] *= alpha;
-        }
-        const float p0 = ex2(__fadd_rn(__fsub_rn(lh[0], m_run[hb]), ll[0]));
-        const float p1 = ex2(__fadd_rn(__fsub_rn(lh[1], m_run[hb]), ll[1]));
         l_run[hb] = __fadd_rn(l_run[hb], __fadd_rn(p0, p1));
 #pragma unroll
         for (int gg = 0; gg < NG; ++gg) {
@@ -902,11 +957,108 @@ __device__ __forceinline__ void page_body(const uint8_t* sb, int nvalid, int gid
     else int2_page<D, G, GQ, FULL>(sb, nvalid, gid, tig, pvs, qo, acc);
 }
 
+// Streams this warp's pages (first + kWarps j, j < n_mine) of one (sequence, KV head, split) through
+// shared memory: kSlots slots of two pages, every lane copying its 16-byte chunks of a page with
+// cp.async, one commit group per slot, so waiting for all but the kSlots - 1 newest groups completes
+// the oldest slot. prologue() runs once the first copies are in flight; body(stage, nvalid, full) runs
+// for every page with a valid id, full = std::integral_constant<bool, nvalid == kPage>. Pairs of two
+// full, valid pages (all but the warp's last pair, normally) take one uniform test.
+template <int D, int G, typename Pro, typename Body>
+__device__ __forceinline__ void page_loop(const SplitArgs& a, int kv, int len, int first, int n_mine,
+                                          const int32_t* table, uint8_t* stage_base, Pro&& prologue, Body&& body) {
+    using GE = Geo<D, G>;
+    constexpr int kChunks = GE::kBlock / 16;                 // 16-byte chunks per page block
+    constexpr int kPerLane = (kChunks + 31) / 32;
+    constexpr uint32_t kSlotBytes = 2 * GE::kBlock;
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    uint8_t* my_stage = stage_base + (size_t)warp * kSlots * kSlotBytes;
+    const uint32_t stage_s = (uint32_t)__cvta_generic_to_shared(my_stage) + 16 * lane;
+    const uint8_t* const pool_kv = a.int2_pool + (size_t)kv * GE::kBlock + 16 * lane;
+    const uint32_t page_stride = (uint32_t)a.h_kv * GE::kBlock;
+    const bool tail_lane = kChunks % 32 == 0 || lane < kChunks % 32;   // copies the page's last chunk row
+    const int n_pairs = (n_mine + 1) / 2;
+    // pages j < j_full hold 16 tokens; only the sequence's last page can be shorter
+    const int j_full = (n_mine > 0 && first + kWarps * (n_mine - 1) == (len - 1) / kPage && len % kPage != 0)
+                           ? n_mine - 1 : n_mine;
+    // page ids, 32 at a time across the lanes: chunk c (pages 32c .. 32c+31 of the warp) lives in
+    // ids[c & 1], loaded two chunks ahead; when its first pair is issued the chunk is checked once
+    // (out-of-range ids become invalid pages, recorded in debug mode) and vm[c & 1] holds its ballot
+    int32_t ids0 = lane < n_mine ? table[first + kWarps * lane] : -1;
+    int32_t ids1 = lane + 32 < n_mine ? table[first + kWarps * (lane + 32)] : -1;
+    uint32_t vm0 = 0u, vm1 = 0u;
+    uint32_t valid_bits = 0u;                               // bits 2s, 2s+1: the pages of slot s are real
+    auto check_chunk = [&](int c, int32_t& ids, uint32_t& vm) {
+        const bool ok = ids >= 0 && (int64_t)ids < a.int2_pages;
+        if (a.debug && !ok && 32 * c + lane < n_mine) record_error(&a.dbg->kind, &a.dbg->index, 2, ids);
+        vm = __ballot_sync(0xffffffffu, ok);
+        ids = ok ? ids : 0;
+    };
+    auto copy_page = [&](uint32_t dst, int32_t phys) {
+        const uint8_t* src = pool_kv + (size_t)((uint32_t)phys * page_stride);
+#pragma unroll
+        for (int k = 0; k < kPerLane; ++k) cp_async16(dst + 512 * k, src + 512 * k, k + 1 < kPerLane || tail_lane);
+    };
+    // pages 2i and 2i+1 of the warp into slot s (both in one chunk of ids: 2i is even)
+    auto issue = [&](int i, int s) {
+        const int j0 = 2 * i;
+        const bool odd_chunk = (j0 >> 5) & 1;
+        if ((j0 & 31) == 0) {
+            if (odd_chunk) check_chunk(j0 >> 5, ids1, vm1); else check_chunk(j0 >> 5, ids0, vm0);
+        }
+        const int32_t cur = odd_chunk ? ids1 : ids0;
+        const uint32_t vb = ((odd_chunk ? vm1 : vm0) >> (j0 & 31)) & 3u;
+        const int32_t p0 = __shfl_sync(0xffffffffu, cur, j0 & 31);
+        const int32_t p1 = __shfl_sync(0xffffffffu, cur, (j0 & 31) + 1);
+        valid_bits = (valid_bits & ~(3u << (2 * s))) | (vb << (2 * s));
+        const uint32_t dst = stage_s + s * kSlotBytes;
+        if (vb & 1u) copy_page(dst, p0);
+        if (vb & 2u) copy_page(dst + GE::kBlock, p1);
+        cp_async_commit();
+    };
+    for (int i = 0; i < kSlots; ++i) {
+        if (i < n_pairs) issue(i, i);
+        else cp_async_commit();              // empty group: the wait count stays uniform
+    }
+    prologue();
+    int slot = 0;
+    for (int i = 0; i < n_pairs; ++i) {
+        cp_async_wait<kSlots - 1>();         // this lane's copies of pair i have landed
+        __syncwarp();                        // ... and every other lane's
+        const uint8_t* sb = my_stage + slot * kSlotBytes;
+        const uint32_t vb = (valid_bits >> (2 * slot)) & 3u;
+        if (vb == 3u && 2 * i + 1 < j_full) {
+#pragma unroll 1
+            for (int e = 0; e < 2; ++e) body(sb + e * GE::kBlock, kPage, std::true_type{});
+        } else {
+#pragma unroll 1
+            for (int e = 0; e < 2; ++e)
+                if (vb & (1u << e)) {
+                    // tokens of this page in the sequence (1..16)
+                    const int nv = min(kPage, len - (first + kWarps * (2 * i + e)) * kPage);
+                    body(sb + e * GE::kBlock, nv, std::false_type{});
+                }
+        }
+        __syncwarp();                        // every lane is done reading the slot before it is refilled
+        if (i + kSlots < n_pairs) {
+            const int ii = i + kSlots;
+            issue(ii, slot);
+            if (((2 * ii + 1) & 31) == 31) {      // chunk (2ii+1)/32 fully issued: load chunk + 2 into its slot
+                const int nj = 2 * ii + 1 + 33 + lane;
+                const int32_t v = nj < n_mine ? table[first + kWarps * nj] : -1;
+                if (((2 * ii + 1) >> 5) & 1) ids1 = v; else ids0 = v;
+            }
+        } else {
+            cp_async_commit();
+        }
+        if (++slot == kSlots) slot = 0;
+    }
+    cp_async_wait<0>();
+}
+
 // INT2 history split on tensor cores. Writes this warp's state into acc_s / ml_s.
 template <int D, int G, int GQ, int CB>
-__device__ void int2_split(const SplitArgs& a, int split, int kv, int b, uint8_t* stage_base, uint64_t* bars,
-                           float* acc_s, float (*ml_s)[GQ][2]) {
-    using GE = Geo<D, G>;
+__device__ void int2_split(const SplitArgs& a, int split, int kv, int b, uint8_t* stage_base, float* acc_s,
+                           float (*ml_s)[GQ][2]) {
     constexpr int NK = D / 16;          // k-steps (QK) = m-steps (PV)
     constexpr int NG = D / G;
     constexpr int KPG = G / 16;         // k-steps per group
@@ -928,140 +1080,71 @@ __device__ void int2_split(const SplitArgs& a, int split, int kv, int b, uint8_t
     const int first = pg0 + warp;
     const int n_mine = first < pg1 ? (pg1 - first + kWarps - 1) / kWarps : 0;
     const int32_t* table = a.int2_tables + (size_t)b * a.int2_stride;
-    // page ids of this warp, 32 at a time across the lanes: chunk c (pages 32c .. 32c+31 of the warp)
-    // lives in ids0 (c even) or ids1 (c odd) and is refilled with chunk c+2 once all its pages are issued
-    int32_t ids0 = lane < n_mine ? table[first + kWarps * lane] : -1;
-    int32_t ids1 = lane + 32 < n_mine ? table[first + kWarps * (lane + 32)] : -1;
 
-    WarpAcc<D, G, GQ> acc;
-    acc.init();
-    auto& O = acc.O;
-    auto& m_run = acc.m_run;
-    auto& l_run = acc.l_run;
-    auto& zacc = acc.zacc;
+    {
+        WarpAcc<D, G, GQ> acc;
+        acc.init();
+        auto& O = acc.O;
+        auto& m_run = acc.m_run;
+        auto& l_run = acc.l_run;
+        auto& zacc = acc.zacc;
+        QueryOps<D, G, GQ> qo;
+        float pvs = 1.0f, inv_pvs = 1.0f;
+        page_loop<D, G>(
+            a, kv, len, first, n_mine, table, stage_base,
+            [&] {
+                pdl_wait();
+                pdl_trigger();
+                load_query_ops<D, G, GQ>(a, head0, gid, tig, qo);
+                pvs = a.pv_scale[kv];
+                inv_pvs = 1.0f / pvs;
+            },
+            [&](const uint8_t* sb, int nv, auto full) {
+                page_body<D, G, GQ, CB, decltype(full)::value>(sb, nv, gid, tig, pvs, qo, acc);
+            });
 
-    // ---- page pipeline: kSlots slots of two pages per warp. Every lane copies its 16-byte chunks of a
-    // page with cp.async; one commit group per slot, so waiting for all but the kSlots - 1 newest groups
-    // completes the oldest slot.
-    uint8_t* my_stage = stage_base + (size_t)warp * kSlots * 2 * GE::kBlock;
-    const uint32_t stage_s = (uint32_t)__cvta_generic_to_shared(my_stage) + 16 * lane;
-    constexpr int kChunks = GE::kBlock / 16;                 // 16-byte chunks per page block
-    constexpr int kPerLane = (kChunks + 31) / 32;
-    const int n_pairs = (n_mine + 1) / 2;
-    uint32_t valid_bits = 0u;    // bit 2s + e: page e of slot s holds a real page
-    // launch arguments used every page, held in registers
-    const uint8_t* const pool_kv = a.int2_pool + (size_t)kv * GE::kBlock + 16 * lane;
-    const size_t page_stride = (size_t)a.h_kv * GE::kBlock;
-    const int64_t pool_pages = a.int2_pages;
-    const bool dbg_on = a.debug != 0;
-    auto copy_page = [&](uint32_t dst, int32_t phys, bool ok) {
-        const uint8_t* src = pool_kv + (size_t)(ok ? phys : 0) * page_stride;
+        // ---- this warp's state -> shared memory (scaled to the CTA max)
 #pragma unroll
-        for (int k = 0; k < kPerLane; ++k)
-            cp_async16(dst + 512 * k, src + 512 * k, ok && (kChunks % 32 == 0 || lane + 32 * k < kChunks));
-    };
-    // pages 2i and 2i+1 of the warp into slot s (both in one 32-page chunk of ids: 2i is even)
-    auto issue = [&](int i, int s) {
-        const int j0 = 2 * i;
-        const int32_t cur = ((j0 >> 5) & 1) ? ids1 : ids0;
-        const int32_t p0 = __shfl_sync(0xffffffffu, cur, j0 & 31);
-        const int32_t p1 = __shfl_sync(0xffffffffu, cur, (j0 & 31) + 1);
-        const bool ok0 = p0 >= 0 && p0 < pool_pages;
-        const bool ok1 = j0 + 1 < n_mine && p1 >= 0 && p1 < pool_pages;
-        if (dbg_on && lane == 0) {
-            if (!ok0) record_error(&a.dbg->kind, &a.dbg->index, 2, p0);
-            if (!ok1 && j0 + 1 < n_mine) record_error(&a.dbg->kind, &a.dbg->index, 2, p1);
-        }
-        valid_bits = (valid_bits & ~(3u << (2 * s))) | ((uint32_t)ok0 << (2 * s)) | ((uint32_t)ok1 << (2 * s + 1));
-        const uint32_t dst = stage_s + s * 2 * GE::kBlock;
-        copy_page(dst, p0, ok0);
-        copy_page(dst + GE::kBlock, p1, ok1);
-        cp_async_commit();
-    };
-    for (int i = 0; i < kSlots; ++i) {
-        if (i < n_pairs) issue(i, i);
-        else cp_async_commit();              // empty group: the wait count stays uniform
-    }
-
-    // the query operands come from q_prep: wait for it (the page copies above are already in flight)
-    pdl_wait();
-    pdl_trigger();
-    QueryOps<D, G, GQ> qo;
-    load_query_ops<D, G, GQ>(a, head0, gid, tig, qo);
-    const float pvs = a.pv_scale[kv];
-    const float inv_pvs = 1.0f / pvs;         // a power of two: exact
-
-    int slot = 0;
-    for (int i = 0; i < n_pairs; ++i) {
-        cp_async_wait<kSlots - 1>();         // this lane's copies of pair i have landed
-        __syncwarp();                        // ... and every other lane's
-        const uint8_t* sb = my_stage + slot * 2 * GE::kBlock;
+        for (int hb = 0; hb < NHB; ++hb) {
+            float l = l_run[hb];
+            l += __shfl_xor_sync(0xffffffffu, l, 4);
+            l += __shfl_xor_sync(0xffffffffu, l, 8);
+            l += __shfl_xor_sync(0xffffffffu, l, 16);
+            l_run[hb] = l;
 #pragma unroll
-        for (int e = 0; e < 2; ++e) {
-            if (valid_bits & (1u << (2 * slot + e))) {
-                // tokens of this page in the sequence: all 16 except on its last page
-                const int nv = len - (first + kWarps * (2 * i + e)) * kPage;
-                if (nv >= kPage) page_body<D, G, GQ, CB, true>(sb + e * GE::kBlock, kPage, gid, tig, pvs, qo, acc);
-                else page_body<D, G, GQ, CB, false>(sb + e * GE::kBlock, nv, gid, tig, pvs, qo, acc);
+            for (int gg = 0; gg < NG; ++gg) {
+                float z = zacc[hb][gg];
+                z += __shfl_xor_sync(0xffffffffu, z, 4);
+                z += __shfl_xor_sync(0xffffffffu, z, 8);
+                z += __shfl_xor_sync(0xffffffffu, z, 16);
+                zacc[hb][gg] = z;
             }
+            const int h = 4 * hb + tig;
+            if (h < GQ && gid == 0) { ml_s[warp][h][0] = m_run[hb]; ml_s[warp][h][1] = l_run[hb]; }
         }
-        __syncwarp();                        // every lane is done reading the slot before it is refilled
-        if (i + kSlots < n_pairs) {
-            const int ii = i + kSlots;
-            issue(ii, slot);
-            if (((2 * ii + 1) & 31) == 31) {      // chunk (2ii+1)/32 fully issued: load chunk + 2 into its slot
-                const int nj = 2 * ii + 1 + 33 + lane;
-                const int32_t v = nj < n_mine ? table[first + kWarps * nj] : -1;
-                if (((2 * ii + 1) >> 5) & 1) ids1 = v; else ids0 = v;
+        __syncthreads();
+#pragma unroll
+        for (int hb = 0; hb < NHB; ++hb) {
+            const int h = 4 * hb + tig;
+            if (h >= GQ) continue;
+            float mm_ = -INFINITY;
+#pragma unroll
+            for (int w2 = 0; w2 < kWarps; ++w2) mm_ = fmaxf(mm_, ml_s[w2][h][0]);
+            const float f = m_run[hb] <= kNoMax ? 0.0f : fast_exp2(m_run[hb] - mm_);
+            if (f == 0.0f) continue;
+#pragma unroll
+            for (int mm = 0; mm < NK; ++mm) {
+                const int gg = mm / KPG;
+                // rows gid and gid+8 of m-step mm carry 2^(2p') of their code position and 2^sigma
+                const int pos0 = mm;
+                const int pos1 = (D == 128) ? mm : 4 + mm;
+                const float sc0 = pos_weight(pos0) * inv_pvs;
+                const float sc1 = pos_weight(pos1) * inv_pvs;
+                const float o0 = __fmaf_rn(O[hb][mm][1], 0x1p-11f, O[hb][mm][0]) * sc0 + zacc[hb][gg];
+                const float o1 = __fmaf_rn(O[hb][mm][3], 0x1p-11f, O[hb][mm][2]) * sc1 + zacc[hb][gg];
+                atomicAdd(&acc_s[h * D + 16 * mm + gid], o0 * f);
+                atomicAdd(&acc_s[h * D + 16 * mm + gid + 8], o1 * f);
             }
-        } else {
-            cp_async_commit();
-        }
-        if (++slot == kSlots) slot = 0;
-    }
-    cp_async_wait<0>();
-
-    // ---- this warp's state -> shared memory (scaled to the CTA max)
-#pragma unroll
-    for (int hb = 0; hb < NHB; ++hb) {
-        float l = l_run[hb];
-        l += __shfl_xor_sync(0xffffffffu, l, 4);
-        l += __shfl_xor_sync(0xffffffffu, l, 8);
-        l += __shfl_xor_sync(0xffffffffu, l, 16);
-        l_run[hb] = l;
-#pragma unroll
-        for (int gg = 0; gg < NG; ++gg) {
-            float z = zacc[hb][gg];
-            z += __shfl_xor_sync(0xffffffffu, z, 4);
-            z += __shfl_xor_sync(0xffffffffu, z, 8);
-            z += __shfl_xor_sync(0xffffffffu, z, 16);
-            zacc[hb][gg] = z;
-        }
-        const int h = 4 * hb + tig;
-        if (h < GQ && gid == 0) { ml_s[warp][h][0] = m_run[hb]; ml_s[warp][h][1] = l_run[hb]; }
-    }
-    __syncthreads();
-#pragma unroll
-    for (int hb = 0; hb < NHB; ++hb) {
-        const int h = 4 * hb + tig;
-        if (h >= GQ) continue;
-        float mm_ = -INFINITY;
-#pragma unroll
-        for (int w2 = 0; w2 < kWarps; ++w2) mm_ = fmaxf(mm_, ml_s[w2][h][0]);
-        const float f = m_run[hb] <= kNoMax ? 0.0f : fast_exp2(m_run[hb] - mm_);
-        if (f == 0.0f) continue;
-#pragma unroll
-        for (int mm = 0; mm < NK; ++mm) {
-            const int gg = mm / KPG;
-            // rows gid and gid+8 of m-step mm carry 2^(2p') of their code position and 2^sigma
-            const int pos0 = mm;
-            const int pos1 = (D == 128) ? mm : 4 + mm;
-            const float sc0 = pos_weight(pos0) * inv_pvs;
-            const float sc1 = pos_weight(pos1) * inv_pvs;
-            const float o0 = __fmaf_rn(O[hb][mm][1], 0x1p-11f, O[hb][mm][0]) * sc0 + zacc[hb][gg];
-            const float o1 = __fmaf_rn(O[hb][mm][3], 0x1p-11f, O[hb][mm][2]) * sc1 + zacc[hb][gg];
-            atomicAdd(&acc_s[h * D + 16 * mm + gid], o0 * f);
-            atomicAdd(&acc_s[h * D + 16 * mm + gid + 8], o1 * f);
         }
     }
 }
@@ -1256,18 +1339,39 @@ __device__ void bf16_split(const SplitArgs& a, int split, int kv, int b, float* 
         const __nv_bfloat16* kp = a.bf16_pool + (((size_t)phys * a.h_kv + kv) * 2 + 0) * kPage * D;
         const __nv_bfloat16* vp = kp + kPage * D;
         const bool valid = pg * kPage + t < len;
+        const int tmax = min(kPage, len - pg * kPage);
+        // the page's V rows (CPL channels of every token per lane) are requested now, so they arrive
+        // while the logits and the softmax are computed
+        uint32_t vraw[kPage][CPL / 2];
+#pragma unroll
+        for (int tt = 0; tt < kPage; ++tt) {
+            if (tt < tmax) {
+                if constexpr (CPL == 4) {
+                    const uint2 u = *reinterpret_cast<const uint2*>(vp + tt * D + 4 * lane);
+                    vraw[tt][0] = u.x;
+                    vraw[tt][1] = u.y;
+                } else {
+                    vraw[tt][0] = *reinterpret_cast<const uint32_t*>(vp + tt * D + 2 * lane);
+                }
+            } else {
+#pragma unroll
+                for (int j = 0; j < CPL / 2; ++j) vraw[tt][j] = 0u;
+            }
+        }
         float lg[GQ];
 #pragma unroll
         for (int h = 0; h < GQ; ++h) lg[h] = 0.0f;
         const __nv_bfloat16* krow = kp + t * D + hf * (D / 2);
+        uint4 ku[D / 16];
 #pragma unroll
-        for (int c8 = 0; c8 < D / 2; c8 += 8) {
-            const uint4 u = *reinterpret_cast<const uint4*>(krow + c8);
-            const __nv_bfloat162* k2 = reinterpret_cast<const __nv_bfloat162*>(&u);
+        for (int c8 = 0; c8 < D / 16; ++c8) ku[c8] = *reinterpret_cast<const uint4*>(krow + 8 * c8);
+#pragma unroll
+        for (int c8 = 0; c8 < D / 16; ++c8) {
+            const __nv_bfloat162* k2 = reinterpret_cast<const __nv_bfloat162*>(&ku[c8]);
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
                 const float2 kf = __bfloat1622float2(k2[e]);
-                const int c = hf * (D / 2) + c8 + 2 * e;
+                const int c = hf * (D / 2) + 8 * c8 + 2 * e;
 #pragma unroll
                 for (int h = 0; h < GQ; ++h)
                     lg[h] = fmaf(qs[h * D + c], kf.x, fmaf(qs[h * D + c + 1], kf.y, lg[h]));
@@ -1294,17 +1398,15 @@ __device__ void bf16_split(const SplitArgs& a, int split, int kv, int b, float* 
         for (int h = 0; h < GQ; ++h)
 #pragma unroll
             for (int j = 0; j < CPL; ++j) acc[h][j] *= alpha[h];
-        const int tmax = min(kPage, len - pg * kPage);
-        for (int tt = 0; tt < tmax; ++tt) {
+#pragma unroll
+        for (int tt = 0; tt < kPage; ++tt) {
+            if (tt >= tmax) break;
             float v[CPL];
-            if constexpr (CPL == 4) {
-                const uint2 u = *reinterpret_cast<const uint2*>(vp + tt * D + 4 * lane);
-                const float2 a0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.x));
-                const float2 a1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.y));
-                v[0] = a0.x; v[1] = a0.y; v[2] = a1.x; v[3] = a1.y;
-            } else {
-                const float2 a0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(vp + tt * D + 2 * lane));
-                v[0] = a0.x; v[1] = a0.y;
+#pragma unroll
+            for (int j = 0; j < CPL / 2; ++j) {
+                const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&vraw[tt][j]));
+                v[2 * j] = f.x;
+                v[2 * j + 1] = f.y;
             }
 #pragma unroll
             for (int h = 0; h < GQ; ++h)
@@ -1442,7 +1544,7 @@ split_kernel(SplitArgs a) {
     __syncthreads();
 
     if (split < a.int2_splits) {
-        int2_split<D, G, GQ, CB>(a, split, kv, b, dyn_smem, bars, acc_s, ml_s);
+        int2_split<D, G, GQ, CB>(a, split, kv, b, dyn_smem, acc_s, ml_s);
     } else {
         pdl_wait();
         pdl_trigger();
@@ -1650,10 +1752,11 @@ DecodePlan plan_decode(const Shape& s, int num_sms, int batch, int max_hist, int
     // (few units: bs1 decode); otherwise at most kMaxPagesPerSplit pages per split, in as many
     // waves as that takes (many units or long sequences)
     const int slots = split_ctas_per_sm(s) * num_sms;
-    // BF16 splits: two when the grid is one wave of few units (bs1), so that the BF16 segment's CTA
-    // (about 1.7x an INT2 split's bytes at 100k) is not the last to finish
+    // BF16 splits: when the grid is one wave of few units (bs1), one page per warp, so that the BF16
+    // segment's CTAs (CUDA-core attention, about 1.7x an INT2 split's bytes at 100k) finish with the
+    // INT2 splits; otherwise one split
     const int bf16_pages = (s.sink + s.recent + kPage - 1) / kPage;
-    p.bf16_splits = (units > 0 && slots / units >= 16 && bf16_pages >= 2) ? 2 : 1;
+    p.bf16_splits = (units > 0 && slots / units >= 16 && bf16_pages >= 2) ? (bf16_pages + kWarps - 1) / kWarps : 1;
     p.bf16_pages_per_split = (bf16_pages + p.bf16_splits - 1) / p.bf16_splits;
     int splits = units > 0 ? slots / units - p.bf16_splits : 1;
     if (splits < 1) splits = 1;
