@@ -480,11 +480,14 @@ struct WarpAcc {
     }
 };
 
-// One INT2 page (16 tokens, the first `nvalid` valid) of one KV head, staged in shared memory at sb,
-// folded into the warp's softmax state.
-template <int D, int G, int GQ, bool FULL>
-__device__ __forceinline__ void int2_page(const uint8_t* sb, int nvalid, int gid, int tig, float pvs,
-                                          const QueryOps<D, G, GQ>& qo, WarpAcc<D, G, GQ>& acc) {
+// NP INT2 pages (16 tokens each; with FULL all valid, otherwise the first `nvalid` of the single page) of
+// one KV head, staged in shared memory at sb[0..NP), folded into the warp's softmax state. With NP = 2
+// the two pages' Q.K products, logits, weights and P.V products are independent chains that the
+// scheduler interleaves; they share one test of the lazy reference.
+template <int D, int G, int GQ, int NP, bool FULL>
+__device__ __forceinline__ void int2_pages(const uint8_t* const (&sb)[NP], int nvalid, int gid, int tig, float pvs,
+                                           const QueryOps<D, G, GQ>& qo, WarpAcc<D, G, GQ>& acc) {
+    static_assert(NP == 1 || FULL, "several pages at once are full pages");
     using GE = Geo<D, G>;
     constexpr int NK = D / 16, NG = D / G, KPG = G / 16, NHB = (GQ + 3) / 4;
     const auto& qB1 = qo.qB1;
@@ -501,75 +504,95 @@ __device__ __forceinline__ void int2_page(const uint8_t* sb, int nvalid, int gid
     const bool v0 = FULL || gid < nvalid, v1 = FULL || gid + 8 < nvalid;
 
     // ---- QK^T on tensor cores: A = K codes [16 tokens x 16 channels], B = query parts
-    uint32_t kw0[2], kw1[2];
-    if constexpr (D == 128) {
-        const uint2 u0 = *reinterpret_cast<const uint2*>(sb + gid * GE::kCodeRow + 8 * tig);
-        const uint2 u1 = *reinterpret_cast<const uint2*>(sb + (gid + 8) * GE::kCodeRow + 8 * tig);
-        kw0[0] = u0.x; kw0[1] = u0.y; kw1[0] = u1.x; kw1[1] = u1.y;
-    } else {
-        kw0[0] = *reinterpret_cast<const uint32_t*>(sb + gid * GE::kCodeRow + 4 * tig);
-        kw1[0] = *reinterpret_cast<const uint32_t*>(sb + (gid + 8) * GE::kCodeRow + 4 * tig);
-        kw0[1] = kw1[1] = 0u;
+    uint32_t kw0[NP][2], kw1[NP][2];
+#pragma unroll
+    for (int pi = 0; pi < NP; ++pi) {
+        if constexpr (D == 128) {
+            const uint2 u0 = *reinterpret_cast<const uint2*>(sb[pi] + gid * GE::kCodeRow + 8 * tig);
+            const uint2 u1 = *reinterpret_cast<const uint2*>(sb[pi] + (gid + 8) * GE::kCodeRow + 8 * tig);
+            kw0[pi][0] = u0.x; kw0[pi][1] = u0.y; kw1[pi][0] = u1.x; kw1[pi][1] = u1.y;
+        } else {
+            kw0[pi][0] = *reinterpret_cast<const uint32_t*>(sb[pi] + gid * GE::kCodeRow + 4 * tig);
+            kw1[pi][0] = *reinterpret_cast<const uint32_t*>(sb[pi] + (gid + 8) * GE::kCodeRow + 4 * tig);
+            kw0[pi][1] = kw1[pi][1] = 0u;
+        }
     }
-    float S1[NG][NHB][4], S2[NG][4];
+    float S1[NP][NG][NHB][4], S2[NP][NG][4];
 #pragma unroll
-    for (int gg = 0; gg < NG; ++gg) {
+    for (int pi = 0; pi < NP; ++pi)
 #pragma unroll
-        for (int e = 0; e < 4; ++e) S2[gg][e] = 0.0f;
+        for (int gg = 0; gg < NG; ++gg) {
 #pragma unroll
-        for (int hb = 0; hb < NHB; ++hb)
+            for (int e = 0; e < 4; ++e) S2[pi][gg][e] = 0.0f;
 #pragma unroll
-            for (int e = 0; e < 4; ++e) S1[gg][hb][e] = 0.0f;
-    }
+            for (int hb = 0; hb < NHB; ++hb)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) S1[pi][gg][hb][e] = 0.0f;
+        }
     static_for<NK>([&](auto kkc) {
         constexpr int kk = decltype(kkc)::value;
-        uint32_t A0, A1, A2, A3;
-        k_operand<D, kk>(kw0, kw1, A0, A1, A2, A3);
         constexpr int gg = kk / KPG;
 #pragma unroll
-        for (int hb = 0; hb < NHB; ++hb) mma16816(S1[gg][hb], A0, A1, A2, A3, qB1[kk][hb][0], qB1[kk][hb][1]);
-        mma16816(S2[gg], A0, A1, A2, A3, qB2[kk][0], qB2[kk][1]);
+        for (int pi = 0; pi < NP; ++pi) {
+            uint32_t A0, A1, A2, A3;
+            k_operand<D, kk>(kw0[pi], kw1[pi], A0, A1, A2, A3);
+#pragma unroll
+            for (int hb = 0; hb < NHB; ++hb)
+                mma16816(S1[pi][gg][hb], A0, A1, A2, A3, qB1[kk][hb][0], qB1[kk][hb][1]);
+            mma16816(S2[pi][gg], A0, A1, A2, A3, qB2[kk][0], qB2[kk][1]);
+        }
     });
 
-    // ---- logits for tokens gid and gid+8 of head 4hb + tig (log2 units: the query carries the scale)
-    const __half2* ksz = reinterpret_cast<const __half2*>(sb + GE::kCodeBytes);
-    const __half2* vsz = reinterpret_cast<const __half2*>(sb + GE::kSeg + GE::kCodeBytes);
-    uint32_t Pv[NHB][NG][2];     // p * s_v * 2^sigma per token slot, as (hi, lo) fp16 pair
+    // ---- logits for tokens gid and gid+8 of head 4hb + tig (log2 units: the query carries the scale),
+    // weights p, and P' = p * s_v * 2^sigma per token slot as an (hi, lo) fp16 pair
+    uint32_t Pv[NP][NHB][NG][2];
 #pragma unroll
     for (int hb = 0; hb < NHB; ++hb) {
         const bool hv = GQ % 4 == 0 || 4 * hb + tig < GQ;
         const bool ok0 = v0 && hv, ok1 = v1 && hv;
-        float p0, p1;
+        float p[NP][2];
         if constexpr (NG == 1) {
             // relative to the integer reference m: l - m = s X_hi + (z Q_hi - m) + z Q_lo + s X_lo, with
             // z Q_hi exact (Q_hi has 13 significant bits, z 11), z Q_hi - m an exact two-sum, and s X_hi
             // exact inside one fused multiply-add whose rounding is at the scale of l - m
-            float xh[2], xl[2], sk[2], zk[2];
+            float xh[NP][2], xl[NP][2], sk[NP][2], zk[NP][2], t[NP][2];
 #pragma unroll
-            for (int slot = 0; slot < 2; ++slot) {
-                const float lo_raw = (GQ == 8) ? S2[0][2 * slot + hb] : S2[0][2 * slot];
-                xh[slot] = __fmul_rn(S1[0][hb][2 * slot], kap_h[hb]);
-                xl[slot] = __fmaf_rn(S1[0][hb][2 * slot + 1], kap_m[hb], __fmul_rn(lo_raw, kap_l[hb]));
-                const float2 sz = __half22float2(ksz[gid + 8 * slot]);
-                sk[slot] = sz.x;
-                zk[slot] = sz.y;
+            for (int pi = 0; pi < NP; ++pi) {
+                const __half2* ksz = reinterpret_cast<const __half2*>(sb[pi] + GE::kCodeBytes);
+#pragma unroll
+                for (int slot = 0; slot < 2; ++slot) {
+                    const float lo_raw = (GQ == 8) ? S2[pi][0][2 * slot + hb] : S2[pi][0][2 * slot];
+                    xh[pi][slot] = __fmul_rn(S1[pi][0][hb][2 * slot], kap_h[hb]);
+                    xl[pi][slot] = __fmaf_rn(S1[pi][0][hb][2 * slot + 1], kap_m[hb], __fmul_rn(lo_raw, kap_l[hb]));
+                    const float2 sz = __half22float2(ksz[gid + 8 * slot]);
+                    sk[pi][slot] = sz.x;
+                    zk[pi][slot] = sz.y;
+                }
             }
-            auto rel = [&](int slot, float m) {
+            auto rel = [&](int pi, int slot, float m) {
                 float vh, vl;
-                two_sum(__fmul_rn(zk[slot], qs_hi[hb][0]), -m, vh, vl);
-                float t = __fmaf_rn(sk[slot], xh[slot], vh);
-                t = __fadd_rn(t, vl);
-                t = __fmaf_rn(zk[slot], qs_lo[hb][0], t);
-                return __fmaf_rn(sk[slot], xl[slot], t);
+                two_sum(__fmul_rn(zk[pi][slot], qs_hi[hb][0]), -m, vh, vl);
+                float r = __fmaf_rn(sk[pi][slot], xh[pi][slot], vh);
+                r = __fadd_rn(r, vl);
+                r = __fmaf_rn(zk[pi][slot], qs_lo[hb][0], r);
+                return __fmaf_rn(sk[pi][slot], xl[pi][slot], r);
             };
-            const float m0 = acc.valid[hb] ? m_run[hb] : 0.0f;
-            float t0 = ok0 ? rel(0, m0) : -INFINITY;
-            float t1 = ok1 ? rel(1, m0) : -INFINITY;
+            auto all_logits = [&](float m) {
+                float mx = -INFINITY;
+#pragma unroll
+                for (int pi = 0; pi < NP; ++pi) {
+                    t[pi][0] = ok0 ? rel(pi, 0, m) : -INFINITY;
+                    t[pi][1] = ok1 ? rel(pi, 1, m) : -INFINITY;
+                    mx = fmaxf(mx, fmaxf(t[pi][0], t[pi][1]));
+                }
+                return mx;
+            };
+            const float mx = all_logits(acc.valid[hb] ? m_run[hb] : 0.0f);
             // lazy reference: set on the warp's first page, then raised (to an integer) only when a logit
             // passes it by more than 2^kSoftmaxHeadroomLog2, so p <= 2^8 and the O rescale is rare; only
-            // then is the page maximum of each head reduced across its lanes and the page re-evaluated
-            if (__any_sync(0xffffffffu, !acc.valid[hb] || fmaxf(t0, t1) > (float)kSoftmaxHeadroomLog2)) {
-                float mp = fmaxf(t0, t1);
+            // then is the maximum of each head reduced across its lanes and the pages re-evaluated
+            if (__any_sync(0xffffffffu, !acc.valid[hb] || mx > (float)kSoftmaxHeadroomLog2)) {
+                float mp = mx;
                 mp = fmaxf(mp, __shfl_xor_sync(0xffffffffu, mp, 4));
                 mp = fmaxf(mp, __shfl_xor_sync(0xffffffffu, mp, 8));
                 mp = fmaxf(mp, __shfl_xor_sync(0xffffffffu, mp, 16));
@@ -577,7 +600,7 @@ __device__ __forceinline__ void int2_page(const uint8_t* sb, int nvalid, int gid
                     if (hv) m_run[hb] = ceilf(mp);                  // every page holds a valid token
                 } else if (mp > (float)kSoftmaxHeadroomLog2) {
                     const float mn = ceilf(m_run[hb] + mp);
-                    const float k = mn - m_run[hb];                // an integer >= 9
+                    const float k = mn - m_run[hb];                 // an integer >= 9
                     const float alpha = k > 126.0f ? 0.0f : __int_as_float((127 - (int)k) << 23);   // 2^-k exactly
                     m_run[hb] = mn;
                     l_run[hb] *= alpha;
@@ -588,44 +611,53 @@ __device__ __forceinline__ void int2_page(const uint8_t* sb, int nvalid, int gid
                     zacc[hb][0] *= alpha;
                 }
                 acc.valid[hb] = true;
-                t0 = ok0 ? rel(0, m_run[hb]) : -INFINITY;
-                t1 = ok1 ? rel(1, m_run[hb]) : -INFINITY;
+                (void)all_logits(m_run[hb]);
             }
-            p0 = ex2(t0);
-            p1 = ex2(t1);
+#pragma unroll
+            for (int pi = 0; pi < NP; ++pi) {
+                p[pi][0] = ex2(t[pi][0]);
+                p[pi][1] = ex2(t[pi][1]);
+            }
         } else {
-            float lh[2], ll[2];
+            // several groups: the logit as hi + lo against a lazy running maximum
+            float lh[NP][2], ll[NP][2];
+            float mx = -INFINITY;
 #pragma unroll
-            for (int slot = 0; slot < 2; ++slot) {
-                const int tok = gid + 8 * slot;
-                float dh = 0.0f, dl = 0.0f;
+            for (int pi = 0; pi < NP; ++pi) {
+                const __half2* ksz = reinterpret_cast<const __half2*>(sb[pi] + GE::kCodeBytes);
 #pragma unroll
-                for (int gg = 0; gg < NG; ++gg) {
-                    const float lo_raw = (GQ == 8) ? S2[gg][2 * slot + hb] : S2[gg][2 * slot];
-                    const float s_hi = __fmul_rn(S1[gg][hb][2 * slot], kap_h[hb]);
-                    const float s_r = __fmaf_rn(S1[gg][hb][2 * slot + 1], kap_m[hb], __fmul_rn(lo_raw, kap_l[hb]));
-                    const float2 sz = __half22float2(ksz[tok * NG + gg]);
-                    float p1, e1, p2, e2, t1, e3;
-                    two_prod(sz.x, s_hi, p1, e1);
-                    two_prod(sz.y, qs_hi[hb][gg], p2, e2);
-                    two_sum(p1, p2, t1, e3);
-                    const float low = __fadd_rn(__fadd_rn(e1, e2),
-                                                __fadd_rn(e3, __fmaf_rn(sz.x, s_r, __fmul_rn(sz.y, qs_lo[hb][gg]))));
-                    float t2, e4;
-                    two_sum(dh, t1, t2, e4);
-                    dh = t2;
-                    dl = __fadd_rn(dl, __fadd_rn(low, e4));
+                for (int slot = 0; slot < 2; ++slot) {
+                    const int tok = gid + 8 * slot;
+                    float dh = 0.0f, dl = 0.0f;
+#pragma unroll
+                    for (int gg = 0; gg < NG; ++gg) {
+                        const float lo_raw = (GQ == 8) ? S2[pi][gg][2 * slot + hb] : S2[pi][gg][2 * slot];
+                        const float s_hi = __fmul_rn(S1[pi][gg][hb][2 * slot], kap_h[hb]);
+                        const float s_r = __fmaf_rn(S1[pi][gg][hb][2 * slot + 1], kap_m[hb],
+                                                    __fmul_rn(lo_raw, kap_l[hb]));
+                        const float2 sz = __half22float2(ksz[tok * NG + gg]);
+                        float p1, e1, p2, e2, t1, e3;
+                        two_prod(sz.x, s_hi, p1, e1);
+                        two_prod(sz.y, qs_hi[hb][gg], p2, e2);
+                        two_sum(p1, p2, t1, e3);
+                        const float low = __fadd_rn(__fadd_rn(e1, e2),
+                                                    __fadd_rn(e3, __fmaf_rn(sz.x, s_r, __fmul_rn(sz.y, qs_lo[hb][gg]))));
+                        float t2, e4;
+                        two_sum(dh, t1, t2, e4);
+                        dh = t2;
+                        dl = __fadd_rn(dl, __fadd_rn(low, e4));
+                    }
+                    lh[pi][slot] = dh;
+                    ll[pi][slot] = dl;
                 }
-                lh[slot] = dh;
-                ll[slot] = dl;
+                if (!ok0) { lh[pi][0] = -INFINITY; ll[pi][0] = 0.0f; }
+                if (!ok1) { lh[pi][1] = -INFINITY; ll[pi][1] = 0.0f; }
+                mx = fmaxf(mx, fmaxf(lh[pi][0], lh[pi][1]));
             }
-            if (!ok0) { lh[0] = -INFINITY; ll[0] = 0.0f; }
-            if (!ok1) { lh[1] = -INFINITY; ll[1] = 0.0f; }
-            // several groups: the logit as hi + lo against a lazy running maximum. Online softmax over the page (lanes sharing tig hold the same head). The reference is lazy:
-            // raised only when a logit passes it by more than 2^kSoftmaxHeadroomLog2, so p <= 2^8 and the
-            // O rescale is rare; only then is the page maximum of each head reduced across its lanes
-            if (__any_sync(0xffffffffu, fmaxf(lh[0], lh[1]) > m_run[hb] + (float)kSoftmaxHeadroomLog2)) {
-                float mp = fmaxf(lh[0], lh[1]);
+            // online softmax (lanes sharing tig hold the same head); the reference is raised only when a
+            // logit passes it by more than 2^kSoftmaxHeadroomLog2, so p <= 2^8 and the O rescale is rare
+            if (__any_sync(0xffffffffu, mx > m_run[hb] + (float)kSoftmaxHeadroomLog2)) {
+                float mp = mx;
                 mp = fmaxf(mp, __shfl_xor_sync(0xffffffffu, mp, 4));
                 mp = fmaxf(mp, __shfl_xor_sync(0xffffffffu, mp, 8));
                 mp = fmaxf(mp, __shfl_xor_sync(0xffffffffu, mp, 16));
@@ -640,72 +672,90 @@ __device__ __forceinline__ void int2_page(const uint8_t* sb, int nvalid, int gid
 #pragma unroll
                 for (int gg = 0; gg < NG; ++gg) zacc[hb][gg] *= alpha;
             }
-            p0 = ex2(__fadd_rn(__fsub_rn(lh[0], m_run[hb]), ll[0]));
-            p1 = ex2(__fadd_rn(__fsub_rn(lh[1], m_run[hb]), ll[1]));
-        }
-        l_run[hb] = __fadd_rn(l_run[hb], __fadd_rn(p0, p1));
 #pragma unroll
-        for (int gg = 0; gg < NG; ++gg) {
-            const float2 s0 = __half22float2(vsz[gid * NG + gg]);
-            const float2 s1 = __half22float2(vsz[(gid + 8) * NG + gg]);
-            // p <= 2^8 and s_v <= (2/3) max T_v, and 2^sigma leaves that headroom, so
-            // x <= 32752 (1 + tiny): fp16 without a clamp
-            const float x0 = ok0 ? __fmul_rn(__fmul_rn(p0, s0.x), pvs) : 0.0f;
-            const float x1 = ok1 ? __fmul_rn(__fmul_rn(p1, s1.x), pvs) : 0.0f;
-            const __half h0 = __float2half_rn(x0), h1 = __float2half_rn(x1);
-            Pv[hb][gg][0] = pack_half2(h0, __float2half_rn(__fmul_rn(__fsub_rn(x0, __half2float(h0)), 2048.0f)));
-            Pv[hb][gg][1] = pack_half2(h1, __float2half_rn(__fmul_rn(__fsub_rn(x1, __half2float(h1)), 2048.0f)));
-            if (ok0) zacc[hb][gg] = __fmaf_rn(p0, s0.y, zacc[hb][gg]);
-            if (ok1) zacc[hb][gg] = __fmaf_rn(p1, s1.y, zacc[hb][gg]);
+            for (int pi = 0; pi < NP; ++pi) {
+                p[pi][0] = ex2(__fadd_rn(__fsub_rn(lh[pi][0], m_run[hb]), ll[pi][0]));
+                p[pi][1] = ex2(__fadd_rn(__fsub_rn(lh[pi][1], m_run[hb]), ll[pi][1]));
+            }
+        }
+#pragma unroll
+        for (int pi = 0; pi < NP; ++pi) {
+            l_run[hb] = __fadd_rn(l_run[hb], __fadd_rn(p[pi][0], p[pi][1]));
+            const __half2* vsz = reinterpret_cast<const __half2*>(sb[pi] + GE::kSeg + GE::kCodeBytes);
+#pragma unroll
+            for (int gg = 0; gg < NG; ++gg) {
+                const float2 s0 = __half22float2(vsz[gid * NG + gg]);
+                const float2 s1 = __half22float2(vsz[(gid + 8) * NG + gg]);
+                // p <= 2^8 and s_v <= (2/3) max T_v, and 2^sigma leaves that headroom, so
+                // x <= 32752 (1 + tiny): fp16 without a clamp
+                const float x0 = ok0 ? __fmul_rn(__fmul_rn(p[pi][0], s0.x), pvs) : 0.0f;
+                const float x1 = ok1 ? __fmul_rn(__fmul_rn(p[pi][1], s1.x), pvs) : 0.0f;
+                const __half h0 = __float2half_rn(x0), h1 = __float2half_rn(x1);
+                Pv[pi][hb][gg][0] = pack_half2(h0, __float2half_rn(__fmul_rn(__fsub_rn(x0, __half2float(h0)), 2048.0f)));
+                Pv[pi][hb][gg][1] = pack_half2(h1, __float2half_rn(__fmul_rn(__fsub_rn(x1, __half2float(h1)), 2048.0f)));
+                if (ok0) zacc[hb][gg] = __fmaf_rn(p[pi][0], s0.y, zacc[hb][gg]);
+                if (ok1) zacc[hb][gg] = __fmaf_rn(p[pi][1], s1.y, zacc[hb][gg]);
+            }
         }
     }
 
     // ---- PV on tensor cores: A = V codes^T [16 channels x 16 tokens], B = p * s_v (hi, lo)
-    uint32_t X01, Y01, X23, Y23;
-    const uint8_t* vc = sb + GE::kSeg;
-    if constexpr (D == 128) {
-        const uint32_t wa = *reinterpret_cast<const uint32_t*>(vc + (2 * tig) * GE::kCodeRow + 4 * gid);
-        const uint32_t wb = *reinterpret_cast<const uint32_t*>(vc + (2 * tig + 1) * GE::kCodeRow + 4 * gid);
-        const uint32_t wc = *reinterpret_cast<const uint32_t*>(vc + (2 * tig + 8) * GE::kCodeRow + 4 * gid);
-        const uint32_t wd = *reinterpret_cast<const uint32_t*>(vc + (2 * tig + 9) * GE::kCodeRow + 4 * gid);
-        X01 = __byte_perm(wa, wb, 0x5410);
-        Y01 = __byte_perm(wa, wb, 0x7632);
-        X23 = __byte_perm(wc, wd, 0x5410);
-        Y23 = __byte_perm(wc, wd, 0x7632);
-    } else {
-        const uint32_t wa = *reinterpret_cast<const uint16_t*>(vc + (2 * tig) * GE::kCodeRow + 2 * gid);
-        const uint32_t wb = *reinterpret_cast<const uint16_t*>(vc + (2 * tig + 1) * GE::kCodeRow + 2 * gid);
-        const uint32_t wc = *reinterpret_cast<const uint16_t*>(vc + (2 * tig + 8) * GE::kCodeRow + 2 * gid);
-        const uint32_t wd = *reinterpret_cast<const uint16_t*>(vc + (2 * tig + 9) * GE::kCodeRow + 2 * gid);
-        X01 = __byte_perm(wa, wb, 0x5410);
-        X23 = __byte_perm(wc, wd, 0x5410);
-        Y01 = X01;
-        Y23 = X23;
-    }
-    const uint32_t X01s = X01 >> 10, Y01s = Y01 >> 10, X23s = X23 >> 10, Y23s = Y23 >> 10;
     // the (hi, lo) part this lane's B column needs: hi for even gid, lo for odd gid
     const uint32_t sel = (gid & 1) ? 0x7632u : 0x5410u;
     const int srcA = 8 * tig + (gid >> 1), srcB = srcA + 4;
-    uint32_t Bf[NHB][NG][2];
 #pragma unroll
-    for (int hb = 0; hb < NHB; ++hb)
-#pragma unroll
-        for (int gg = 0; gg < NG; ++gg) {
-            const uint32_t a0 = __shfl_sync(0xffffffffu, Pv[hb][gg][0], srcA);
-            const uint32_t a1 = __shfl_sync(0xffffffffu, Pv[hb][gg][1], srcA);
-            const uint32_t b0 = __shfl_sync(0xffffffffu, Pv[hb][gg][0], srcB);
-            const uint32_t b1 = __shfl_sync(0xffffffffu, Pv[hb][gg][1], srcB);
-            Bf[hb][gg][0] = __byte_perm(a0, b0, sel);
-            Bf[hb][gg][1] = __byte_perm(a1, b1, sel);
+    for (int pi = 0; pi < NP; ++pi) {
+        uint32_t X01, Y01, X23, Y23;
+        const uint8_t* vc = sb[pi] + GE::kSeg;
+        if constexpr (D == 128) {
+            const uint32_t wa = *reinterpret_cast<const uint32_t*>(vc + (2 * tig) * GE::kCodeRow + 4 * gid);
+            const uint32_t wb = *reinterpret_cast<const uint32_t*>(vc + (2 * tig + 1) * GE::kCodeRow + 4 * gid);
+            const uint32_t wc = *reinterpret_cast<const uint32_t*>(vc + (2 * tig + 8) * GE::kCodeRow + 4 * gid);
+            const uint32_t wd = *reinterpret_cast<const uint32_t*>(vc + (2 * tig + 9) * GE::kCodeRow + 4 * gid);
+            X01 = __byte_perm(wa, wb, 0x5410);
+            Y01 = __byte_perm(wa, wb, 0x7632);
+            X23 = __byte_perm(wc, wd, 0x5410);
+            Y23 = __byte_perm(wc, wd, 0x7632);
+        } else {
+            const uint32_t wa = *reinterpret_cast<const uint16_t*>(vc + (2 * tig) * GE::kCodeRow + 2 * gid);
+            const uint32_t wb = *reinterpret_cast<const uint16_t*>(vc + (2 * tig + 1) * GE::kCodeRow + 2 * gid);
+            const uint32_t wc = *reinterpret_cast<const uint16_t*>(vc + (2 * tig + 8) * GE::kCodeRow + 2 * gid);
+            const uint32_t wd = *reinterpret_cast<const uint16_t*>(vc + (2 * tig + 9) * GE::kCodeRow + 2 * gid);
+            X01 = __byte_perm(wa, wb, 0x5410);
+            X23 = __byte_perm(wc, wd, 0x5410);
+            Y01 = X01;
+            Y23 = X23;
         }
-    static_for<NK>([&](auto mc) {
-        constexpr int mm = decltype(mc)::value;
-        constexpr int gg = mm / KPG;
-        uint32_t A0, A1, A2, A3;
-        v_operand<D, mm>(X01, X01s, Y01, Y01s, X23, X23s, Y23, Y23s, A0, A1, A2, A3);
+        const uint32_t X01s = X01 >> 10, Y01s = Y01 >> 10, X23s = X23 >> 10, Y23s = Y23 >> 10;
+        uint32_t Bf[NHB][NG][2];
 #pragma unroll
-        for (int hb = 0; hb < NHB; ++hb) mma16816(O[hb][mm], A0, A1, A2, A3, Bf[hb][gg][0], Bf[hb][gg][1]);
-    });
+        for (int hb = 0; hb < NHB; ++hb)
+#pragma unroll
+            for (int gg = 0; gg < NG; ++gg) {
+                const uint32_t a0 = __shfl_sync(0xffffffffu, Pv[pi][hb][gg][0], srcA);
+                const uint32_t a1 = __shfl_sync(0xffffffffu, Pv[pi][hb][gg][1], srcA);
+                const uint32_t b0 = __shfl_sync(0xffffffffu, Pv[pi][hb][gg][0], srcB);
+                const uint32_t b1 = __shfl_sync(0xffffffffu, Pv[pi][hb][gg][1], srcB);
+                Bf[hb][gg][0] = __byte_perm(a0, b0, sel);
+                Bf[hb][gg][1] = __byte_perm(a1, b1, sel);
+            }
+        static_for<NK>([&](auto mc) {
+            constexpr int mm = decltype(mc)::value;
+            constexpr int gg = mm / KPG;
+            uint32_t A0, A1, A2, A3;
+            v_operand<D, mm>(X01, X01s, Y01, Y01s, X23, X23s, Y23, Y23s, A0, A1, A2, A3);
+#pragma unroll
+            for (int hb = 0; hb < NHB; ++hb) mma16816(O[hb][mm], A0, A1, A2, A3, Bf[hb][gg][0], Bf[hb][gg][1]);
+        });
+    }
+}
+
+// One INT2 page (16 tokens, the first `nvalid` valid) of one KV head, staged in shared memory at sb.
+template <int D, int G, int GQ, bool FULL>
+__device__ __forceinline__ void int2_page(const uint8_t* sb, int nvalid, int gid, int tig, float pvs,
+                                          const QueryOps<D, G, GQ>& qo, WarpAcc<D, G, GQ>& acc) {
+    const uint8_t* const one[1] = {sb};
+    int2_pages<D, G, GQ, 1, FULL>(one, nvalid, gid, tig, pvs, qo, acc);
 }
 
 // K operand of the low-bit plane: b0 * 2^(2p'-24) per code, the same positions and scale as k_operand.
@@ -960,12 +1010,13 @@ __device__ __forceinline__ void page_body(const uint8_t* sb, int nvalid, int gid
 // Streams this warp's pages (first + kWarps j, j < n_mine) of one (sequence, KV head, split) through
 // shared memory: kSlots slots of two pages, every lane copying its 16-byte chunks of a page with
 // cp.async, one commit group per slot, so waiting for all but the kSlots - 1 newest groups completes
-// the oldest slot. prologue() runs once the first copies are in flight; body(stage, nvalid, full) runs
-// for every page with a valid id, full = std::integral_constant<bool, nvalid == kPage>. Pairs of two
-// full, valid pages (all but the warp's last pair, normally) take one uniform test.
-template <int D, int G, typename Pro, typename Body>
+// the oldest slot. prologue() runs once the first copies are in flight; pair(stage0, stage1) takes two
+// full pages with valid ids (all but the warp's last pair, normally, after one uniform test), and
+// body(stage, nvalid) any other page with a valid id.
+template <int D, int G, typename Pro, typename Pair, typename Body>
 __device__ __forceinline__ void page_loop(const SplitArgs& a, int kv, int len, int first, int n_mine,
-                                          const int32_t* table, uint8_t* stage_base, Pro&& prologue, Body&& body) {
+                                          const int32_t* table, uint8_t* stage_base, Pro&& prologue, Pair&& pair,
+                                          Body&& body) {
     using GE = Geo<D, G>;
     constexpr int kChunks = GE::kBlock / 16;                 // 16-byte chunks per page block
     constexpr int kPerLane = (kChunks + 31) / 32;
@@ -1027,15 +1078,14 @@ __device__ __forceinline__ void page_loop(const SplitArgs& a, int kv, int len, i
         const uint8_t* sb = my_stage + slot * kSlotBytes;
         const uint32_t vb = (valid_bits >> (2 * slot)) & 3u;
         if (vb == 3u && 2 * i + 1 < j_full) {
-#pragma unroll 1
-            for (int e = 0; e < 2; ++e) body(sb + e * GE::kBlock, kPage, std::true_type{});
+            pair(sb, sb + GE::kBlock);
         } else {
 #pragma unroll 1
             for (int e = 0; e < 2; ++e)
                 if (vb & (1u << e)) {
                     // tokens of this page in the sequence (1..16)
                     const int nv = min(kPage, len - (first + kWarps * (2 * i + e)) * kPage);
-                    body(sb + e * GE::kBlock, nv, std::false_type{});
+                    body(sb + e * GE::kBlock, nv);
                 }
         }
         __syncwarp();                        // every lane is done reading the slot before it is refilled
@@ -1099,9 +1149,18 @@ __device__ void int2_split(const SplitArgs& a, int split, int kv, int b, uint8_t
                 pvs = a.pv_scale[kv];
                 inv_pvs = 1.0f / pvs;
             },
-            [&](const uint8_t* sb, int nv, auto full) {
-                page_body<D, G, GQ, CB, decltype(full)::value>(sb, nv, gid, tig, pvs, qo, acc);
-            });
+            [&](const uint8_t* sb0, const uint8_t* sb1) {
+                if constexpr (CB == OSCAR_CODEBOOK_LLOYD_MAX || GQ == 8) {
+                    // one page at a time: two pages' state does not fit beside these bodies' registers
+#pragma unroll 1
+                    for (int e = 0; e < 2; ++e)
+                        page_body<D, G, GQ, CB, true>(e ? sb1 : sb0, kPage, gid, tig, pvs, qo, acc);
+                } else {
+                    const uint8_t* const two[2] = {sb0, sb1};
+                    int2_pages<D, G, GQ, 2, true>(two, kPage, gid, tig, pvs, qo, acc);
+                }
+            },
+            [&](const uint8_t* sb, int nv) { page_body<D, G, GQ, CB, false>(sb, nv, gid, tig, pvs, qo, acc); });
 
         // ---- this warp's state -> shared memory (scaled to the CTA max)
 #pragma unroll
