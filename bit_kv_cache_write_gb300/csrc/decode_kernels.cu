@@ -1648,7 +1648,7 @@ template <int D>
 __global__ void __launch_bounds__(4 * D)
 merge_kernel(const float* __restrict__ partials, const float* __restrict__ r_vt, float* __restrict__ out, int h_q,
              int g, int int2_splits, int total_splits) {
-    constexpr int kPer = 16;
+    constexpr int kPer = 24;                 // 96 splits per round: one round at bs1 (79 splits)
     __shared__ float red_m[4], red_l[4];
     __shared__ float acc_rot[D];
     __shared__ float part_i[4][D], part_b[4][D];
