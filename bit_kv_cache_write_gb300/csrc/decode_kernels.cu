@@ -1811,11 +1811,11 @@ DecodePlan plan_decode(const Shape& s, int num_sms, int batch, int max_hist, int
     // (few units: bs1 decode); otherwise at most kMaxPagesPerSplit pages per split, in as many
     // waves as that takes (many units or long sequences)
     const int slots = split_ctas_per_sm(s) * num_sms;
-    // BF16 splits: when the grid is one wave of few units (bs1), one page per warp, so that the BF16
-    // segment's CTAs (CUDA-core attention, about 1.7x an INT2 split's bytes at 100k) finish with the
-    // INT2 splits; otherwise one split
+    // BF16 splits: two when the grid is one wave of few units (bs1), so that the BF16 segment's CTAs
+    // (CUDA-core attention, about 1.7x an INT2 split's bytes at 100k) finish within the INT2 splits'
+    // time while taking few of the wave's CTA slots (measured against three and five); otherwise one
     const int bf16_pages = (s.sink + s.recent + kPage - 1) / kPage;
-    p.bf16_splits = (units > 0 && slots / units >= 16 && bf16_pages >= 2) ? (bf16_pages + kWarps - 1) / kWarps : 1;
+    p.bf16_splits = (units > 0 && slots / units >= 16 && bf16_pages >= 2) ? 2 : 1;
     p.bf16_pages_per_split = (bf16_pages + p.bf16_splits - 1) / p.bf16_splits;
     int splits = units > 0 ? slots / units - p.bf16_splits : 1;
     if (splits < 1) splits = 1;
