@@ -1572,10 +1572,12 @@ __device__ __noinline__ void merge_group(const SplitArgs& a, int kv, int b, floa
     }
 }
 
-// Resident CTAs per SM the split kernel is compiled for: the Lloyd-Max body holds a second set of
-// Q.K accumulators.
+// Resident CTAs per SM the split kernel is compiled for: 3 (168 registers) for the uniform codebook. The
+// two-page body wants about 157 registers; at 4 CTAs (128) it is squeezed, and at bs1 the longer splits
+// of a 3-CTA wave also spread each warp's fixed costs over more pages (33.5 against 35.4 us per layer;
+// batch 64 within 1 %). The Lloyd-Max body holds a second set of Q.K accumulators.
 __host__ __device__ constexpr int split_min_blocks(int gq, int cb) {
-    return cb == OSCAR_CODEBOOK_LLOYD_MAX ? (gq == 8 ? 2 : 3) : (gq == 8 ? 3 : 4);
+    return cb == OSCAR_CODEBOOK_LLOYD_MAX ? (gq == 8 ? 2 : 3) : 3;
 }
 
 template <int D, int G, int GQ, int CB>
