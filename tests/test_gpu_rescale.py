@@ -60,8 +60,7 @@ def test_decode_with_large_logit_changes(cuda, name, over, kind):
         u /= np.linalg.norm(u)
         k[:, kv] += c[:, None] * u[None, :] * (1.0 / (d ** -0.5 * 1.4426950408889634 * np.linalg.norm(
             case.q[0, kv * g:(kv + 1) * g].astype(np.float64).mean(axis=0)) + 1e-30))
-    k = k.reshape(n_hist, h_kv * d)
-    k = torch.from_numpy(k.astype(np.float32)).to(torch.bfloat16).float().numpy()
+    k = torch.from_numpy(k.astype(np.float32)).to(torch.bfloat16).float().numpy()      # rows stay bf16
     t = np.arange(n_hist)
     slots = case.int2_tables[0, t // P].astype(np.int64) * P + t % P
     case.int2_pool[:] = 0
