@@ -228,18 +228,6 @@ __host__ __device__ constexpr int bit_offset(int kind, int c, int d) {
     return kind == 0 ? k_bit_offset(c, d) : v_bit_offset(c, d);
 }
 
-// Sum over the channels packed into word w of (0x4B400000 << bit). The float bits of
-// 1.5 * 2^23 + code are 0x4B400000 + code, so adding (bits << bit) for every channel and
-// subtracting this constant leaves the codes in place (all mod 2^32).
-__host__ __device__ constexpr uint32_t pack_bias(int kind, int w, int d) {
-    uint32_t b = 0u;
-    for (int c = 0; c < d; ++c) {
-        const int o = bit_offset(kind, c, d);
-        if (o / 32 == w) b += 0x4B400000u << (o % 32);
-    }
-    return b;
-}
-
 // The packed bit offset of channel 32 ch + j is off(j) + off(32 ch) for both layouts and head
 // sizes, with no carry out of a 32-bit word and a word shift of at most one. So one 32-channel
 // chunk body, with compile-time offsets, serves every chunk.
@@ -257,27 +245,75 @@ __host__ __device__ constexpr bool chunk_additive(int kind, int d) {
 static_assert(chunk_additive(0, 64) && chunk_additive(0, 128) && chunk_additive(1, 64) && chunk_additive(1, 128),
               "packed layout not chunk-additive");
 
-template <int KIND, int D, int W = 0>
-__device__ __forceinline__ void init_words(uint32_t* words) {
-    if constexpr (W < D / 16) {
-        constexpr uint32_t bias = pack_bias(KIND, W, D);
-        words[W] = 0u - bias;
-        init_words<KIND, D, W + 1>(words);
+// Pass 2 packs in fp32. Packed pairs are adjacent channels (j, j+1), j even. Channel c of a chunk
+// goes to a 16-bit slot (word, half) = (off / 32, off / 16 % 2) at field shift off % 16. Both
+// channels of a pair share the field shift, and the pairs with the same two slots form one chain.
+// A chain is packed by Horner steps on exact small integers, so each slot ends as 2^23 + its
+// 16-bit value (the float bits hold it in the low half).
+__host__ __device__ constexpr int slot_of(int kind, int c, int d) {
+    return 2 * (bit_offset(kind, c, d) >> 5) + ((bit_offset(kind, c, d) >> 4) & 1);
+}
+__host__ __device__ constexpr int field_of(int kind, int c, int d) { return bit_offset(kind, c, d) & 15; }
+// the first pair of pair j's chain
+__host__ __device__ constexpr int chain_head(int kind, int j, int d) {
+    for (int i = 0; i < j; i += 2)
+        if (slot_of(kind, i, d) == slot_of(kind, j, d) && slot_of(kind, i + 1, d) == slot_of(kind, j + 1, d)) return i;
+    return j;
+}
+// the pair of chain h whose field shift is s, or -1
+__host__ __device__ constexpr int chain_pair(int kind, int h, int s, int d) {
+    for (int j = h; j < 32; j += 2)
+        if (chain_head(kind, j, d) == h && field_of(kind, j, d) == s) return j;
+    return -1;
+}
+// every pair's channels share a field shift, every chain holds field 0, and the two channels of
+// a pair sit in different slots
+__host__ __device__ constexpr bool float_packable(int kind, int d) {
+    for (int j = 0; j < 32; j += 2) {
+        if (field_of(kind, j, d) != field_of(kind, j + 1, d)) return false;
+        if (slot_of(kind, j, d) == slot_of(kind, j + 1, d)) return false;
+        if (chain_head(kind, j, d) == j && chain_pair(kind, j, 0, d) < 0) return false;
+    }
+    return true;
+}
+static_assert(float_packable(0, 64) && float_packable(0, 128) && float_packable(1, 64) && float_packable(1, 128),
+              "packed layout not packable in fp32 pairs");
+
+// One Horner step per field of chain H, from field S down to 0 (PREV = the field before, or -1).
+template <int KIND, int D, int H, int S, int PREV>
+__device__ __forceinline__ uint64_t chain_step(const float (&v)[32], uint64_t mn2, uint64_t inv2, uint64_t acc) {
+    if constexpr (S < 0) {
+        return acc;
+    } else {
+        constexpr int J = chain_pair(KIND, H, S, D);
+        if constexpr (J < 0) {
+            return chain_step<KIND, D, H, S - 2, PREV>(v, mn2, inv2, acc);
+        } else {
+            // rint(u) + 1.5 * 2^23, then minus 1.5 * 2^23 (or minus 2^22 on field 0, leaving 2^23 + code)
+            const uint64_t r2 = add_f32x2(mul_f32x2(sub_f32x2(f32x2(v[J], v[J + 1]), mn2), inv2),
+                                          f32x2(12582912.0f, 12582912.0f));
+            const uint64_t c2 = S == 0 ? sub_f32x2(r2, f32x2(4194304.0f, 4194304.0f))
+                                       : sub_f32x2(r2, f32x2(12582912.0f, 12582912.0f));
+            uint64_t a = c2;
+            if constexpr (PREV >= 0) {
+                constexpr float k = (float)(1 << (PREV - S));
+                a = fma_f32x2(acc, f32x2(k, k), c2);                   // exact: every partial sum < 2^24
+            }
+            return chain_step<KIND, D, H, S - 2, S>(v, mn2, inv2, a);
+        }
     }
 }
 
-// Packs one row's clipped values (32-column chunk ch at a time) into words and stores the row.
-template <int D, int G, int KIND>
-__device__ __forceinline__ void pack_chunk(const float (&v)[32], int ch, const float* mn, const float* inv,
-                                           uint32_t* words) {
-#pragma unroll
-    for (int j = 0; j < 32; ++j) {
-        const int c = 32 * ch + j, g = c / G;
-        // u in [0, 3 + tiny]: adding 1.5 * 2^23 rounds it half-to-even onto the integer grid
-        const float u = __fmul_rn(__fsub_rn(v[j], mn[g]), inv[g]);
-        const uint32_t bits = __float_as_uint(__fadd_rn(u, 12582912.0f));
-        const int off = bit_offset(KIND, c, D);
-        words[off >> 5] += bits << (off & 31);
+// Packs one 32-channel chunk: slot k ends as the float 2^23 + (its 16-bit value).
+template <int KIND, int D, int H = 0>
+__device__ __forceinline__ void pack_chains(const float (&v)[32], uint64_t mn2, uint64_t inv2, uint32_t* slot) {
+    if constexpr (H < 32) {
+        if constexpr (chain_head(KIND, H, D) == H) {
+            const uint64_t acc = chain_step<KIND, D, H, 14, -1>(v, mn2, inv2, 0ull);
+            slot[slot_of(KIND, H, D)] = (uint32_t)acc;
+            slot[slot_of(KIND, H + 1, D)] = (uint32_t)(acc >> 32);
+        }
+        pack_chains<KIND, D, H + 2>(v, mn2, inv2, slot);
     }
 }
 
@@ -601,11 +637,12 @@ __device__ __forceinline__ void epilogue_tile(uint32_t tacc, uint32_t acc_empty,
     for (int g = 0; g < NG; ++g) { mn_sz[g] = mn[g]; mx_sz[g] = mx[g]; }
     const bool any_need = __any_sync(0xffffffffu, need);
 
-    // ---- pass 2: codes in fp32, packed in place (one chunk body; offsets = off(j) + off(32 ch))
+    // ---- pass 2: codes in fp32, packed by fp32 Horner steps (one chunk body; offsets = off(j) + off(32 ch))
     float inv[NG];
     group_inv<D, G>(mn, mx, inv);
     uint32_t words[D / 16];
-    init_words<KIND, D>(words);
+#pragma unroll
+    for (int w = 0; w < D / 16; ++w) words[w] = 0u;
 #pragma unroll 1
     for (int ch = 0; ch < NCH; ++ch) {
         float v[32];
@@ -619,29 +656,24 @@ __device__ __forceinline__ void epilogue_tile(uint32_t tacc, uint32_t acc_empty,
 #pragma unroll
         for (int g = 1; g < NG; ++g)
             if ((32 * ch) / G == g) { gmn = mn[g]; ginv = inv[g]; }
-        uint32_t cw[D / 16];
-#pragma unroll
-        for (int w = 0; w < D / 16; ++w) cw[w] = 0u;
         // u = (x_hat - mn) * inv, then + 1.5 * 2^23, two channels per packed fp32 instruction (each
         // half rounds exactly as the scalar op would). u is in [0, 3 + tiny], so adding 1.5 * 2^23
-        // rounds it half-to-even onto the integer grid. x_hat was clipped in pass 1.
-        const uint64_t mn2 = f32x2(gmn, gmn), inv2 = f32x2(ginv, ginv), mag2 = f32x2(12582912.0f, 12582912.0f);
+        // rounds it half-to-even onto the integer grid; subtracting 1.5 * 2^23 again leaves the code
+        // (2^22 instead on a chain's field 0, which leaves 2^23 + code). x_hat was clipped in pass 1.
+        const uint64_t mn2 = f32x2(gmn, gmn), inv2 = f32x2(ginv, ginv);
+        uint32_t slot[D / 8];
 #pragma unroll
-        for (int j = 0; j < 32; j += 2) {
-            const uint64_t b2 = add_f32x2(mul_f32x2(sub_f32x2(f32x2(v[j], v[j + 1]), mn2), inv2), mag2);
-            const uint32_t bits0 = (uint32_t)b2, bits1 = (uint32_t)(b2 >> 32);
-            const int off0 = bit_offset(KIND, j, D), off1 = bit_offset(KIND, j + 1, D);
-            cw[off0 >> 5] += bits0 << (off0 & 31);
-            cw[off1 >> 5] += bits1 << (off1 & 31);
-        }
+        for (int k = 0; k < D / 8; ++k) slot[k] = 0x4B000000u;
+        pack_chains<KIND, D>(v, mn2, inv2, slot);
+        // the low 16 bits of each slot's float bits hold its codes; PRMT joins the two halves of a word
         const int delta = bit_offset(KIND, 32 * ch, D);
         const int bs = delta & 31;
         if (delta >> 5) {
 #pragma unroll
-            for (int w = D / 16 - 1; w >= 1; --w) words[w] += cw[w - 1] << bs;
+            for (int w = D / 16 - 1; w >= 1; --w) words[w] += __byte_perm(slot[2 * w - 2], slot[2 * w - 1], 0x5410) << bs;
         } else {
 #pragma unroll
-            for (int w = 0; w < D / 16; ++w) words[w] += cw[w] << bs;
+            for (int w = 0; w < D / 16; ++w) words[w] += __byte_perm(slot[2 * w], slot[2 * w + 1], 0x5410) << bs;
         }
     }
     // the codes are final (they use the tensor-core stats): store them now, so that only a few
