@@ -428,13 +428,11 @@ def measured_peak():
 
 def oracle_sample(cfg, sample_hist, layer=0):
     """Build the oracle-side cache for a bounded sample (one layer, ``sample_hist`` history tokens)."""
-    import numpy as np
-    sys.path.insert(0, os.path.join(ROOT, "tests"))
-    import cases
     from bit_kv_cache_write_gb300 import synth
+    from oracle.paged_case import DecodeCase
     c = dict(cfg)
     c["hist"] = sample_hist
-    case = cases.DecodeCase(c, [sample_hist], [synth.SINK + synth.RECENT], layer=layer, extra_pages=1)
+    case = DecodeCase(c, [sample_hist], [synth.SINK + synth.RECENT], layer=layer, extra_pages=1)
     return case
 
 

@@ -29,4 +29,5 @@ quantize   rotate -> clip -> group scale/zero -> 2-bit code; dequant.
 layout     the paged INT2 / BF16 page layout: bit positions, packing, pool I/O.
 attention  three-segment decode attention and the online-softmax merge.
 calibrate  per-(layer, KV head) calibration driver built from ``rotation``.
+paged_case seeded paged INT2 + BF16 caches written by the oracle, and their expected decode.
 """
