@@ -42,6 +42,7 @@ WRITE_CASES = [
     ("qwen3_8b_bs1_100k", dict(group=32), 333),
     ("qwen3_8b_bs1_100k", dict(group=64, h_kv=2, h_q=4), 5),
     ("tiny", {}, 1),
+    ("qwen3_8b_bs1_100k", {}, 8),                                # one token per CTA, four warps per token
     ("qwen3_8b_bs1_100k", dict(rotation="hadamard"), 777),      # Hadamard-only ablation, tensor cores
     ("qwen3_8b_bs1_100k", dict(rotation="hadamard"), 40),       # and CUDA cores
 ]
@@ -149,7 +150,9 @@ def test_write_twice_is_idempotent_and_n0_is_noop(cuda):
     assert torch.equal(first, pool)
 
 
-@pytest.mark.parametrize("name,n", [("tiny", 300), ("qwen3_8b_bs1_100k", 256)])
+# 1 and 8 tokens take the one-token-per-CTA kernel (the bs1 demote), 256 and 300 one token per warp
+@pytest.mark.parametrize("name,n", [("tiny", 300), ("qwen3_8b_bs1_100k", 256), ("qwen3_8b_bs1_100k", 1),
+                                    ("tiny", 8), ("qwen3_4b_b64_32k", 3)])
 def test_demote_parity(cuda, name, n):
     cfg = cases.workload(name)
     li, (rk, rv, tk, tv) = cases.calibration(cfg)
