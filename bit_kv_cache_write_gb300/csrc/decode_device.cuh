@@ -1672,21 +1672,29 @@ merge_kernel(const float* __restrict__ partials, const float* __restrict__ r_vt,
     pdl_wait();
     pdl_trigger();
     const float* part = partials + (size_t)bh * total_splits * (D + 2);
+    const int lane = tid % 32;
     float M = -INFINITY, L = 0.0f, ai = 0.0f, ab = 0.0f;
     for (int s0 = 0; s0 < total_splits; s0 += 4 * kPer) {
-        float ms[kPer], ls[kPer], as[kPer];
-        float mloc = -INFINITY;
+        // the quarter's splits s0 + 4k + quarter: lane k of each warp loads split k's (m, l) (the same
+        // for every channel), every thread its channel's accumulator of each split
+        float m_k = -INFINITY, l_k = 0.0f;
+        {
+            const int sp = s0 + 4 * lane + quarter;
+            if (lane < kPer && sp < total_splits) {
+                const float* r = part + (size_t)sp * (D + 2);
+                m_k = __ldcg(r);
+                l_k = __ldcg(r + 1);
+            }
+        }
+        float as[kPer];
 #pragma unroll
         for (int k = 0; k < kPer; ++k) {
             const int sp = s0 + 4 * k + quarter;
-            const bool ok = sp < total_splits;
-            const float* r = part + (size_t)sp * (D + 2);
-            ms[k] = ok ? __ldcg(r) : -INFINITY;
-            ls[k] = ok ? __ldcg(r + 1) : 0.0f;
-            as[k] = ok ? __ldcg(r + 2 + c) : 0.0f;
-            mloc = fmaxf(mloc, ms[k]);
+            as[k] = sp < total_splits ? __ldcg(part + (size_t)sp * (D + 2) + 2 + c) : 0.0f;
         }
-        // every channel of a quarter holds the same m values
+        float mloc = m_k;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) mloc = fmaxf(mloc, __shfl_xor_sync(0xffffffffu, mloc, o));
         if (c == 0) red_m[quarter] = mloc;
         __syncthreads();
         const float mn = fmaxf(M, fmaxf(fmaxf(red_m[0], red_m[1]), fmaxf(red_m[2], red_m[3])));
@@ -1694,11 +1702,15 @@ merge_kernel(const float* __restrict__ partials, const float* __restrict__ r_vt,
         ai *= sc;
         ab *= sc;
         L *= sc;
+        const float w_k = m_k == -INFINITY ? 0.0f : fast_exp2(m_k - mn);
+        float lw = l_k * w_k;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) lw += __shfl_xor_sync(0xffffffffu, lw, o);
+        L += lw;
 #pragma unroll
         for (int k = 0; k < kPer; ++k) {
             const int sp = s0 + 4 * k + quarter;
-            const float w = ms[k] == -INFINITY ? 0.0f : fast_exp2(ms[k] - mn);
-            L = fmaf(ls[k], w, L);
+            const float w = __shfl_sync(0xffffffffu, w_k, k);
             if (sp < int2_splits) ai = fmaf(as[k], w, ai); else ab = fmaf(as[k], w, ab);
         }
         M = mn;
