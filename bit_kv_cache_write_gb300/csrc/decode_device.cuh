@@ -103,6 +103,7 @@ constexpr int kMaxPagesPerSplit = 128;             // longest INT2 split when th
 // bs1 decodes with ~80 splits keep the wider merge kernel
 constexpr int kFuseWeights = 128;
 constexpr int kSliceCh = 32;                       // rotated channels per q_prep CTA
+constexpr size_t kMergeUnitWeightBytes = 160 * 1024;  // largest weight table of the per-unit merge
 
 __device__ __forceinline__ float fast_exp2(float x) { return exp2f(x); }
 
@@ -1732,6 +1733,101 @@ merge_kernel(const float* __restrict__ partials, const float* __restrict__ r_vt,
         const float oi = (part_i[0][c] + part_i[1][c]) + (part_i[2][c] + part_i[3][c]);
         const float ob = (part_b[0][c] + part_b[1][c]) + (part_b[2][c] + part_b[3][c]);
         out[(size_t)bh * D + c] = Lt > 0.0f ? (oi + ob) / Lt : 0.0f;
+    }
+}
+
+// Merge of all splits of the GQ query heads of one (sequence, KV head), for plans whose per-head merge
+// grid would take more than one wave (many query heads): R_v^T is read once per (sequence, KV head)
+// instead of once per query head, and the grid is GQ times smaller. Block of 4*D threads: warp h finds
+// head h's split weights; thread (c, quarter) then sums its quarter of the splits for every head (loads
+// of kRound splits in flight per round, spread over the heads) and a quarter of the un-rotation terms.
+template <int D, int GQ>
+__global__ void __launch_bounds__(4 * D)
+merge_unit_kernel(const float* __restrict__ partials, const float* __restrict__ r_vt, float* __restrict__ out,
+                  int h_kv, int int2_splits, int total_splits) {
+    constexpr int kRound = 24;                          // accumulator loads per thread per round
+    constexpr int kPerHead = (kRound + GQ - 1) / GQ;    // splits of each head per round and quarter
+    static_assert(GQ <= 4 * D / 32, "one warp per query head");
+    extern __shared__ float w_s[];                      // [GQ][total_splits] split weights
+    __shared__ float l_s[GQ];
+    __shared__ float red_i[4][GQ][D], red_b[4][GQ][D];
+    __shared__ float acc_rot[GQ][D], acc_b[GQ][D];
+    const int unit = blockIdx.x, b = unit / h_kv, kv = unit % h_kv;
+    const int tid = threadIdx.x, c = tid % D, quarter = tid / D, warp = tid / 32, lane = tid % 32;
+    const int T = total_splits;
+    const float* rt = r_vt + (size_t)kv * D * D + (size_t)quarter * (D / 4) * D + c;
+    float rv[D / 4];
+#pragma unroll
+    for (int i = 0; i < D / 4; ++i) rv[i] = __ldg(rt + (size_t)i * D);
+    pdl_wait();
+    pdl_trigger();
+    const float* part0 = partials + ((size_t)b * h_kv * GQ + (size_t)kv * GQ) * T * (D + 2);
+    if (warp < GQ) {
+        const float* part = part0 + (size_t)warp * T * (D + 2);
+        float M = -INFINITY;
+        for (int s0 = 0; s0 < T; s0 += 32)
+            if (s0 + lane < T) M = fmaxf(M, __ldcg(part + (size_t)(s0 + lane) * (D + 2)));
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+        float L = 0.0f;
+        for (int s0 = 0; s0 < T; s0 += 32) {
+            const int sp = s0 + lane;
+            if (sp < T) {
+                const float m = __ldcg(part + (size_t)sp * (D + 2));
+                const float w = (M == -INFINITY || m == -INFINITY) ? 0.0f : fast_exp2(m - M);
+                w_s[warp * T + sp] = w;
+                L = fmaf(__ldcg(part + (size_t)sp * (D + 2) + 1), w, L);
+            }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
+        if (lane == 0) l_s[warp] = L;
+    }
+    __syncthreads();
+    float ai[GQ], ab[GQ];
+#pragma unroll
+    for (int h = 0; h < GQ; ++h) { ai[h] = 0.0f; ab[h] = 0.0f; }
+    for (int k0 = 0; 4 * k0 + quarter < T; k0 += kPerHead) {
+        // splits with weight 0 (empty splits of the shorter sequences, or far below the maximum) are not read
+        float v[GQ][kPerHead], wv[GQ][kPerHead];
+#pragma unroll
+        for (int h = 0; h < GQ; ++h)
+#pragma unroll
+            for (int k = 0; k < kPerHead; ++k) {
+                const int sp = 4 * (k0 + k) + quarter;
+                wv[h][k] = sp < T ? w_s[h * T + sp] : 0.0f;
+                v[h][k] = wv[h][k] != 0.0f ? __ldcg(part0 + ((size_t)h * T + sp) * (D + 2) + 2 + c) : 0.0f;
+            }
+#pragma unroll
+        for (int h = 0; h < GQ; ++h)
+#pragma unroll
+            for (int k = 0; k < kPerHead; ++k) {
+                const int sp = 4 * (k0 + k) + quarter;
+                const float x = v[h][k] * wv[h][k];
+                if (sp < int2_splits) ai[h] += x; else ab[h] += x;
+            }
+    }
+#pragma unroll
+    for (int h = 0; h < GQ; ++h) { red_i[quarter][h][c] = ai[h]; red_b[quarter][h][c] = ab[h]; }
+    __syncthreads();
+    for (int h = quarter; h < GQ; h += 4) {
+        acc_rot[h][c] = (red_i[0][h][c] + red_i[1][h][c]) + (red_i[2][h][c] + red_i[3][h][c]);
+        acc_b[h][c] = (red_b[0][h][c] + red_b[1][h][c]) + (red_b[2][h][c] + red_b[3][h][c]);
+    }
+    __syncthreads();
+    // un-rotation: quarter q of the terms of every head, then the quarters are summed per head
+#pragma unroll
+    for (int h = 0; h < GQ; ++h) {
+        float o = 0.0f;
+#pragma unroll
+        for (int i = 0; i < D / 4; ++i) o = fmaf(acc_rot[h][quarter * (D / 4) + i], rv[i], o);
+        red_i[quarter][h][c] = o;
+    }
+    __syncthreads();
+    for (int h = quarter; h < GQ; h += 4) {
+        const float Lt = l_s[h];
+        const float oi = (red_i[0][h][c] + red_i[1][h][c]) + (red_i[2][h][c] + red_i[3][h][c]);
+        out[((size_t)unit * GQ + h) * D + c] = Lt > 0.0f ? (oi + acc_b[h][c]) / Lt : 0.0f;
     }
 }
 

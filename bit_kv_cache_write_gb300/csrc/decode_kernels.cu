@@ -54,6 +54,11 @@ DecodePlan plan_decode(const Shape& s, int num_sms, int batch, int max_hist, int
     p.ws_total = p.ws_partials + p.ws_qrot + p.ws_counters;
     // the last-CTA merge keeps its weights in the page-stage shared memory (at least 12 KB)
     p.fuse_merge = prefix_pages == 0 && (size_t)(s.h_q / s.h_kv) * p.total_splits <= kFuseWeights;
+    // the merge kernel runs one CTA per SM (512 threads, about 120 registers): when one CTA per query head
+    // would take more than one wave, one CTA per (sequence, KV head) merges all its query heads and reads
+    // R_v^T once for them
+    p.merge_per_unit = !p.fuse_merge && s.h_q / s.h_kv >= 2 && (long long)batch * s.h_q > num_sms &&
+                       (size_t)(s.h_q / s.h_kv) * p.total_splits * sizeof(float) <= kMergeUnitWeightBytes;
     return p;
 }
 
@@ -119,6 +124,22 @@ cudaError_t launch_decode(const Shape& s, const LayerParams& prm, const DecodePl
     if (plan.fuse_merge) return cudaSuccess;           // merged by the last CTA of each unit
 
     ProfScope ps_merge(prof, OSCAR_KERNEL_MERGE, st);
+    if (plan.merge_per_unit) {
+        const size_t wbytes = (size_t)g * plan.total_splits * sizeof(float);
+        const dim3 grid(a.batch * s.h_kv), block(4 * s.d);
+        const int i2 = plan.prefix_splits + plan.int2_splits;
+#define OSCAR_MERGE_UNIT(D_, G_)                                                                            \
+        if (s.d == D_ && g == G_) {                                                                         \
+            const cudaError_t at = smem_opt_in<merge_unit_kernel<D_, G_>>(kMergeUnitWeightBytes);         \
+            if (at != cudaSuccess) return at;                                                                \
+            return launch_pdl(merge_unit_kernel<D_, G_>, grid, block, wbytes, st, (const float*)partials,  \
+                              prm.r_vt, a.out, s.h_kv, i2, plan.total_splits);                              \
+        }
+        OSCAR_MERGE_UNIT(128, 2) OSCAR_MERGE_UNIT(128, 4) OSCAR_MERGE_UNIT(128, 8)
+        OSCAR_MERGE_UNIT(64, 2) OSCAR_MERGE_UNIT(64, 4) OSCAR_MERGE_UNIT(64, 8)
+#undef OSCAR_MERGE_UNIT
+        return cudaErrorInvalidValue;
+    }
     if (s.d == 128)
         return launch_pdl(merge_kernel<128>, dim3(a.batch * s.h_q), dim3(4 * 128), 0, st, (const float*)partials,
                           prm.r_vt, a.out, s.h_q, g, plan.prefix_splits + plan.int2_splits, plan.total_splits);

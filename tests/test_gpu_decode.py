@@ -134,6 +134,19 @@ def test_workspace_too_small_is_rejected(cuda):
     assert e.value.status == -7
 
 
+def test_merge_one_cta_per_kv_head(cuda):
+    """GQA 4, five sequences, one of 66,000 tokens: 33 INT2 splits of up to 128 pages keep 34 partials per
+    query head (too many for the last-CTA merge), and 160 query heads exceed one wave of merge CTAs, so the
+    merge takes one (sequence, KV head) per CTA. Checked on every head of the long and one short sequence."""
+    cfg = cases.workload("qwen3_8b_bs1_100k")
+    case = cases.DecodeCase(cfg, [66000, 1000, 1000, 1000, 1000], [320] * 5)
+    got, _ = run_gpu(case, cuda)
+    want = case.oracle_out(seqs=[0, 3])
+    err, rel = cases.check_decode(got[[0, 3]], want[[0, 3]])
+    assert np.isfinite(got).all()
+    print("max-abs %.3g rel-L2 %.3g" % (err, rel))
+
+
 def test_qwen3_8b_full_100k_context(cuda):
     """bs1, 100,000-token context (64 sink + 99,680 INT2 + 256 recent), Qwen3-8B shape, all 32 heads."""
     cfg = cases.workload("qwen3_8b_bs1_100k")
