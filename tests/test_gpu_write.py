@@ -229,6 +229,37 @@ def test_debug_bounds_records_bad_slot(cuda):
     assert float(np.abs(s.astype(np.float64)).max()) > 0
 
 
+def test_debug_bounds_records_bad_demote_source(cuda):
+    """Two-token demote (one CTA per token) with debug bounds: a source slot past the BF16 pool is recorded
+    (kind 1) and its destination left untouched; the other token is demoted."""
+    cfg = cases.workload("tiny")
+    li, (rk, rv, tk, tv) = cases.calibration(cfg)
+    d, h_kv = cfg["d"], cfg["h_kv"]
+    geo = layout.Int2Geometry(d, cfg["group"], h_kv)
+    ctx = make_ctx(cfg, debug=1)
+    ctx.calibrate_upload(0, rk, rv, tk, tv)
+    bf_pages = 2
+    k, v = li.kv("dbg-demote", bf_pages * P)
+    bf_pool = np.zeros(bf_pages * h_kv * 2 * P * d, np.float32)
+    for s_ in range(bf_pages * P):
+        for h in range(h_kv):
+            o = layout.bf16_offset(s_ // P, h, "k", s_ % P, d, h_kv)
+            bf_pool[o:o + d] = k[s_, h]
+            o = layout.bf16_offset(s_ // P, h, "v", s_ % P, d, h_kv)
+            bf_pool[o:o + d] = v[s_, h]
+    src = torch.tensor([3, 5 * P + 1], dtype=torch.int64, device=cuda)      # page 5 does not exist
+    dst = torch.tensor([17, 2], dtype=torch.int64, device=cuda)
+    pool = torch.zeros(2 * geo.page_bytes, dtype=torch.uint8, device=cuda)
+    ctx.demote_recent(0, bf16(bf_pool, cuda), src, pool, dst)
+    st, kind, index = ctx.debug_error()
+    assert st == -5 and kind == 1 and index == 5 * P + 1
+    got = pool.cpu().numpy()
+    c, s17, z = layout.read_int2_token(got, geo, 17, 0, "k")
+    assert float(np.abs(s17.astype(np.float64)).max()) > 0
+    c, s2, z = layout.read_int2_token(got, geo, 2, 0, "k")
+    assert float(np.abs(s2.astype(np.float64)).max()) == 0 and not c.any()
+
+
 def test_debug_bounds_on_the_tensor_core_path(cuda):
     cfg = cases.workload("qwen3_8b_bs1_100k")
     li, (rk, rv, tk, tv) = cases.calibration(cfg)
