@@ -219,6 +219,75 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t phase) {
 // Query preparation
 // ---------------------------------------------------------------------------------------------
 
+// The rest of q_prep for one (query head, channel) once the four quarter partials of q . R_k[:, c] are
+// known: double-float sum, times sm_scale log2(e), the exponent grid from the norm bound, the three
+// digits, and (through the warp, whose 32 lanes are the slice's channels) the slice's digit sums.
+template <int D>
+__device__ __forceinline__ void q_prep_finish(const float (&hi_u)[4], const float (&lo_u)[4], float nq2, float cmax,
+                                              float sl2_hi, float sl2_lo, size_t bh, int slice, int cl, int c,
+                                              __half* __restrict__ qb, float* __restrict__ kap,
+                                              float* __restrict__ qdig) {
+    constexpr int NS = D / kSliceCh;
+    float h = 0.0f, l = 0.0f;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+        float s2, e2;
+        two_sum(h, hi_u[u], s2, e2);
+        h = s2;
+        l = __fadd_rn(l, __fadd_rn(lo_u[u], e2));
+    }
+    {
+        float s2, e2;
+        two_sum(h, l, s2, e2);
+        h = s2;
+        l = e2;
+    }
+    // times sm_scale * log2(e) (hi + lo): the INT2 logits come out in log2 units
+    {
+        float p, e, s2, e2;
+        two_prod(h, sl2_hi, p, e);
+        e = __fmaf_rn(h, sl2_lo, __fmaf_rn(l, sl2_hi, e));
+        two_sum(p, e, s2, e2);
+        h = s2;
+        l = e2;
+    }
+    // exponent from the bound: (sl2 |q| cmax)^2 with a relative margin for the rounding of |q|^2
+    const float sc = sl2_hi * cmax;
+    const float bound2 = nq2 * sc * sc * 1.0001f;
+    int e2x = 0;
+    frexpf(bound2, &e2x);                              // bound2 < 2^e2x
+    const int ex = (e2x + 1) >> 1;                     // bound < 2^ex (arithmetic shift: ceil(e2x / 2))
+    const bool any = nq2 > 0.0f;
+    // r_hi, r_mid, r_lo: successive 11-bit digits of q_rot / 2^(ex-11)
+    const float xh = ldexpf(h, 11 - ex), xl = ldexpf(l, 11 - ex);
+    const float r_hi = any ? rintf(xh) : 0.0f;
+    const float rem1 = __fadd_rn(__fsub_rn(xh, r_hi), xl);                // |rem1| <= 0.5 + tiny
+    const float r_mid = any ? rintf(__fmul_rn(rem1, 2048.0f)) : 0.0f;
+    const float rem2 = __fsub_rn(__fmul_rn(rem1, 2048.0f), r_mid);
+    const float r_lo = any ? rintf(__fmul_rn(rem2, 2048.0f)) : 0.0f;
+    const int pos = 2 * ((c / 16) % 4) + (c % 4) / 2;                     // K-layout position of channel c
+    const int sh = 4 - 2 * pos_scale(pos);
+    __half* dst = qb + (size_t)bh * 3 * D;
+    dst[c] = __float2half_rn(ldexpf(r_hi, sh));
+    dst[D + c] = __float2half_rn(ldexpf(r_mid, sh));
+    dst[2 * D + c] = __float2half_rn(ldexpf(r_lo, sh));
+    if (slice == 0 && cl == 0) kap[bh] = any ? ldexpf(1.0f, ex + 9) : 0.0f;
+    // exact integer digit sums of the slice (|sum| <= 32 * 2048)
+    float d0 = r_hi, d1 = r_mid, d2 = r_lo;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        d0 += __shfl_xor_sync(0xffffffffu, d0, o);
+        d1 += __shfl_xor_sync(0xffffffffu, d1, o);
+        d2 += __shfl_xor_sync(0xffffffffu, d2, o);
+    }
+    if (cl == 0) {
+        float* qd = qdig + ((size_t)bh * NS + slice) * 3;
+        qd[0] = d0;
+        qd[1] = d1;
+        qd[2] = d2;
+    }
+}
+
 // One CTA of 128 threads per (query head, slice of 32 rotated channels): thread (channel, quarter)
 // accumulates D/4 terms of the dot product.
 //   q_rot[c] = sum_i q_i R[i][c] as hi + lo fp32 (error-free products and sums), times
@@ -237,7 +306,6 @@ q_prep_kernel(const __nv_bfloat16* __restrict__ q, const float* __restrict__ r_k
               __half* __restrict__ qb, float* __restrict__ kap, float* __restrict__ qdig, int h_q, int g,
               float sl2_hi, float sl2_lo, int* __restrict__ counters, int counters_per_unit) {
     constexpr int Q4 = D / 4;
-    constexpr int NS = D / kSliceCh;
     __shared__ float qs[D];
     __shared__ float hi_s[4][kSliceCh], lo_s[4][kSliceCh];
     __shared__ float nq2_s;
@@ -282,64 +350,74 @@ q_prep_kernel(const __nv_bfloat16* __restrict__ q, const float* __restrict__ r_k
     lo_s[quarter][cl] = lo;
     __syncthreads();
     if (quarter != 0) return;
-    float h = 0.0f, l = 0.0f;
+    float hi_u[4], lo_u[4];
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-        float s2, e2;
-        two_sum(h, hi_s[u][cl], s2, e2);
-        h = s2;
-        l = __fadd_rn(l, __fadd_rn(lo_s[u][cl], e2));
-    }
-    {
-        float s2, e2;
-        two_sum(h, l, s2, e2);
-        h = s2;
-        l = e2;
-    }
-    // times sm_scale * log2(e) (hi + lo): the INT2 logits come out in log2 units
-    {
-        float p, e, s2, e2;
-        two_prod(h, sl2_hi, p, e);
-        e = __fmaf_rn(h, sl2_lo, __fmaf_rn(l, sl2_hi, e));
-        two_sum(p, e, s2, e2);
-        h = s2;
-        l = e2;
-    }
-    // exponent from the bound: (sl2 |q| cmax)^2 with a relative margin for the rounding of |q|^2
-    const float nq2 = nq2_s;
-    const float sc = sl2_hi * cmax;
-    const float bound2 = nq2 * sc * sc * 1.0001f;
-    int e2x = 0;
-    frexpf(bound2, &e2x);                              // bound2 < 2^e2x
-    const int ex = (e2x + 1) >> 1;                     // bound < 2^ex (arithmetic shift: ceil(e2x / 2))
-    const bool any = nq2 > 0.0f;
-    // r_hi, r_mid, r_lo: successive 11-bit digits of q_rot / 2^(ex-11)
-    const float xh = ldexpf(h, 11 - ex), xl = ldexpf(l, 11 - ex);
-    const float r_hi = any ? rintf(xh) : 0.0f;
-    const float rem1 = __fadd_rn(__fsub_rn(xh, r_hi), xl);                // |rem1| <= 0.5 + tiny
-    const float r_mid = any ? rintf(__fmul_rn(rem1, 2048.0f)) : 0.0f;
-    const float rem2 = __fsub_rn(__fmul_rn(rem1, 2048.0f), r_mid);
-    const float r_lo = any ? rintf(__fmul_rn(rem2, 2048.0f)) : 0.0f;
-    const int pos = 2 * ((c / 16) % 4) + (c % 4) / 2;                     // K-layout position of channel c
-    const int sh = 4 - 2 * pos_scale(pos);
-    __half* dst = qb + (size_t)bh * 3 * D;
-    dst[c] = __float2half_rn(ldexpf(r_hi, sh));
-    dst[D + c] = __float2half_rn(ldexpf(r_mid, sh));
-    dst[2 * D + c] = __float2half_rn(ldexpf(r_lo, sh));
-    if (slice == 0 && cl == 0) kap[bh] = any ? ldexpf(1.0f, ex + 9) : 0.0f;
-    // exact integer digit sums of the slice (|sum| <= 32 * 2048)
-    float d0 = r_hi, d1 = r_mid, d2 = r_lo;
+    for (int u = 0; u < 4; ++u) { hi_u[u] = hi_s[u][cl]; lo_u[u] = lo_s[u][cl]; }
+    q_prep_finish<D>(hi_u, lo_u, nq2_s, cmax, sl2_hi, sl2_lo, bh, slice, cl, c, qb, kap, qdig);
+}
+
+// q_prep for the GQ query heads of one (sequence, KV head) and one slice of 32 rotated channels, for plans
+// with many query heads: the R_k terms load once for the GQ heads, and the GQ double-float chains of a
+// thread are independent. Every head's |q|^2, dot products and digits are formed in the same order as in
+// q_prep_kernel, so both give the same bits.
+template <int D, int GQ>
+__global__ void __launch_bounds__(128)
+q_prep_unit_kernel(const __nv_bfloat16* __restrict__ q, const float* __restrict__ r_k,
+                   const float* __restrict__ colmax, __half* __restrict__ qb, float* __restrict__ kap,
+                   float* __restrict__ qdig, int h_kv, float sl2_hi, float sl2_lo, int* __restrict__ counters,
+                   int counters_per_unit) {
+    constexpr int Q4 = D / 4;
+    __shared__ float qs[GQ][D];
+    __shared__ float hi_s[GQ][4][kSliceCh], lo_s[GQ][4][kSliceCh];
+    __shared__ float nq2_s[GQ];
+    const int unit = blockIdx.x, slice = blockIdx.y;
+    const int kv = unit % h_kv;
+    const int cl = threadIdx.x % kSliceCh, quarter = threadIdx.x / kSliceCh;
+    const int c = slice * kSliceCh + cl;
+    const float* r = r_k + (size_t)kv * D * D + (size_t)quarter * Q4 * D + c;
+    float rv[Q4];
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        d0 += __shfl_xor_sync(0xffffffffu, d0, o);
-        d1 += __shfl_xor_sync(0xffffffffu, d1, o);
-        d2 += __shfl_xor_sync(0xffffffffu, d2, o);
+    for (int i = 0; i < Q4; ++i) rv[i] = __ldg(r + (size_t)i * D);
+    const float cmax = __ldg(colmax + kv);
+    pdl_wait();
+    pdl_trigger();
+    if (slice == 0)
+        for (int i = threadIdx.x; i < counters_per_unit; i += blockDim.x) counters[(size_t)unit * counters_per_unit + i] = 0;
+    const size_t bh0 = (size_t)unit * GQ;                 // b * h_q + kv * GQ
+    for (int i = threadIdx.x; i < GQ * D; i += blockDim.x) qs[i / D][i % D] = __bfloat162float(q[bh0 * D + i]);
+    __syncthreads();
+    // |q|^2 of head h by warp h % 4, in the per-head kernel's order
+    for (int h = quarter; h < GQ; h += 4) {
+        float s2 = 0.0f;
+#pragma unroll
+        for (int k = 0; k < D / 32; ++k) s2 = __fmaf_rn(qs[h][cl + 32 * k], qs[h][cl + 32 * k], s2);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) s2 = __fadd_rn(s2, __shfl_xor_sync(0xffffffffu, s2, o));
+        if (cl == 0) nq2_s[h] = s2;
     }
-    if (cl == 0) {
-        float* qd = qdig + ((size_t)bh * NS + slice) * 3;
-        qd[0] = d0;
-        qd[1] = d1;
-        qd[2] = d2;
+    float hi[GQ], lo[GQ];
+#pragma unroll
+    for (int h = 0; h < GQ; ++h) { hi[h] = 0.0f; lo[h] = 0.0f; }
+#pragma unroll
+    for (int i = 0; i < Q4; ++i) {
+#pragma unroll
+        for (int h = 0; h < GQ; ++h) {
+            float p, e, s2, e2;
+            two_prod(qs[h][quarter * Q4 + i], rv[i], p, e);
+            two_sum(hi[h], p, s2, e2);
+            hi[h] = s2;
+            lo[h] = __fadd_rn(lo[h], __fadd_rn(e, e2));
+        }
+    }
+#pragma unroll
+    for (int h = 0; h < GQ; ++h) { hi_s[h][quarter][cl] = hi[h]; lo_s[h][quarter][cl] = lo[h]; }
+    __syncthreads();
+    // warp w finishes heads w, w + 4, ...: its 32 lanes are the slice's channels
+    for (int h = quarter; h < GQ; h += 4) {
+        float hu[4], lu[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) { hu[u] = hi_s[h][u][cl]; lu[u] = lo_s[h][u][cl]; }
+        q_prep_finish<D>(hu, lu, nq2_s[h], cmax, sl2_hi, sl2_lo, bh0 + h, slice, cl, c, qb, kap, qdig);
     }
 }
 

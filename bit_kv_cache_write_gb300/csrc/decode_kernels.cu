@@ -59,6 +59,9 @@ DecodePlan plan_decode(const Shape& s, int num_sms, int batch, int max_hist, int
     // R_v^T once for them
     p.merge_per_unit = !p.fuse_merge && s.h_q / s.h_kv >= 2 && (long long)batch * s.h_q > num_sms &&
                        (size_t)(s.h_q / s.h_kv) * p.total_splits * sizeof(float) <= kMergeUnitWeightBytes;
+    // q_prep: one CTA per (query head, slice) while that grid fits about one wave of its small CTAs;
+    // beyond that one CTA per (sequence, KV head, slice) loads the R_k terms once for the g heads
+    p.qprep_per_unit = s.h_q / s.h_kv >= 2 && (long long)batch * s.h_q * (s.d / kSliceCh) > 8LL * num_sms;
     return p;
 }
 
@@ -81,6 +84,15 @@ cudaError_t launch_decode(const Shape& s, const LayerParams& prm, const DecodePl
     {
         ProfScope ps(prof, OSCAR_KERNEL_QROT, st);
         const dim3 grid(a.batch * s.h_q, s.d / kSliceCh);
+        const dim3 ugrid(a.batch * s.h_kv, s.d / kSliceCh);
+#define OSCAR_QPREP_UNIT(D_, G_)                                                                            \
+        if (plan.qprep_per_unit && s.d == D_ && g == G_)                                                    \
+            e = launch_pdl(q_prep_unit_kernel<D_, G_>, ugrid, dim3(128), 0, st, q, prm.r_k, prm.rk_colmax, qb,   \
+                           kap, qdig, s.h_kv, sl2_hi, sl2_lo, counters, 1);                                 \
+        else
+        OSCAR_QPREP_UNIT(128, 2) OSCAR_QPREP_UNIT(128, 4) OSCAR_QPREP_UNIT(128, 8)
+        OSCAR_QPREP_UNIT(64, 2) OSCAR_QPREP_UNIT(64, 4) OSCAR_QPREP_UNIT(64, 8)
+#undef OSCAR_QPREP_UNIT
         if (s.d == 128)
             e = launch_pdl(q_prep_kernel<128>, grid, dim3(128), 0, st, q, prm.r_k, prm.rk_colmax, qb, kap, qdig,
                            s.h_q, g, sl2_hi, sl2_lo, counters, 1);

@@ -165,6 +165,7 @@ struct DecodePlan {
     size_t ws_counters;     // bytes of per-(sequence, KV head) tickets of the last-CTA merge
     bool fuse_merge;        // the split kernel merges (else the merge kernel runs)
     bool merge_per_unit;    // the merge kernel takes one (sequence, KV head) per CTA (else one query head)
+    bool qprep_per_unit;    // q_prep takes one (sequence, KV head, slice) per CTA (else one query head)
     size_t ws_total;
 };
 
