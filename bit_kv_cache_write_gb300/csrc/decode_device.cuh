@@ -10,11 +10,12 @@
 //
 // Two or three launches per layer:
 //   1. q_prep: q_rot = q @ R_k for every query head, accumulated as two fp32
-//      (about 48 bits), one CTA per 32 rotated channels. It is cut into three
-//      11-bit fp16 tensor-core operands on a fixed-point grid whose exponent
-//      comes from a bound (|q| times the largest column norm of R_k), so the
-//      CTAs of one head agree on it without exchanging a maximum. Each CTA
-//      also writes the exact digit sums of its channels.
+//      (about 48 bits), one CTA per 32 rotated channels (of one query head, or of
+//      all g heads of a KV head when the per-head grid is more than about a wave).
+//      It is cut into three 11-bit fp16 tensor-core operands on a fixed-point
+//      grid whose exponent comes from a bound (|q| times the largest column norm
+//      of R_k), so the CTAs of one head agree on it without exchanging a maximum.
+//      Each CTA also writes the exact digit sums of its channels.
 //   2. split: one CTA per (split, KV head, sequence).
 //      - INT2 splits stream page blocks into shared memory, each lane copying
 //        its 16-byte chunks with cp.async, three slots of two pages per warp.
@@ -27,7 +28,10 @@
 //        group, with m in log2 units.
 //   3. merge: combines the splits of each query head, un-rotates the INT2
 //      accumulator by R_v^T and normalises. Its R_v^T terms load before it
-//      waits for the split kernel. When that merge is short (g x splits <=
+//      waits for the split kernel. One CTA takes one query head, or all g heads
+//      of a (sequence, KV head) when one CTA per head would take more than a
+//      wave; that one skips the partials of zero weight (the empty splits of
+//      shorter sequences). When that merge is short (g x splits <=
 //      128, i.e. large batches in several waves) the CTA of the split kernel
 //      that finishes a (sequence, KV head) last does it instead, found by an
 //      atomic ticket (zeroed by q_prep; nothing waits on another CTA), and
